@@ -1,0 +1,229 @@
+"""Pins for the oracle's attention (CPU only).
+
+- With every quantizer replaced by identity, the tiled online-softmax path must
+  equal textbook softmax(Q K^T s) V computed here with numpy on the full score
+  matrix (tiling, running max / sum, rescale, masks, GQA head map, ragged tiles,
+  and the smoothing identities: K-mean invariance, S = gamma(Q)gamma(K)^T + dS
+  with a row-constant remainder, P~ V_m = V_m).
+- With inputs the quantizers represent exactly, the quantized Q/K path must
+  equal textbook attention (dequantization scales and constants).
+- With constant scores (P~ = 1 everywhere) and exactly representable V, the
+  quantized P~ path must equal textbook attention (the 448 scale, delta_V,
+  the two-level 448*6 constant).
+- Loose statistical pins from the "Quantization for Attention" simulator.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import golden
+
+
+def textbook(q, k, v, causal, scale):
+    """softmax(q k^T * scale) v over the full score matrix, fp64; q [B,Hq,N,d],
+    k, v [B,Hkv,M,d]; query head h reads kv head h // (Hq/Hkv); causal masks are
+    bottom-right aligned (key j visible to query i iff j <= i + M - N)."""
+    B, Hq, N, d = q.shape
+    Hkv, M = k.shape[1], k.shape[2]
+    k = np.repeat(k, Hq // Hkv, axis=1)
+    v = np.repeat(v, Hq // Hkv, axis=1)
+    s = np.einsum("bhnd,bhmd->bhnm", q, k) * scale
+    if causal:
+        i = np.arange(N)[:, None]
+        j = np.arange(M)[None, :]
+        s = np.where(j <= i + (M - N), s, -np.inf)
+    s = s - s.max(-1, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(-1, keepdims=True)
+    return np.einsum("bhnm,bhmd->bhnd", p, v)
+
+
+def bf16_tensor(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def run_oracle(orc, shape, mode, flags, bq, bk, causal, scale, q, k, v):
+    qz = orc.quantize(shape, mode, flags & 0xFF, bq, bk, q, k, v)
+    B, Hq, _, N, _, d = shape
+    rows = np.arange(B * Hq * N)
+    out = orc.attn_rows(shape, mode, flags, bq, bk, causal, scale, q, k, v, qz, rows)
+    return out.reshape(B, Hq, N, d), qz
+
+
+def rand_qkv(B, Hq, Hkv, N, M, d, seed, koff=0.0, qoff=0.0, voff=0.0):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((B, Hq, N, d)) + qoff * r.standard_normal((B, Hq, 1, d))
+    k = r.standard_normal((B, Hkv, M, d)) + koff * r.standard_normal((B, Hkv, 1, d))
+    v = r.standard_normal((B, Hkv, M, d)) + voff * r.standard_normal((B, Hkv, 1, d))
+    return bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+
+
+SHAPES = [
+    # B, Hq, Hkv, N, M, d, bq, bk, causal
+    (1, 1, 1, 1, 1, 16, 16, 16, False),
+    (1, 2, 1, 17, 17, 16, 16, 16, True),
+    (2, 4, 2, 64, 130, 64, 128, 64, False),
+    (1, 4, 1, 130, 130, 64, 64, 16, True),
+    (1, 2, 2, 17, 64, 16, 16, 16, True),      # N < M, bottom-right causal
+    (1, 4, 4, 64, 17, 16, 16, 64, False),     # one ragged key tile
+    (1, 2, 1, 130, 64, 64, 128, 16, False),   # ragged query block
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("flags", [0, 1, 1 | 2 | 4])
+@pytest.mark.parametrize("mode", [0, 2])
+def test_identity_quantizers_equal_textbook(orc, shape, flags, mode):
+    B, Hq, Hkv, N, M, d, bq, bk, causal = shape
+    q, k, v = rand_qkv(B, Hq, Hkv, N, M, d, seed=N * 31 + M, koff=3.0, qoff=2.0, voff=2.0)
+    scale = 1.0 / math.sqrt(d)
+    got, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, flags | orc.EXACT_QK | orc.EXACT_PV,
+                        bq, bk, causal, scale, q, k, v)
+    ref = textbook(f64(q), f64(k), f64(v), causal, scale)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("shape", SHAPES[:5])
+def test_exact_attention_equals_textbook(orc, shape):
+    B, Hq, Hkv, N, M, d, bq, bk, causal = shape
+    q, k, v = rand_qkv(B, Hq, Hkv, N, M, d, seed=7)
+    rows = np.arange(B * Hq * N)
+    got = orc.attn_exact_rows((B, Hq, Hkv, N, M, d), causal, 0.125, q, k, v, rows).reshape(B, Hq, N, d)
+    ref = textbook(f64(q), f64(k), f64(v), causal, 0.125)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- exact Q/K codes
+def _int8_exact(rng, shape, blk):
+    """values c * 2^-4, integer c in [-127,127], every blk-row block holding +-127*2^-4"""
+    B, H, L, d = shape
+    c = rng.integers(-127, 128, size=shape).astype(np.float64)
+    for t0 in range(0, L, blk):
+        c[:, :, t0, 0] = 127 * rng.choice([-1, 1])
+    return c * 2.0 ** -4
+
+
+def _fp8_exact(rng, shape, blk, orc):
+    mags = orc.e4m3_decode(np.arange(127))
+    x = rng.choice(mags, size=shape) * rng.choice([-1, 1], size=shape)
+    for t0 in range(0, shape[2], blk):
+        x[:, :, t0, 0] = 448.0
+    return x * 2.0 ** -6
+
+
+def _nvfp4_exact_rows(rng, shape):
+    """each 1x16 block along d: E2M1 values times 2^e with one element at 6*2^e"""
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    x = rng.choice(mags, size=shape) * rng.choice([-1, 1], size=shape)
+    B, H, L, d = shape
+    e = rng.integers(-5, 3, size=(B, H, L, d // 16))
+    x = x.reshape(B, H, L, d // 16, 16)
+    x[..., 3] = 6.0
+    x = x * (2.0 ** e)[..., None]
+    return x.reshape(shape)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_exact_qk_codes_reproduce_textbook(orc, mode, causal):
+    rng = np.random.default_rng(3 + mode)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 1, 40, 80, 32, 16, 16
+    if mode == 0:
+        qf = _int8_exact(rng, (B, Hq, N, d), bq)
+        kf = _int8_exact(rng, (B, Hkv, M, d), bk)
+    elif mode == 1:
+        qf = _fp8_exact(rng, (B, Hq, N, d), bq, orc)
+        kf = _fp8_exact(rng, (B, Hkv, M, d), bk, orc)
+    else:
+        qf = _nvfp4_exact_rows(rng, (B, Hq, N, d))
+        kf = _nvfp4_exact_rows(rng, (B, Hkv, M, d))
+    vf = rng.standard_normal((B, Hkv, M, d))
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(q), qf) and np.array_equal(f64(k), kf)
+    scale = 0.02
+    got, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, orc.EXACT_PV, bq, bk, causal, scale, q, k, v)
+    ref = textbook(qf, kf, f64(v), causal, scale)
+    assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- exact P~ path
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_scores_exact_p_path(orc, mode, causal):
+    """All keys equal -> K - mean(K) = 0 -> S = 0 -> P~ = 1: e4m3(448*1) = 448
+    (FP8 modes) or s_P1 = 1/2688, s_P2 = 448, code 6 (NVFP4); with V exactly
+    representable the quantized output equals the mean of the visible V rows."""
+    rng = np.random.default_rng(21 + mode)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 2, 48, 96, 32, 16, 32
+    qf = rng.standard_normal((B, Hq, N, d))
+    kf = np.broadcast_to(rng.standard_normal((B, Hkv, 1, d)), (B, Hkv, M, d)).copy()
+    if mode in (0, 1):
+        mags = orc.e4m3_decode(np.arange(127))
+        vf = rng.choice(mags, size=(B, Hkv, M, d)) * rng.choice([-1, 1], size=(B, Hkv, M, d))
+        vf[:, :, 5, :] = 448.0                              # per-channel absmax 448*2^e
+        vf = vf * (2.0 ** rng.integers(-8, 0, size=(B, Hkv, 1, d)))
+    else:
+        mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+        vf = rng.choice(mags, size=(B, Hkv, M, d)) * rng.choice([-1, 1], size=(B, Hkv, M, d))
+        vf = vf.reshape(B, Hkv, M // 16, 16, d)
+        vf[:, :, :, 2, :] = 6.0                             # each 16-token block max 6*2^e
+        vf = (vf * (2.0 ** rng.integers(-4, 2, size=(B, Hkv, M // 16, 1, d)))).reshape(B, Hkv, M, d)
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(v), vf)
+    got, qz = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, orc.SMOOTH_K, bq, bk, causal, 0.1, q, k, v)
+    assert not qz.kc.any()
+    ref = textbook(qf, kf, vf, causal, 0.1)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- accuracy sanity
+# INT8 Q/K (the mode of the INT8/FP8 workloads) reaches 0.999.  The extra E4M3
+# Q/K mode carries 3 mantissa bits per operand (about 0.9987 here).  NVFP4 on
+# i.i.d. Gaussian inputs, whose attention rows are nearly flat, lands near 0.98
+# (the pages' 99.5 % is measured on real video-model tensors).
+@pytest.mark.parametrize("mode,min_cos", [(0, 0.999), (1, 0.998), (2, 0.975)])
+def test_quantized_accuracy_against_fp64(orc, mode, min_cos):
+    B, Hq, Hkv, N, M, d = 1, 2, 1, 200, 300, 64
+    q, k, v = rand_qkv(B, Hq, Hkv, N, M, d, seed=99, koff=3.0)
+    got, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, orc.SMOOTH_K, 128, 64, True, 0.125, q, k, v)
+    ref = textbook(f64(q), f64(k), f64(v), True, 0.125)
+    cos = (got * ref).sum() / np.sqrt((got ** 2).sum() * (ref ** 2).sum())
+    assert cos >= min_cos
+
+
+def test_quantize_rejects_out_of_range(orc):
+    q, k, v = rand_qkv(1, 1, 1, 16, 16, 16, seed=1)
+    k[0, 0, 3, 3] = 70000.0
+    with pytest.raises(orc.OracleError):
+        orc.quantize((1, 1, 1, 16, 16, 16), 0, 1, 16, 16, q, k, v)
+
+
+@pytest.mark.slow
+def test_simulator_statistics(orc):
+    """K smoothing roughly halves the relative L1 of per-block INT8 Q/K
+    (about 2.5 % -> 1.3 %) on the simulator's synthetic recipe."""
+    g = golden("p5_simulator.txt")
+    B, H, N, d = 1, 8, 1024, 128
+    r = np.random.default_rng(0)
+    qf, kf, vf = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    kf[..., 7] += 8.0
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    shape = (B, H, H, N, N, d)
+    heads = [0, 3]
+    rows = np.concatenate([np.arange(h * N, (h + 1) * N) for h in heads])
+    ref = orc.attn_exact_rows(shape, False, 1 / math.sqrt(d), q, k, v, rows)
+    rel = {}
+    for flags in (0, orc.SMOOTH_K):
+        qz = orc.quantize(shape, 0, flags, 64, 64, q, k, v)
+        out = orc.parallel_attn_rows(shape, 0, flags | orc.EXACT_PV, 64, 64, False, 1 / math.sqrt(d),
+                                     q, k, v, qz, rows)
+        rel[flags] = np.abs(out - ref).sum() / np.abs(ref).sum()
+    assert 0.5 * g["rel_l1_no_smooth"] < rel[0] < 2.0 * g["rel_l1_no_smooth"]
+    assert 0.5 * g["rel_l1_smooth_k"] < rel[orc.SMOOTH_K] < 2.0 * g["rel_l1_smooth_k"]
+    assert rel[orc.SMOOTH_K] < 0.75 * rel[0]
