@@ -1,0 +1,182 @@
+"""ctypes binding of libsage.so with the C ABI's names (include/sage.h).
+
+Argument marshalling only: torch supplies device memory and the current
+stream; every step of the path runs in the library's CUDA kernels.  There is
+no fallback: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsage.so")
+
+SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4 = 0, 1, 2
+SAGE_SMOOTH_K, SAGE_SMOOTH_Q, SAGE_SMOOTH_V = 1, 2, 4
+STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3: "SAGE_ERR_WORKSPACE",
+          4: "SAGE_ERR_RANGE", 5: "SAGE_ERR_TIMEOUT", 6: "SAGE_ERR_CUDA"}
+
+EXPORTS = ["sage_workspace_bytes", "sage_workspace_layout", "sage_quantize_qkv", "sage_attn_fwd",
+           "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str"]
+
+
+class SageError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, STATUS.get(code, code)))
+
+
+class Shape(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("B", "Hq", "Hkv", "N", "M", "d")]
+
+
+class WsLayout(C.Structure):
+    _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
+                                          "qsf", "ksf", "vsf", "stats", "status", "total")] + \
+               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libsage.so is not built (run __graft_entry__.build() or "
+                          "python -m bit_quantized_attention_gb300.build); there is no fallback path")
+    L = C.CDLL(LIB_PATH)
+    P, vp, sz, i32, f32 = C.POINTER, C.c_void_p, C.c_size_t, C.c_int, C.c_float
+    L.sage_workspace_bytes.argtypes, L.sage_workspace_bytes.restype = [P(Shape), i32, i32, i32], sz
+    L.sage_workspace_layout.argtypes, L.sage_workspace_layout.restype = [P(Shape), i32, i32, i32, P(WsLayout)], i32
+    L.sage_quantize_qkv.argtypes = [P(Shape), i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.sage_quantize_qkv.restype = i32
+    L.sage_attn_fwd.argtypes = [P(Shape), i32, f32, i32, i32, i32, i32, vp, sz, vp, vp]
+    L.sage_attn_fwd.restype = i32
+    L.sage_host_buffer_bytes.argtypes, L.sage_host_buffer_bytes.restype = [P(Shape), i32, i32, i32], sz
+    L.sage_attn_host.argtypes = [P(Shape), i32, f32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    L.sage_attn_host.restype = i32
+    L.sage_read_status.argtypes = [P(Shape), i32, i32, i32, vp, P(i32), P(i32)]
+    L.sage_read_status.restype = i32
+    L.sage_status_str.argtypes, L.sage_status_str.restype = [i32], C.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise SageError(rc, where)
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor) -> C.c_void_p:
+    return C.c_void_p(t.data_ptr())
+
+
+def _bf16_cuda(t: torch.Tensor, name: str):
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+        raise ValueError("%s must be a contiguous 4-D bf16 CUDA tensor" % name)
+
+
+def shape_of(q: torch.Tensor, k: torch.Tensor) -> Shape:
+    B, Hq, N, d = q.shape
+    Bk, Hkv, M, dk = k.shape
+    if B != Bk or d != dk:
+        raise ValueError("q and k disagree on batch or head dim")
+    return Shape(B, Hq, Hkv, N, M, d)
+
+
+def sage_workspace_layout(shape: Shape, mode: int, bq: int, bk: int) -> WsLayout:
+    L = WsLayout()
+    _check(lib.sage_workspace_layout(C.byref(shape), mode, bq, bk, C.byref(L)), "sage_workspace_layout")
+    return L
+
+
+def sage_workspace_bytes(shape: Shape, mode: int, bq: int, bk: int) -> int:
+    return int(lib.sage_workspace_bytes(C.byref(shape), mode, bq, bk))
+
+
+@dataclass
+class Workspace:
+    """A caller-owned device workspace for one (shape, mode, bq, bk, flags)."""
+    buf: torch.Tensor
+    shape: Shape
+    mode: int
+    flags: int
+    bq: int
+    bk: int
+    layout: WsLayout
+
+    def region(self, name: str, nbytes: int) -> torch.Tensor:
+        off = getattr(self.layout, name)
+        return self.buf[off:off + nbytes]
+
+
+def new_workspace(shape: Shape, mode: int, flags: int, bq: int = 128, bk: int = 64, device=None) -> Workspace:
+    L = sage_workspace_layout(shape, mode, bq, bk)
+    buf = torch.empty(L.total + 1024, dtype=torch.uint8, device=device or "cuda")
+    off = (-buf.data_ptr()) % 1024  # the library wants a 1024-byte aligned base
+    return Workspace(buf[off:off + L.total], shape, mode, flags, bq, bk, L)
+
+
+def sage_quantize_qkv(q, k, v, mode: int, flags: int, bq: int = 128, bk: int = 64, workspace=None,
+                      stream=None) -> Workspace:
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _bf16_cuda(t, n)
+    shape = shape_of(q, k)
+    ws = workspace or new_workspace(shape, mode, flags, bq, bk, q.device)
+    ws.flags = flags
+    _check(lib.sage_quantize_qkv(C.byref(shape), mode, flags, bq, bk, _ptr(q), _ptr(k), _ptr(v), _ptr(ws.buf),
+                                 ws.buf.numel(), _stream(stream)), "sage_quantize_qkv")
+    return ws
+
+
+def sage_attn_fwd(ws: Workspace, causal: bool, sm_scale: float, out=None, stream=None) -> torch.Tensor:
+    s = ws.shape
+    if out is None:
+        out = torch.empty((s.B, s.Hq, s.N, s.d), dtype=torch.bfloat16, device=ws.buf.device)
+    _check(lib.sage_attn_fwd(C.byref(s), int(bool(causal)), float(sm_scale), ws.mode, ws.flags, ws.bq, ws.bk,
+                             _ptr(ws.buf), ws.buf.numel(), _ptr(out), _stream(stream)), "sage_attn_fwd")
+    return out
+
+
+def sage_read_status(ws: Workspace):
+    code, site = C.c_int(0), C.c_int(0)
+    _check(lib.sage_read_status(C.byref(ws.shape), ws.mode, ws.bq, ws.bk, _ptr(ws.buf), C.byref(code),
+                                C.byref(site)), "sage_read_status")
+    return code.value, site.value
+
+
+def sage_host_buffer_bytes(shape: Shape, mode: int, bq: int, bk: int) -> int:
+    return int(lib.sage_host_buffer_bytes(C.byref(shape), mode, bq, bk))
+
+
+def sage_attn_host(shape: Shape, causal: bool, sm_scale: float, mode: int, flags: int, bq: int, bk: int,
+                   q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor, o_host: torch.Tensor,
+                   dev_buf: torch.Tensor, stream=None):
+    """End-to-end call on host tensors (pinned for asynchronous copies)."""
+    if (dev_buf.data_ptr() % 1024) != 0:
+        raise ValueError("dev_buf must be 1024-byte aligned")
+    _check(lib.sage_attn_host(C.byref(shape), int(bool(causal)), float(sm_scale), mode, flags, bq, bk,
+                              _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(dev_buf),
+                              dev_buf.numel(), _stream(stream)), "sage_attn_host")
+
+
+def sage_status_str(code: int) -> str:
+    return lib.sage_status_str(code).decode()
+
+
+def sage_attn(q, k, v, causal: bool, sm_scale: float, mode: int = SAGE_Q8_PV8, flags: int = SAGE_SMOOTH_K,
+              bq: int = 128, bk: int = 64, stream=None) -> torch.Tensor:
+    """Quantize + attend: the two library calls in order on one stream."""
+    ws = sage_quantize_qkv(q, k, v, mode, flags, bq, bk, stream=stream)
+    return sage_attn_fwd(ws, causal, sm_scale, stream=stream)

@@ -1,0 +1,171 @@
+// C ABI entry points (declared in include/sage.h): argument checks, workspace
+// layout, TMA descriptors and dispatch to the kernel launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "layout.h"
+#include "launch.h"
+
+using namespace sage;
+
+namespace sage {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  });
+  return fn;
+}
+
+sage_status make_tmap_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t pitch,
+                         uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return SAGE_ERR_CUDA;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
+long long spin_limit_cycles() {
+  // about two seconds at GB300 clocks unless SAGE_SPIN_LIMIT (cycles) says otherwise
+  static long long v = [] {
+    const char *e = getenv("SAGE_SPIN_LIMIT");
+    long long x = e ? atoll(e) : 0;
+    return x > 0 ? x : 4000000000LL;
+  }();
+  return v;
+}
+
+}  // namespace sage
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+extern "C" {
+
+size_t sage_workspace_bytes(const sage_shape *shape, int quant_mode, int bq, int bk) {
+  sage_ws_layout L;
+  if (compute_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  return L.total;
+}
+
+sage_status sage_workspace_layout(const sage_shape *shape, int quant_mode, int bq, int bk, sage_ws_layout *out) {
+  if (!out) return SAGE_ERR_INVALID_ARG;
+  return compute_layout(shape, quant_mode, bq, bk, out);
+}
+
+sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags, int bq, int bk, const void *q,
+                              const void *k, const void *v, void *workspace, size_t workspace_bytes,
+                              sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  return launch_quantize_q8(*shape, quant_mode, flags, bq, bk, q, k, v, workspace, L, (cudaStream_t)stream);
+}
+
+sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
+                          int bk, const void *workspace, size_t workspace_bytes, void *o, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if (!workspace || !o || !aligned16(o) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
+  if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
+  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  return launch_attn_q8(*shape, causal, sm_scale, quant_mode, flags, bk, workspace, L, o, (cudaStream_t)stream);
+}
+
+static size_t io_bytes(const sage_shape *s) {
+  const size_t qn = (size_t)s->B * s->Hq * s->N * s->d * 2, kn = (size_t)s->B * s->Hkv * s->M * s->d * 2;
+  return align_up(qn, 1024) * 2 + align_up(kn, 1024) * 2;  // q, o, k, v
+}
+
+size_t sage_host_buffer_bytes(const sage_shape *shape, int quant_mode, int bq, int bk) {
+  sage_ws_layout L;
+  if (compute_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  return L.total + io_bytes(shape);
+}
+
+sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
+                           int bk, const void *q_host, const void *k_host, const void *v_host, void *o_host,
+                           void *dev_buf, size_t dev_bytes, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (!q_host || !k_host || !v_host || !o_host || !dev_buf) return SAGE_ERR_INVALID_ARG;
+  if (((uintptr_t)dev_buf & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (dev_bytes < L.total + io_bytes(shape)) return SAGE_ERR_WORKSPACE;
+  const size_t qn = (size_t)shape->B * shape->Hq * shape->N * shape->d * 2;
+  const size_t kn = (size_t)shape->B * shape->Hkv * shape->M * shape->d * 2;
+  char *ws = (char *)dev_buf;
+  char *dq = ws + L.total;
+  char *dk = dq + align_up(qn, 1024);
+  char *dv = dk + align_up(kn, 1024);
+  char *dO = dv + align_up(kn, 1024);
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(dq, q_host, qn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
+  if (cudaMemcpyAsync(dk, k_host, kn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
+  if (cudaMemcpyAsync(dv, v_host, kn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
+  st = sage_quantize_qkv(shape, quant_mode, flags, bq, bk, dq, dk, dv, ws, L.total, stream);
+  if (st != SAGE_OK) return st;
+  st = sage_attn_fwd(shape, causal, sm_scale, quant_mode, flags, bq, bk, ws, L.total, dO, stream);
+  if (st != SAGE_OK) return st;
+  if (cudaMemcpyAsync(o_host, dO, qn, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return SAGE_ERR_CUDA;
+  return SAGE_OK;
+}
+
+sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,
+                             int *code, int *site) {
+  sage_ws_layout L;
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (!workspace || !code || !site) return SAGE_ERR_INVALID_ARG;
+  int buf[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(buf, (const char *)workspace + L.status, sizeof(buf), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SAGE_ERR_CUDA;
+  *code = buf[0];
+  *site = buf[1];
+  return SAGE_OK;
+}
+
+const char *sage_status_str(sage_status s) {
+  switch (s) {
+    case SAGE_OK: return "ok";
+    case SAGE_ERR_INVALID_ARG: return "invalid argument";
+    case SAGE_ERR_UNSUPPORTED: return "unsupported request";
+    case SAGE_ERR_WORKSPACE: return "workspace too small";
+    case SAGE_ERR_RANGE: return "input out of range (non-finite or |x| >= 2^16)";
+    case SAGE_ERR_TIMEOUT: return "bounded wait gave up on the device";
+    case SAGE_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

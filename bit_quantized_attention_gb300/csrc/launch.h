@@ -1,0 +1,27 @@
+// Kernel launchers behind the C ABI (host declarations).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sage.h"
+
+namespace sage {
+
+// Pre-pass for SAGE_Q8_PV8 / SAGE_QF8_PV8 (quantize.cu).
+sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
+                               const void *k, const void *v, void *ws, const sage_ws_layout &L,
+                               cudaStream_t stream);
+
+// Attention for SAGE_Q8_PV8 / SAGE_QF8_PV8 (attn_q8.cu).
+sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
+                           const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (api.cu).
+// A 2-D byte tensor [rows][cols] with row pitch `pitch` bytes, box {box_cols, box_rows}.
+sage_status make_tmap_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t pitch,
+                         uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
+
+// Spin limit (clock cycles) for bounded waits inside kernels.
+long long spin_limit_cycles();
+
+}  // namespace sage

@@ -1,0 +1,97 @@
+// Workspace layout and argument checks shared by the entry points and the
+// kernel launchers (host code).
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sage.h"
+
+namespace sage {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kMaxTokens = 1 << 23;  // fixed-point means stay exact in int64 up to here
+
+// Statistics scratch of the quantize pre-pass, per (b, kv-head) and channel:
+// K column sums and V column sums as fixed-point int64 (lsb 2^-24), V column
+// min and max as order-preserving int32 encodings of the fp32 values.
+struct StatsView {
+  int64_t *ksum;  // [B*Hkv, d]
+  int64_t *vsum;  // [B*Hkv, d]
+  int *vmin;      // [B*Hkv, d]
+  int *vmax;      // [B*Hkv, d]
+};
+
+inline size_t stats_bytes(const sage_shape &s) {
+  const size_t n = (size_t)s.B * s.Hkv * s.d;
+  return n * (8 + 8 + 4 + 4);
+}
+
+// Argument checks common to every entry point.  Returns SAGE_OK or the reason.
+inline sage_status check_request(const sage_shape *s, int mode, int bq, int bk) {
+  if (!s) return SAGE_ERR_INVALID_ARG;
+  if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->N <= 0 || s->M <= 0 || s->d <= 0)
+    return SAGE_ERR_INVALID_ARG;
+  if (s->Hq % s->Hkv != 0) return SAGE_ERR_INVALID_ARG;
+  if (mode < SAGE_Q8_PV8 || mode > SAGE_NVFP4) return SAGE_ERR_INVALID_ARG;
+  if (bq <= 0 || bk <= 0) return SAGE_ERR_INVALID_ARG;
+  if (s->N > kMaxTokens || s->M > kMaxTokens) return SAGE_ERR_UNSUPPORTED;
+  if (s->d != 64 && s->d != 128) return SAGE_ERR_UNSUPPORTED;
+  if (bq != 128) return SAGE_ERR_UNSUPPORTED;
+  if (bk != 64 && bk != 128) return SAGE_ERR_UNSUPPORTED;
+  if ((int64_t)s->B * s->Hq > (1 << 20) || (int64_t)s->B * s->Hkv > (1 << 20)) return SAGE_ERR_UNSUPPORTED;
+  return SAGE_OK;
+}
+
+inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk, sage_ws_layout *L) {
+  sage_status st = check_request(s, mode, bq, bk);
+  if (st != SAGE_OK) return st;
+  const int64_t B = s->B, Hq = s->Hq, Hkv = s->Hkv, d = s->d;
+  const int64_t N_pad = align_up((size_t)s->N, 128), M_pad = align_up((size_t)s->M, 128);
+  const int64_t Tm = N_pad / bq, Tn = cdiv(s->M, bk);
+  // bytes per stored code: fp16 integer (mode 0), E4M3 byte (1), packed E2M1 (2)
+  const double code_bytes = (mode == SAGE_Q8_PV8) ? 2.0 : (mode == SAGE_QF8_PV8 ? 1.0 : 0.5);
+  const double v_bytes = (mode == SAGE_NVFP4) ? 0.5 : 1.0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + (bytes ? bytes : 1), 1024);
+    return o;
+  };
+  L->qhat = take((size_t)(B * Hq * N_pad * d * code_bytes));
+  L->dq = take((size_t)(B * Hq * Tm * 4));
+  L->qbar = take((size_t)(B * Hq * Tm * d * 4));
+  L->khat = take((size_t)(B * Hkv * M_pad * d * code_bytes));
+  L->dk = take((size_t)(B * Hkv * Tn * 4));
+  L->kbar = take((size_t)(B * Hkv * d * 4));
+  L->vhat = take((size_t)(B * Hkv * d * M_pad * v_bytes));
+  L->dv = take((size_t)(B * Hkv * d * 4));
+  L->vm = take((size_t)(B * Hkv * d * 4));
+  // NVFP4 block scales: one E4M3 byte per 16 codes
+  const bool fp4 = (mode == SAGE_NVFP4);
+  L->qsf = take(fp4 ? (size_t)(B * Hq * N_pad * (d / 16)) : 0);
+  L->ksf = take(fp4 ? (size_t)(B * Hkv * M_pad * (d / 16)) : 0);
+  L->vsf = take(fp4 ? (size_t)(B * Hkv * d * (M_pad / 16)) : 0);
+  L->stats = take(stats_bytes(*s));
+  L->status = take(16);
+  L->total = off;
+  L->N_pad = (int)N_pad;
+  L->M_pad = (int)M_pad;
+  L->Tm = (int)Tm;
+  L->Tn = (int)Tn;
+  return SAGE_OK;
+}
+
+inline StatsView stats_view(void *ws, const sage_ws_layout &L, const sage_shape &s) {
+  const size_t n = (size_t)s.B * s.Hkv * s.d;
+  char *base = (char *)ws + L.stats;
+  StatsView v;
+  v.ksum = (int64_t *)base;
+  v.vsum = (int64_t *)(base + n * 8);
+  v.vmin = (int *)(base + n * 16);
+  v.vmax = (int *)(base + n * 20);
+  return v;
+}
+
+}  // namespace sage

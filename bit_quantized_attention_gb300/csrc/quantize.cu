@@ -1,0 +1,442 @@
+// Smoothing + quantization pre-pass for the INT8 / FP8 modes.
+//
+// What it computes (SageAttention2 Technical Report summary, §3.2 item 1 and
+// §3.4 "Smoothing Q" / "FP8 Quantization for P~V" / "Optional Smoothing of V";
+// SageAttention3 summary §3.4 "SageBwd Forward Pass" for the per-block INT8
+// quantizer):
+//   k_bar = mean over tokens of K, gamma(K) = K - k_bar     (if SMOOTH_K)
+//   per K block j of bk tokens: delta_K = max|gamma(K_j)| / 127, K^ = round(gamma/delta_K)
+//   q_bar_i = mean of the block's rows, gamma(Q_i) = Q_i - q_bar_i (if SMOOTH_Q)
+//   per Q block i of 128 rows: delta_Q = max|gamma(Q_i)| / 127, Q^ = round(gamma/delta_Q)
+//   V_m = mean over tokens of V (if SMOOTH_V), V' = V - V_m
+//   per channel c: delta_V[c] = max_t |V'[t,c]| / 448, V^ = e4m3(V' / delta_V)
+// (FP8 Q/K mode: / 448 and E4M3 codes instead of / 127 and integers.)
+//
+// Every arithmetic step is one IEEE binary32 (or binary64 for the mean)
+// operation with round-to-nearest-even, issued through the _rn intrinsics, so
+// the results are a fixed function of the inputs:
+//   - means use an exact integer sum of the values in fixed point (lsb 2^-24,
+//     truncated toward zero), converted once to double and divided once;
+//     integer addition is associative, so any reduction order gives the same
+//     bits;
+//   - the V per-channel absmax after subtracting V_m is taken from the channel
+//     min and max (rounded subtraction is monotone, so
+//     max_t |fl(v_t - m)| = max(|fl(max v - m)|, |fl(min v - m)|)), which lets
+//     one statistics pass carry everything the quantize pass needs.
+//
+// Launches: init (clear stats + status), stats (K/V column sums, V min/max),
+// quantize (Q blocks, K blocks, V token chunks in one grid).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.h"
+#include "launch.h"
+#include "sm103.cuh"
+
+namespace sage {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kStatTokens = 256;  // tokens per statistics CTA
+
+__device__ __forceinline__ int order_key(float f) {
+  int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float order_val(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
+
+__device__ __forceinline__ bool in_range(float f) { return fabsf(f) < 65536.0f; }  // false for NaN too
+
+__device__ __forceinline__ long long fixed24(float f) { return __float2ll_rz(__fmul_rn(f, 16777216.0f)); }
+
+__device__ __forceinline__ float mean_from_sum(long long sum, int n) {
+  return __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(sum), 0x1p-24), (double)n));
+}
+
+__device__ __forceinline__ void raise_status(int *status, int code, int site) {
+  if (atomicCAS(status, 0, code) == 0) status[1] = site;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// block-wide max of non-negative floats (all threads get the result)
+__device__ float block_max(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kThreads / 32; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+// ------------------------------------------------------------------ init
+__global__ void init_kernel(StatsView st, int n, int *status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    st.ksum[i] = 0;
+    st.vsum[i] = 0;
+    st.vmin[i] = order_key(__int_as_float(0x7F800000));   // +inf
+    st.vmax[i] = order_key(__int_as_float(0xFF800000));   // -inf
+  }
+  if (i < 4) status[i] = 0;
+}
+
+// ------------------------------------------------------------------ stats
+// grid (ceil(M / kStatTokens), B*Hkv).  Column sums of K and V (fixed point),
+// column min / max of V, range check of K and V.
+template <int D>
+__global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                         int M, StatsView st, int *status) {
+  constexpr int VPR = D / 8;               // 16-byte vectors per row
+  constexpr int RPP = kThreads / VPR;      // rows per pass
+  __shared__ long long sk[RPP][D];
+  __shared__ long long sv[RPP][D];
+  __shared__ int smin[RPP][D];
+  __shared__ int smax[RPP][D];
+  const int hb = blockIdx.y;
+  const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  const int t0 = blockIdx.x * kStatTokens;
+  long long ks[8], vs[8];
+  float vmn[8], vmx[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ks[e] = 0;
+    vs[e] = 0;
+    vmn[e] = __int_as_float(0x7F800000);
+    vmx[e] = __int_as_float(0xFF800000);
+  }
+  bool bad_k = false, bad_v = false;
+  for (int t = t0 + rr; t < min(M, t0 + kStatTokens); t += RPP) {
+    const size_t off = ((size_t)hb * M + t) * VPR + vc;
+    float fk[8], fv[8];
+    unpack_bf16x8(k[off], fk);
+    unpack_bf16x8(v[off], fv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bad_k |= !in_range(fk[e]);
+      bad_v |= !in_range(fv[e]);
+      ks[e] += fixed24(fk[e]);
+      vs[e] += fixed24(fv[e]);
+      vmn[e] = fminf(vmn[e], fv[e]);
+      vmx[e] = fmaxf(vmx[e], fv[e]);
+    }
+  }
+  if (bad_k) raise_status(status, SAGE_ERR_RANGE, 1);
+  if (bad_v) raise_status(status, SAGE_ERR_RANGE, 2);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sk[rr][vc * 8 + e] = ks[e];
+    sv[rr][vc * 8 + e] = vs[e];
+    smin[rr][vc * 8 + e] = order_key(vmn[e]);
+    smax[rr][vc * 8 + e] = order_key(vmx[e]);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += kThreads) {
+    long long a = 0, b = 0;
+    int mn = smin[0][c], mx = smax[0][c];
+    for (int r = 0; r < RPP; ++r) {
+      a += sk[r][c];
+      b += sv[r][c];
+      mn = min(mn, smin[r][c]);
+      mx = max(mx, smax[r][c]);
+    }
+    const size_t i = (size_t)hb * D + c;
+    atomicAdd((unsigned long long *)&st.ksum[i], (unsigned long long)a);
+    atomicAdd((unsigned long long *)&st.vsum[i], (unsigned long long)b);
+    atomicMin(&st.vmin[i], mn);
+    atomicMax(&st.vmax[i], mx);
+  }
+}
+
+// ------------------------------------------------------------------ quantize
+struct QuantArgs {
+  const uint4 *q, *k, *v;  // bf16 inputs, as 16-byte vectors
+  int B, Hq, Hkv, N, M, N_pad, M_pad, Tm, Tn, bk;
+  int mode, flags;
+  uint8_t *qhat, *khat, *vhat;
+  float *dq, *qbar, *dk, *kbar, *dv, *vm;
+  StatsView st;
+  int *status;
+  int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
+};
+
+// Codes of 8 smoothed values with scale delta: 8 fp16 integers (INT8 mode,
+// 16 bytes) or 8 E4M3 bytes (FP8 mode).
+template <bool kInt8>
+__device__ __forceinline__ void encode8(const float (&g)[8], float delta, bool valid, uint8_t *dst) {
+  if (kInt8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float c0 = 0.0f, c1 = 0.0f;
+      if (valid && delta != 0.0f) {
+        c0 = fminf(fmaxf(rintf(__fdiv_rn(g[2 * i], delta)), -127.0f), 127.0f);
+        c1 = fminf(fmaxf(rintf(__fdiv_rn(g[2 * i + 1], delta)), -127.0f), 127.0f);
+      }
+      const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
+      w[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid && delta != 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e] = __fdiv_rn(g[4 * i + e], delta);
+      }
+      w[i] = (uint32_t)cvt_e4m3x2(c[0], c[1]) | ((uint32_t)cvt_e4m3x2(c[2], c[3]) << 16);
+    }
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+  }
+}
+
+// One block of `rows` rows (<= 128) of a [*, D] bf16 matrix: optional
+// per-block mean (fixed point over the valid rows) or a given mean, then the
+// per-block absmax scale and the codes.  Rows past `valid_rows` get code 0.
+template <int D, bool kInt8>
+__device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
+                            const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
+                            float *mean_out, int *status, int site) {
+  constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
+  __shared__ long long ssum[RPP][D];
+  __shared__ float smean[D];
+  __shared__ float red[kThreads / 32];
+  const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  uint4 x[PASSES];
+  bool bad = false;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int r = rr + p * RPP;
+    x[p] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+  }
+  if (own_mean) {
+    long long s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      if (rr + p * RPP >= valid_rows) continue;
+      float f[8];
+      unpack_bf16x8(x[p], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bad |= !in_range(f[e]);
+        s[e] += fixed24(f[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ssum[rr][vc * 8 + e] = s[e];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+      long long a = 0;
+      for (int r = 0; r < RPP; ++r) a += ssum[r][c];
+      smean[c] = mean_from_sum(a, valid_rows);
+    }
+  } else {
+    for (int c = threadIdx.x; c < D; c += kThreads) smean[c] = given_mean ? given_mean[c] : 0.0f;
+  }
+  __syncthreads();
+  float mu[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mu[e] = smean[vc * 8 + e];
+  float amax = 0.0f;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    if (rr + p * RPP >= valid_rows) continue;
+    float f[8];
+    unpack_bf16x8(x[p], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bad |= !in_range(f[e]);
+      amax = fmaxf(amax, fabsf(__fsub_rn(f[e], mu[e])));
+    }
+  }
+  if (bad) raise_status(status, SAGE_ERR_RANGE, site);
+  amax = block_max(amax, red);
+  const float delta = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
+  constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int r = rr + p * RPP;
+    if (r >= rows) continue;
+    float f[8], g[8];
+    unpack_bf16x8(x[p], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __fsub_rn(f[e], mu[e]);
+    encode8<kInt8>(g, delta, r < valid_rows, dst + ((size_t)r * D + vc * 8) * CB);
+  }
+  if (threadIdx.x == 0) *delta_out = delta;
+  if (mean_out)
+    for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
+}
+
+template <int D, bool kInt8>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
+  constexpr int CB = kInt8 ? 2 : 1;
+  int cta = blockIdx.x;
+  if (cta < a.nq) {
+    // ---- Q block (b, h, i)
+    const int i = cta % a.Tm, bh = cta / a.Tm;
+    const int r0 = i * 128;
+    const int valid = max(0, min(128, a.N - r0));
+    const bool smooth = (a.flags & SAGE_SMOOTH_Q) != 0;
+    float *qbar = a.qbar + ((size_t)bh * a.Tm + i) * D;
+    quant_block<D, kInt8>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0, nullptr,
+                          a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i, qbar,
+                          a.status, 3);
+    return;
+  }
+  cta -= a.nq;
+  if (cta < a.nk) {
+    // ---- K block (b, g, j): mean over all tokens from the statistics pass
+    const int j = cta % a.Tn, hb = cta / a.Tn;
+    __shared__ float kmean[D];
+    const bool smooth = (a.flags & SAGE_SMOOTH_K) != 0;
+    for (int c = threadIdx.x; c < D; c += kThreads)
+      kmean[c] = smooth ? mean_from_sum(a.st.ksum[(size_t)hb * D + c], a.M) : 0.0f;
+    __syncthreads();
+    if (j == 0)
+      for (int c = threadIdx.x; c < D; c += kThreads) a.kbar[(size_t)hb * D + c] = kmean[c];
+    const int t0 = j * a.bk;
+    const int valid = max(0, min(a.bk, a.M - t0));
+    quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, kmean,
+                          a.khat + ((size_t)hb * a.M_pad + t0) * D * CB, a.dk + (size_t)hb * a.Tn + j, nullptr,
+                          a.status, 1);
+    return;
+  }
+  cta -= a.nk;
+  // ---- V token chunk (b, g, 128 tokens): per-channel scales from the stats,
+  // E4M3 codes written transposed (token-contiguous per channel).
+  {
+    const int nchunk = a.M_pad / 128;
+    const int ch = cta % nchunk, hb = cta / nchunk;
+    __shared__ float vmean[D], vinv[D];
+    __shared__ uint8_t tile[D][128 + 16];
+    const bool smooth = (a.flags & SAGE_SMOOTH_V) != 0;
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+      const size_t i = (size_t)hb * D + c;
+      const float mu = smooth ? mean_from_sum(a.st.vsum[i], a.M) : 0.0f;
+      const float hi = order_val(a.st.vmax[i]), lo = order_val(a.st.vmin[i]);
+      const float amax = fmaxf(fabsf(__fsub_rn(hi, mu)), fabsf(__fsub_rn(lo, mu)));
+      const float delta = __fdiv_rn(amax, 448.0f);
+      vmean[c] = mu;
+      vinv[c] = delta;
+      if (ch == 0) {
+        a.vm[i] = mu;
+        a.dv[i] = delta;
+      }
+    }
+    __syncthreads();
+    constexpr int VPR = D / 8, RPP = kThreads / VPR;
+    const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+    const int t0 = ch * 128;
+    for (int r = rr; r < 128; r += RPP) {
+      const int t = t0 + r;
+      float f[8];
+      if (t < a.M)
+        unpack_bf16x8(a.v[((size_t)hb * a.M + t) * VPR + vc], f);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int c = vc * 8 + e;
+        float c0 = 0.0f, c1 = 0.0f;
+        if (t < a.M) {
+          if (vinv[c] != 0.0f) c0 = __fdiv_rn(__fsub_rn(f[e], vmean[c]), vinv[c]);
+          if (vinv[c + 1] != 0.0f) c1 = __fdiv_rn(__fsub_rn(f[e + 1], vmean[c + 1]), vinv[c + 1]);
+        }
+        const uint16_t p = cvt_e4m3x2(c0, c1);
+        tile[c][r] = (uint8_t)(p & 0xFF);
+        tile[c + 1][r] = (uint8_t)(p >> 8);
+      }
+    }
+    __syncthreads();
+    // coalesced store: each channel row of 128 tokens is 128 contiguous bytes
+    for (int idx = threadIdx.x; idx < D * 8; idx += kThreads) {
+      const int c = idx / 8, part = idx % 8;
+      uint4 w;
+      const uint8_t *s = &tile[c][part * 16];
+      w.x = s[0] | (s[1] << 8) | (s[2] << 16) | ((uint32_t)s[3] << 24);
+      w.y = s[4] | (s[5] << 8) | (s[6] << 16) | ((uint32_t)s[7] << 24);
+      w.z = s[8] | (s[9] << 8) | (s[10] << 16) | ((uint32_t)s[11] << 24);
+      w.w = s[12] | (s[13] << 8) | (s[14] << 16) | ((uint32_t)s[15] << 24);
+      *reinterpret_cast<uint4 *>(a.vhat + ((size_t)hb * D + c) * a.M_pad + t0 + part * 16) = w;
+    }
+  }
+}
+
+}  // namespace
+
+sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
+                               const void *k, const void *v, void *ws, const sage_ws_layout &L,
+                               cudaStream_t stream) {
+  (void)bq;
+  char *w = (char *)ws;
+  StatsView st = stats_view(ws, L, s);
+  int *status = (int *)(w + L.status);
+  const int n = s.B * s.Hkv * s.d;
+  init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
+  dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
+  if (s.d == 64)
+    stats_kernel<64><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+  else
+    stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+
+  QuantArgs a;
+  a.q = (const uint4 *)q;
+  a.k = (const uint4 *)k;
+  a.v = (const uint4 *)v;
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.N = s.N;
+  a.M = s.M;
+  a.N_pad = L.N_pad;
+  a.M_pad = L.M_pad;
+  a.Tm = L.Tm;
+  a.Tn = L.Tn;
+  a.bk = bk;
+  a.mode = mode;
+  a.flags = flags;
+  a.qhat = (uint8_t *)(w + L.qhat);
+  a.khat = (uint8_t *)(w + L.khat);
+  a.vhat = (uint8_t *)(w + L.vhat);
+  a.dq = (float *)(w + L.dq);
+  a.qbar = (float *)(w + L.qbar);
+  a.dk = (float *)(w + L.dk);
+  a.kbar = (float *)(w + L.kbar);
+  a.dv = (float *)(w + L.dv);
+  a.vm = (float *)(w + L.vm);
+  a.st = st;
+  a.status = status;
+  a.nq = s.B * s.Hq * L.Tm;
+  a.nk = s.B * s.Hkv * L.Tn;
+  const int nv = s.B * s.Hkv * (L.M_pad / 128);
+  const unsigned grid = (unsigned)(a.nq + a.nk + nv);
+  const bool i8 = (mode == SAGE_Q8_PV8);
+  if (s.d == 64) {
+    if (i8)
+      quantize_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
+    else
+      quantize_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
+  } else {
+    if (i8)
+      quantize_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
+    else
+      quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
+}  // namespace sage

@@ -1,0 +1,150 @@
+/*
+ * sage.h — C ABI of the GB300 (sm_103a) quantized attention forward.
+ *
+ * The operation (SageAttention2 Technical Report summary, arXiv 2411.10958,
+ * §3.2 "Big-Picture Architecture" and §3.4 "The Complete Algorithm";
+ * SageAttention3 summary, arXiv 2505.11594, §3.4 "FP4 Attention Kernel
+ * Algorithm"):
+ *
+ *   O = softmax(Q K^T * sm_scale) V
+ *
+ * computed tile by tile without materialising the N x M score matrix, with
+ *   - K smoothing: K <- K - mean over tokens of K (exact under softmax);
+ *   - optional Q smoothing: gamma(Q_i) = Q_i - mean(Q_i) per query block, and
+ *     dS_ij = q_bar_i deq(K^_j)^T added back to the scores;
+ *   - optional V smoothing: V' = V - V_m, O = O' + V_m;
+ *   - Q/K quantized per block (INT8, or FP8 E4M3) or NVFP4 (E2M1 in 1x16 blocks
+ *     with E4M3 scales);
+ *   - P~ quantized to FP8 E4M3 with the static scale 1/448 and V per channel to
+ *     FP8 E4M3 (or both NVFP4 with the two-level P~ scaling);
+ *   - two-level accumulation: each key tile's P^ V^ partial is computed alone
+ *     and added into an FP32 running output with the online-softmax rescale.
+ *
+ * Conventions
+ *   - All tensors are device memory owned by the caller.  The library never
+ *     allocates, frees or synchronises (except sage_read_status, which copies
+ *     four words back and waits for that copy).
+ *   - Inputs q [B,Hq,N,d], k and v [B,Hkv,M,d], output o [B,Hq,N,d]: bf16,
+ *     contiguous, 16-byte aligned.  Query head h reads kv head h / (Hq/Hkv).
+ *   - sage_quantize_qkv writes the workspace; sage_attn_fwd reads it.  Both
+ *     launch on the caller's stream and return at once.
+ *   - Argument errors are reported synchronously, before anything is
+ *     launched.  Conditions found on the device (an input out of range, a
+ *     bounded wait that gave up) are written to a status word inside the
+ *     workspace; read it with sage_read_status after the stream has run.
+ *     Nothing traps, aborts or throws across this boundary.
+ */
+#ifndef SAGE_H
+#define SAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *sage_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad shape, bad flags */
+  SAGE_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement */
+  SAGE_ERR_WORKSPACE = 3,   /* workspace smaller than sage_workspace_bytes() */
+  SAGE_ERR_RANGE = 4,       /* (device) an input was non-finite or |x| >= 2^16 */
+  SAGE_ERR_TIMEOUT = 5,     /* (device) a bounded wait gave up; outputs undefined */
+  SAGE_ERR_CUDA = 6         /* a CUDA runtime call failed (launch, copy) */
+} sage_status;
+
+/* quant_mode */
+enum {
+  SAGE_Q8_PV8 = 0,  /* INT8 per-block Q/K, FP8 E4M3 P~ (1/448) and per-channel FP8 V */
+  SAGE_QF8_PV8 = 1, /* FP8 E4M3 per-block Q/K, FP8 P~ / V as above */
+  SAGE_NVFP4 = 2    /* NVFP4 Q/K/V (E2M1, 1x16 blocks, E4M3 scales), two-level P~ */
+};
+
+/* flags */
+enum {
+  SAGE_SMOOTH_K = 1, /* subtract mean(K) over tokens (always exact) */
+  SAGE_SMOOTH_Q = 2, /* subtract the per-block mean of Q, add dS back */
+  SAGE_SMOOTH_V = 4  /* subtract mean(V) over tokens, add it back to O */
+};
+
+typedef struct {
+  int B, Hq, Hkv, N, M, d;
+} sage_shape;
+
+/* Byte offsets of the workspace regions (each 1024-byte aligned), for tests
+ * and tools that read the quantized tensors.  Element layouts:
+ *   qhat   [B*Hq*N_pad, d] codes: fp16 value of the INT8 code (mode 0: GB300's
+ *          tensor cores have no INT8 path, so INT8 codes are carried as exact
+ *          fp16 integers), E4M3 bytes (mode 1), packed E2M1 pairs (mode 2)
+ *   dq     [B*Hq*Tm]      fp32 per-block Q scale (modes 0, 1)
+ *   qbar   [B*Hq*Tm, d]   fp32 per-block Q mean (0 unless SAGE_SMOOTH_Q)
+ *   khat   [B*Hkv*M_pad, d] codes as qhat
+ *   dk     [B*Hkv*Tn]     fp32 per-block K scale (modes 0, 1)
+ *   kbar   [B*Hkv, d]     fp32 K mean (0 unless SAGE_SMOOTH_K)
+ *   vhat   [B*Hkv*d, M_pad] V codes transposed (token-contiguous): E4M3 bytes,
+ *          or packed E2M1 pairs (mode 2)
+ *   dv     [B*Hkv, d]     fp32 per-channel V scale (modes 0, 1)
+ *   vm     [B*Hkv, d]     fp32 V mean (0 unless SAGE_SMOOTH_V)
+ *   qsf, ksf, vsf         E4M3 block scales (mode 2), layouts in the .cu file
+ *   stats                 reduction scratch of sage_quantize_qkv
+ *   status                int32[4]: code, site, detail, spare
+ * N_pad = N rounded up to 128, M_pad = M rounded up to 128, Tm = N_pad/bq,
+ * Tn = ceil(M/bk). */
+typedef struct {
+  size_t qhat, dq, qbar, khat, dk, kbar, vhat, dv, vm, qsf, ksf, vsf, stats, status, total;
+  int N_pad, M_pad, Tm, Tn;
+} sage_ws_layout;
+
+/* Workspace size in bytes for a shape and mode; 0 if the request is invalid
+ * or unsupported (see sage_workspace_layout for the reason). */
+size_t sage_workspace_bytes(const sage_shape *shape, int quant_mode, int bq, int bk);
+
+/* Fill *out with the workspace regions for this request. */
+sage_status sage_workspace_layout(const sage_shape *shape, int quant_mode, int bq, int bk,
+                                  sage_ws_layout *out);
+
+/* Smoothing and quantization pre-pass (SageAttention2 summary §3.2 item 1 and
+ * §3.4 "Smoothing Q"; SageAttention3 summary §3.4, quantizer phi).
+ * Reads q, k, v (bf16, see Conventions), writes the quantized tensors, scales
+ * and means into the workspace.  Supported: d in {64, 128}, bq == 128,
+ * bk in {64, 128}, Hq % Hkv == 0, 1 <= N, M <= 2^23.  Every quantizer is a
+ * fixed binary32 function of the inputs (round to nearest even), so codes and
+ * scales are reproducible bit for bit. */
+sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags, int bq, int bk,
+                              const void *q, const void *k, const void *v, void *workspace,
+                              size_t workspace_bytes, sage_stream_t stream);
+
+/* Fused attention over the quantized workspace (SageAttention2 summary §3.4
+ * "The Complete Algorithm", SageAttention3 summary §3.4 "FP4 Attention Kernel
+ * Algorithm").  causal != 0 masks key j for query i when j > i + (M - N)
+ * (bottom-right aligned; requires M >= N).  quant_mode, flags, bq and bk must
+ * be those given to sage_quantize_qkv for this workspace.  Writes o (bf16). */
+sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode,
+                          int flags, int bq, int bk, const void *workspace, size_t workspace_bytes,
+                          void *o, sage_stream_t stream);
+
+/* End-to-end call on HOST buffers: copies q, k, v (host, ideally pinned) into
+ * dev_buf, runs sage_quantize_qkv and sage_attn_fwd, copies o back to o_host,
+ * all on `stream` (asynchronous with pinned host memory).  dev_buf is one
+ * caller-allocated device buffer of at least sage_host_buffer_bytes(). */
+size_t sage_host_buffer_bytes(const sage_shape *shape, int quant_mode, int bq, int bk);
+sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, int quant_mode,
+                           int flags, int bq, int bk, const void *q_host, const void *k_host,
+                           const void *v_host, void *o_host, void *dev_buf, size_t dev_bytes,
+                           sage_stream_t stream);
+
+/* Copy the device status word back (blocking on that copy only): *code is a
+ * sage_status (SAGE_OK, SAGE_ERR_RANGE or SAGE_ERR_TIMEOUT), *site says where
+ * it was raised.  The status word is cleared by every sage_quantize_qkv. */
+sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,
+                             int *code, int *site);
+
+const char *sage_status_str(sage_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,90 @@
+"""Helpers for the GPU parity tests: read the library's workspace back into the
+oracle's logical layouts, and compare outputs with the stated tolerances."""
+import numpy as np
+import torch
+
+
+def _np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def read_workspace(ws, mode: int) -> dict:
+    """Device workspace -> numpy arrays in the oracle's logical (unpadded) layouts."""
+    s, L = ws.shape, ws.layout
+    B, Hq, Hkv, N, M, d = s.B, s.Hq, s.Hkv, s.N, s.M, s.d
+    Np, Mp, Tm, Tn = L.N_pad, L.M_pad, L.Tm, L.Tn
+    cb = 2 if mode == 0 else 1
+
+    def f32(name, n):
+        return _np(ws.region(name, 4 * n).view(torch.float32))
+
+    qraw = ws.region("qhat", B * Hq * Np * d * cb)
+    kraw = ws.region("khat", B * Hkv * Mp * d * cb)
+    if mode == 0:
+        qc = _np(qraw.view(torch.float16)).astype(np.float32).reshape(B, Hq, Np, d)[:, :, :N]
+        kc = _np(kraw.view(torch.float16)).astype(np.float32).reshape(B, Hkv, Mp, d)[:, :, :M]
+        assert np.all(qc == np.round(qc)) and np.all(np.abs(qc) <= 127)
+        qc = qc.astype(np.int8).view(np.uint8)
+        kc = kc.astype(np.int8).view(np.uint8)
+    else:
+        qc = _np(qraw).reshape(B, Hq, Np, d)[:, :, :N]
+        kc = _np(kraw).reshape(B, Hkv, Mp, d)[:, :, :M]
+    vt = _np(ws.region("vhat", B * Hkv * d * Mp)).reshape(B, Hkv, d, Mp)[..., :M]
+    return dict(
+        qc=np.ascontiguousarray(qc), kc=np.ascontiguousarray(kc),
+        vc=np.ascontiguousarray(vt.transpose(0, 1, 3, 2)),
+        dq=f32("dq", B * Hq * Tm).reshape(B, Hq, Tm),
+        qbar=f32("qbar", B * Hq * Tm * d).reshape(B, Hq, Tm, d),
+        dk=f32("dk", B * Hkv * Tn).reshape(B, Hkv, Tn),
+        kbar=f32("kbar", B * Hkv * d).reshape(B, Hkv, d),
+        dv=f32("dv", B * Hkv * d).reshape(B, Hkv, d),
+        vm=f32("vm", B * Hkv * d).reshape(B, Hkv, d),
+        pad_q=_np(qraw).reshape(B, Hq, Np, d * cb)[:, :, N:],
+        pad_v=vt_pad(ws, B, Hkv, d, Mp, M),
+    )
+
+
+def vt_pad(ws, B, Hkv, d, Mp, M):
+    vt = _np(ws.region("vhat", B * Hkv * d * Mp)).reshape(B, Hkv, d, Mp)
+    return vt[..., M:]
+
+
+def fold_neg_zero_e4m3(c: np.ndarray) -> np.ndarray:
+    """E4M3 codes with -0 (0x80) folded onto +0: both encode zero."""
+    c = c.copy()
+    c[c == 0x80] = 0
+    return c
+
+
+def compare_codes(got: dict, ref, mode: int, flags: int):
+    """Bit-exact comparison of codes, scales and means (E4M3 +-0 folded)."""
+    def bits(a):
+        return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+    qc_ref, kc_ref, vc_ref = ref.qc, ref.kc, ref.vc
+    qc, kc, vc = got["qc"], got["kc"], got["vc"]
+    if mode == 1:
+        qc, kc, qc_ref, kc_ref = map(fold_neg_zero_e4m3, (qc, kc, qc_ref, kc_ref))
+    vc, vc_ref = fold_neg_zero_e4m3(vc), fold_neg_zero_e4m3(vc_ref)
+    out = {}
+    out["dq"] = np.array_equal(bits(got["dq"]), bits(ref.dq))
+    out["dk"] = np.array_equal(bits(got["dk"]), bits(ref.dk))
+    out["dv"] = np.array_equal(bits(got["dv"]), bits(ref.dv))
+    out["kbar"] = np.array_equal(bits(got["kbar"]), bits(ref.kbar))
+    out["vm"] = np.array_equal(bits(got["vm"]), bits(ref.vm))
+    out["qbar"] = np.array_equal(bits(got["qbar"]), bits(ref.qbar))
+    out["qc"] = np.array_equal(qc, qc_ref)
+    out["kc"] = np.array_equal(kc, kc_ref)
+    out["vc"] = np.array_equal(vc, vc_ref)
+    out["pad_zero"] = (not got["pad_q"].any()) and (not got["pad_v"].any())
+    return out
+
+
+def output_metrics(got: np.ndarray, ref: np.ndarray) -> dict:
+    got = got.astype(np.float64).ravel()
+    ref = ref.astype(np.float64).ravel()
+    err = np.abs(got - ref)
+    return dict(max_rel=float(err.max() / max(np.abs(ref).max(), 1e-30)),
+                rel_l1=float(err.sum() / max(np.abs(ref).sum(), 1e-30)),
+                cos=float(np.dot(got, ref) / np.sqrt(np.dot(got, got) * np.dot(ref, ref))),
+                rmse=float(np.sqrt(np.mean((got - ref) ** 2))))

@@ -1,0 +1,110 @@
+"""The C ABI library loads and exports every symbol include/sage.h declares;
+host-side checks (layout, argument validation) behave as documented.
+
+Every call here fails validation before anything is launched, so these tests
+run without a GPU (and never hand a device a fake pointer on one that has it).
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sage():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import bit_quantized_attention_gb300 as s
+    return s
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sage.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sage_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sage_quantize_qkv", "sage_attn_fwd", "sage_workspace_bytes", "sage_read_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sage):
+    lib = C.CDLL(sage.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(sage.EXPORTS) == set(declared_functions())
+
+
+def test_workspace_layout_is_aligned_and_ordered(sage):
+    for shp, mode, bk in [((4, 32, 32, 4096, 4096, 128), 0, 64), ((2, 48, 48, 17776, 17776, 64), 0, 64),
+                          ((1, 32, 8, 4096, 65536, 128), 1, 128), ((1, 2, 2, 256, 256, 64), 0, 64)]:
+        s = sage.Shape(*shp)
+        L = sage.sage_workspace_layout(s, mode, 128, bk).as_dict()
+        offs = [L[k] for k in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm", "qsf", "ksf",
+                               "vsf", "stats", "status", "total")]
+        assert all(o % 1024 == 0 for o in offs)
+        assert offs == sorted(offs)
+        assert L["N_pad"] % 128 == 0 and L["N_pad"] >= shp[3]
+        assert L["M_pad"] % 128 == 0 and L["M_pad"] >= shp[4]
+        assert L["Tn"] == -(-shp[4] // bk)
+        code_b = 2 if mode == 0 else 1
+        assert L["dq"] - L["qhat"] >= shp[0] * shp[1] * L["N_pad"] * shp[5] * code_b
+        assert sage.sage_workspace_bytes(s, mode, 128, bk) == L["total"]
+
+
+@pytest.mark.parametrize("shp,mode,bq,bk,code", [
+    ((1, 2, 2, 256, 256, 96), 0, 128, 64, 2),     # head dim not in {64, 128}
+    ((1, 3, 2, 256, 256, 64), 0, 128, 64, 1),     # Hq % Hkv != 0
+    ((1, 2, 2, 256, 256, 64), 0, 64, 64, 2),      # bq != 128
+    ((1, 2, 2, 256, 256, 64), 0, 128, 32, 2),     # bk not in {64, 128}
+    ((1, 2, 2, 0, 256, 64), 0, 128, 64, 1),       # empty query
+    ((1, 2, 2, 256, 0, 64), 0, 128, 64, 1),       # empty keys
+    ((1, 2, 2, 256, 256, 64), 7, 128, 64, 1),     # unknown mode
+    ((1, 2, 2, 1 << 24, 256, 64), 0, 128, 64, 2),  # beyond the exact-mean token limit
+])
+def test_invalid_requests_rejected(sage, shp, mode, bq, bk, code):
+    s = sage.Shape(*shp)
+    assert sage.sage_workspace_bytes(s, mode, bq, bk) == 0
+    L = sage.WsLayout()
+    assert sage.lib.sage_workspace_layout(C.byref(s), mode, bq, bk, C.byref(L)) == code
+    fake = C.c_void_p(1 << 20)
+    rc = sage.lib.sage_quantize_qkv(C.byref(s), mode, 1, bq, bk, fake, fake, fake, fake, 1 << 40, None)
+    assert rc == code
+
+
+def test_pointer_workspace_and_flag_checks(sage):
+    s = sage.Shape(1, 2, 2, 256, 256, 64)
+    need = sage.sage_workspace_bytes(s, 0, 128, 64)
+    ok = C.c_void_p(1 << 20)                 # 1024-aligned, never dereferenced: every call below fails first
+    q = sage.lib.sage_quantize_qkv
+    a = sage.lib.sage_attn_fwd
+    assert q(C.byref(s), 0, 1, 128, 64, None, ok, ok, ok, need, None) == 1            # null q
+    assert q(C.byref(s), 0, 1, 128, 64, C.c_void_p((1 << 20) + 8), ok, ok, ok, need, None) == 1  # misaligned
+    assert q(C.byref(s), 0, 1, 128, 64, ok, ok, ok, C.c_void_p((1 << 20) + 16), need, None) == 1  # ws align
+    assert q(C.byref(s), 0, 1, 128, 64, ok, ok, ok, ok, need - 1, None) == 3          # workspace too small
+    assert q(C.byref(s), 0, 64, 128, 64, ok, ok, ok, ok, need, None) == 1             # unknown flag
+    assert a(C.byref(s), 0, 0.125, 0, 1, 128, 64, ok, need - 1, ok, None) == 3
+    assert a(C.byref(s), 0, 0.0, 0, 1, 128, 64, ok, need, ok, None) == 1              # sm_scale <= 0
+    assert a(C.byref(s), 0, float("nan"), 0, 1, 128, 64, ok, need, ok, None) == 1
+    assert a(C.byref(s), 0, 0.125, 0, 1, 128, 64, ok, need, None, None) == 1          # null output
+    s2 = sage.Shape(1, 2, 2, 512, 256, 64)
+    need2 = sage.sage_workspace_bytes(s2, 0, 128, 64)
+    assert a(C.byref(s2), 1, 0.125, 0, 1, 128, 64, ok, need2, ok, None) == 2          # causal with N > M
+
+
+def test_status_strings(sage):
+    for code in range(7):
+        assert sage.sage_status_str(code)
+    assert "range" in sage.sage_status_str(4)
+
+
+def test_package_has_no_fallback():
+    src = open(os.path.join(ROOT, "bit_quantized_attention_gb300", "_binding.py")).read()
+    assert "raise ImportError" in src
+    for bad in ("import oracle", "from oracle", "sage_oracle"):
+        assert bad not in src
