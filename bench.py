@@ -1,0 +1,380 @@
+"""Throughput of the quantized attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--bk BK] [--impl reference]
+
+One step = the whole hot path over one batch: the smoothing + quantization
+pre-pass (sage_quantize_qkv) and the fused attention (sage_attn_fwd), with
+inputs resident in HBM.  Metric: TOPS = 4*B*H*N*M*d / t (halved when causal).
+Timing: W warm-up steps, then K steps bracketed by a barrier and a device
+synchronize, CUDA events on the launching stream, max over ranks.  Inputs
+(Q, K, V in bf16) are larger than L2, so no flush is needed between steps.
+
+Extra keys on the JSON line:
+  e2e          the same metric through sage_attn_host (pinned host buffers, the
+               host->device copies and the device->host copy of O in the timed region)
+  roofline     the attention kernel against the measured tensor peak
+  cpu_baseline the CPU oracle on a bounded sample of the same workload
+  clocks       SM clocks and throttle reasons sampled during the timed region
+Under torchrun (N > 1) every rank runs its own batch of the workload on its
+own GPU (independent problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024
+NOMINAL_FP8_OVER_BF16 = 2.0   # dense fp8 / dense bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained"), d["hbm_gbs"], "measured"
+    return FALLBACK_BF16_TFLOPS, None, FALLBACK_HBM_GBS, "fallback"
+
+
+def attention_peak(mode: int, bf16_tflops: float):
+    """Dense tensor peak of the attention kernel's instruction mix, TFLOP/s.
+    INT8 Q/K runs QK^T as kind::f16 (INT8 codes held as fp16) and P^V as
+    kind::f8f6f4: equal op counts at the bf16 and fp8 rates."""
+    fp8 = bf16_tflops * NOMINAL_FP8_OVER_BF16
+    if mode == 0:
+        return 2.0 / (1.0 / bf16_tflops + 1.0 / fp8), "kind::f16 (QK) + kind::f8f6f4 (PV)"
+    if mode == 1:
+        return fp8, "kind::f8f6f4"
+    return fp8 * 2.0, "kind::mxf4nvf4 (nominal 2x fp8)"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms in the background while running."""
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sms = sorted(r["sm"] for r in rows)
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in rows),
+                "samples": len(rows), "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- reference arm
+class OracleSample:
+    """The oracle (as it stands) on a bounded sample of the workload: the
+    pre-pass of one (batch, kv-head) and the attention rows of a spread of
+    query rows of its heads, on all host cores."""
+
+    def __init__(self, cfg, threads: int | None = None):
+        import oracle
+        from workload import make_inputs
+        self.oracle = oracle
+        self.cfg = cfg
+        self.threads = threads or os.cpu_count() or 1
+        self.sub = cfg.with_(B=1, Hq=cfg.Hq // cfg.Hkv, Hkv=1)   # one kv-head and its query heads
+        self.q, self.k, self.v = make_inputs(self.sub)
+        s = self.sub
+        self.shape = (s.B, s.Hq, s.Hkv, s.N, s.M, s.d)
+
+    def run(self, nrows: int):
+        """Time the pre-pass and nrows attention rows; returns (TOPS, seconds, rows)."""
+        import numpy as np
+        s, o = self.sub, self.oracle
+        t0 = time.perf_counter()
+        qz = o.quantize(self.shape, s.mode, s.flags, s.bq, s.bk, self.q, self.k, self.v)
+        tq = time.perf_counter() - t0
+        # rows spread evenly over all query rows of the sample (causal rows see
+        # about M/2 keys on average)
+        rows = np.linspace(0, s.Hq * s.N - 1, nrows).astype(np.int64)
+        t1 = time.perf_counter()
+        o.parallel_attn_rows(self.shape, s.mode, s.flags, s.bq, s.bk, s.causal, s.sm_scale, self.q, self.k,
+                             self.v, qz, rows, threads=self.threads)
+        ta = time.perf_counter() - t1
+        off = s.M - s.N
+        pairs = sum(min(s.M, int(r) % s.N + off + 1) if s.causal else s.M for r in rows)
+        # the literal metric counts half the pairs when causal: scale to it so the
+        # GPU and CPU values share one unit
+        lit_over_exact = self.cfg.ops / (4.0 * self.cfg.d * self.cfg.B * self.cfg.Hq * self.cfg.visible_pairs)
+        # pre-pass share: its time prorated to the fraction of query rows done
+        t_total = ta + tq * (len(rows) / (s.Hq * s.N))
+        return 4.0 * s.d * pairs * lit_over_exact / t_total / 1e12, t_total, len(rows)
+
+    def calibrated_rows(self, budget_s: float) -> int:
+        _, secs, n = self.run(32)
+        return int(max(32, min(self.sub.Hq * self.sub.N, budget_s / max(secs / n, 1e-6))))
+
+    def describe(self, nrows: int) -> str:
+        return ("oracle pre-pass of 1 kv-head (%d query heads, time prorated) + attention of %d query rows "
+                "spread over them" % (self.sub.Hq, nrows))
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    smp = OracleSample(cfg)
+    per_step = max(1.0, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
+    nrows = smp.calibrated_rows(per_step)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        tops, secs, _ = smp.run(nrows)
+        if i >= args.warmup:
+            vals.append((tops, secs))
+    tops = sum(v[0] for v in vals) / len(vals)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * sum(v[1] for v in vals) / len(vals), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": smp.threads, "kind": "oracle",
+                         "sample": smp.describe(nrows)},
+        "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+METRIC = "quantized attention TOPS (4*B*H*N*M*d/s, causal halved) and % of tensor peak"
+
+
+def workload_config(cfg):
+    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "N": cfg.N, "M": cfg.M, "d": cfg.d,
+            "causal": cfg.causal, "quant_mode": ["int8_qk_fp8_pv", "fp8_qk_fp8_pv", "nvfp4"][cfg.mode],
+            "flags": {"smooth_k": bool(cfg.flags & 1), "smooth_q": bool(cfg.flags & 2),
+                      "smooth_v": bool(cfg.flags & 4)},
+            "bq": cfg.bq, "bk": cfg.bk,
+            "l2": "inputs larger than L2 (%.0f MB of bf16 Q/K/V per step), no flush" % (
+                2.0 * cfg.d * (cfg.B * cfg.Hq * cfg.N + 2 * cfg.B * cfg.Hkv * cfg.M) / 1e6),
+            "parallelism": "independent batch per GPU"}
+
+
+def run_gpu(args, cfg):
+    import torch
+
+    import bit_quantized_attention_gb300 as sage
+    from workload import make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    qh, kh, vh = make_inputs(cfg)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    shape = sage.shape_of(q, k)
+    ws = sage.new_workspace(shape, cfg.mode, cfg.flags, cfg.bq, cfg.bk, dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        sage.sage_quantize_qkv(q, k, v, cfg.mode, cfg.flags, cfg.bq, cfg.bk, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        sage.sage_attn_fwd(ws, cfg.causal, cfg.sm_scale, out=o, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert sage.sage_read_status(ws) == (0, 0), "device status after warm-up"
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    clocks = clk.summary()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    code = sage.sage_read_status(ws)
+    if pg is not None:
+        t = torch.tensor([total_ms, attn_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, attn_ms = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+    value = cfg.ops * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- e2e through the C ABI on host buffers (pinned), copies inside the timed region
+    q_pin, k_pin, v_pin = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+    o_pin = torch.empty_like(qh).pin_memory()
+    nbytes = sage.sage_host_buffer_bytes(shape, cfg.mode, cfg.bq, cfg.bk)
+    raw = torch.empty(nbytes + 1024, dtype=torch.uint8, device=dev)
+    dev_buf = raw[(-raw.data_ptr()) % 1024:][:nbytes]
+    del ws
+    for _ in range(max(1, args.warmup // 2)):
+        sage.sage_attn_host(shape, cfg.causal, cfg.sm_scale, cfg.mode, cfg.flags, cfg.bq, cfg.bk,
+                            q_pin, k_pin, v_pin, o_pin, dev_buf, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        sage.sage_attn_host(shape, cfg.causal, cfg.sm_scale, cfg.mode, cfg.flags, cfg.bq, cfg.bk,
+                            q_pin, k_pin, v_pin, o_pin, dev_buf, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_val = cfg.ops * world / (e2e_ms * 1e-3) / 1e12
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = qh.numel() * 2
+
+    bf16, bf16_sus, hbm, src = peaks()
+    peak, kinds = attention_peak(cfg.mode, bf16)
+    achieved = cfg.ops / (attn_ms * 1e-3) / 1e12
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if os.path.exists(tf):
+        rec = json.load(open(tf)).get(cfg.name + "_bk%d" % cfg.bk)
+        if rec and rec.get("kernel_hash") == kernel_hash():
+            traffic = rec["bytes_per_launch"]
+    out = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": ["int8/e4m3", "e4m3", "e2m1"][cfg.mode], "data": "synthetic",
+        "config": workload_config(cfg),
+        "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_q8_kernel (sage_attn_fwd)", "instructions": kinds,
+                     "peak_source": "%s bf16 burst %.1f TFLOP/s x nominal fp8/bf16 ratio %.0f" % (
+                         src, bf16, NOMINAL_FP8_OVER_BF16),
+                     "attn_ms": attn_ms},
+        "attn_only_tops": achieved,
+        "prepass_ms": ms_per_step - attn_ms,
+        "clocks": clocks,
+        "device_status": list(code),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = OracleSample(cfg)
+        nrows = smp.calibrated_rows(args.ref_budget)
+        tops, secs, _ = smp.run(nrows)
+        out["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": smp.threads, "kind": "oracle",
+                               "sample": smp.describe(nrows), "seconds": secs}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for f in sorted(os.listdir(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc"))):
+        h.update(open(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llm_prefill")
+    ap.add_argument("--bk", type=int, default=None)
+    ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from workload import CONFIGS
+    cfg = CONFIGS[args.workload]
+    if args.bk:
+        cfg = cfg.with_(bk=args.bk)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    main()
