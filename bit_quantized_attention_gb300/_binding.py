@@ -21,7 +21,8 @@ STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3:
           4: "SAGE_ERR_RANGE", 5: "SAGE_ERR_TIMEOUT", 6: "SAGE_ERR_CUDA"}
 
 EXPORTS = ["sage_workspace_bytes", "sage_workspace_layout", "sage_quantize_qkv", "sage_attn_fwd",
-           "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str"]
+           "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str",
+           "sage_quantize_qkv_static_scratch"]
 
 
 class SageError(RuntimeError):
@@ -53,6 +54,8 @@ def _load():
     L.sage_workspace_layout.argtypes, L.sage_workspace_layout.restype = [P(Shape), i32, i32, i32, P(WsLayout)], i32
     L.sage_quantize_qkv.argtypes = [P(Shape), i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     L.sage_quantize_qkv.restype = i32
+    L.sage_quantize_qkv_static_scratch.argtypes = [P(Shape), i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.sage_quantize_qkv_static_scratch.restype = i32
     L.sage_attn_fwd.argtypes = [P(Shape), i32, f32, i32, i32, i32, i32, vp, sz, vp, vp]
     L.sage_attn_fwd.restype = i32
     L.sage_host_buffer_bytes.argtypes, L.sage_host_buffer_bytes.restype = [P(Shape), i32, i32, i32], sz
@@ -137,6 +140,21 @@ def sage_quantize_qkv(q, k, v, mode: int, flags: int, bq: int = 128, bk: int = 6
     ws.flags = flags
     _check(lib.sage_quantize_qkv(C.byref(shape), mode, flags, bq, bk, _ptr(q), _ptr(k), _ptr(v), _ptr(ws.buf),
                                  ws.buf.numel(), _stream(stream)), "sage_quantize_qkv")
+    return ws
+
+
+def sage_quantize_qkv_static_scratch(q, k, v, mode: int, flags: int, bq: int = 128, bk: int = 64,
+                                     workspace=None, stream=None) -> Workspace:
+    """The pre-pass with its reduction scratch inside the library (no scratch
+    region is needed from the caller; see include/sage.h for the limit)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _bf16_cuda(t, n)
+    shape = shape_of(q, k)
+    ws = workspace or new_workspace(shape, mode, flags, bq, bk, q.device)
+    ws.flags = flags
+    _check(lib.sage_quantize_qkv_static_scratch(C.byref(shape), mode, flags, bq, bk, _ptr(q), _ptr(k), _ptr(v),
+                                                _ptr(ws.buf), ws.buf.numel(), _stream(stream)),
+           "sage_quantize_qkv_static_scratch")
     return ws
 
 

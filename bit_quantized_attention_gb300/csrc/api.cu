@@ -102,6 +102,22 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
   return launch_attn_q8(*shape, causal, sm_scale, quant_mode, flags, bk, workspace, L, o, (cudaStream_t)stream);
 }
 
+sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_mode, int flags, int bq, int bk,
+                                             const void *q, const void *k, const void *v, void *workspace,
+                                             size_t workspace_bytes, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  if ((long long)shape->B * shape->Hkv * shape->d > 32768) return SAGE_ERR_UNSUPPORTED;
+  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  return launch_quantize_q8_static_scratch(*shape, quant_mode, flags, bq, bk, q, k, v, workspace, L,
+                                           (cudaStream_t)stream);
+}
+
 static size_t io_bytes(const sage_shape *s) {
   const size_t qn = (size_t)s->B * s->Hq * s->N * s->d * 2, kn = (size_t)s->B * s->Hkv * s->M * s->d * 2;
   return align_up(qn, 1024) * 2 + align_up(kn, 1024) * 2;  // q, o, k, v

@@ -12,6 +12,12 @@ sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq,
                                const void *k, const void *v, void *ws, const sage_ws_layout &L,
                                cudaStream_t stream);
 
+// Same pre-pass with its statistics scratch in a device array inside the
+// library (quantize.cu); B*Hkv*d must not exceed 32768.
+sage_status launch_quantize_q8_static_scratch(const sage_shape &s, int mode, int flags, int bq, int bk,
+                                              const void *q, const void *k, const void *v, void *ws,
+                                              const sage_ws_layout &L, cudaStream_t stream);
+
 // Attention for SAGE_Q8_PV8 / SAGE_QF8_PV8 (attn_q8.cu).
 sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
                            const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream);

@@ -31,6 +31,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "layout.h"
 #include "launch.h"
 #include "sm103.cuh"
@@ -386,6 +388,118 @@ sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq,
   StatsView st = stats_view(ws, L, s);
   int *status = (int *)(w + L.status);
   const int n = s.B * s.Hkv * s.d;
+  init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
+  dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
+  if (s.d == 64)
+    stats_kernel<64><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+  else
+    stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+
+  QuantArgs a;
+  a.q = (const uint4 *)q;
+  a.k = (const uint4 *)k;
+  a.v = (const uint4 *)v;
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.N = s.N;
+  a.M = s.M;
+  a.N_pad = L.N_pad;
+  a.M_pad = L.M_pad;
+  a.Tm = L.Tm;
+  a.Tn = L.Tn;
+  a.bk = bk;
+  a.mode = mode;
+  a.flags = flags;
+  a.qhat = (uint8_t *)(w + L.qhat);
+  a.khat = (uint8_t *)(w + L.khat);
+  a.vhat = (uint8_t *)(w + L.vhat);
+  a.dq = (float *)(w + L.dq);
+  a.qbar = (float *)(w + L.qbar);
+  a.dk = (float *)(w + L.dk);
+  a.kbar = (float *)(w + L.kbar);
+  a.dv = (float *)(w + L.dv);
+  a.vm = (float *)(w + L.vm);
+  a.st = st;
+  a.status = status;
+  a.nq = s.B * s.Hq * L.Tm;
+  a.nk = s.B * s.Hkv * L.Tn;
+  const int nv = s.B * s.Hkv * (L.M_pad / 128);
+  const unsigned grid = (unsigned)(a.nq + a.nk + nv);
+  const bool i8 = (mode == SAGE_Q8_PV8);
+  if (s.d == 64) {
+    if (i8)
+      quantize_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
+    else
+      quantize_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
+  } else {
+    if (i8)
+      quantize_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
+    else
+      quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
+}  // namespace sage
+
+// ---------------------------------------------------------------------------
+// Pre-pass whose statistics scratch lives inside the library.
+//
+// The statistics pass needs B*Hkv*d * 24 bytes of device scratch (fixed-point
+// column sums of K and V, V column min and max).  sage_quantize_qkv takes it
+// from the caller's workspace.  This variant takes it from the fixed device
+// array below instead, so a caller that is not allowed to obtain device memory
+// for scratch — for example a plug-in whose host framework owns every device
+// allocation, or a latency-critical caller that must not call cudaMalloc
+// because it can synchronise the device — only has to provide the inputs and
+// the output workspace.  The array is part of the library image: every GPU
+// that loads the library holds it until the process exits.
+//
+// All calls share the one array and it keeps the previous call's contents: the
+// init kernel clears it at the start of every call, and calls that overlap on
+// the GPU (different streams, or several host threads) race on it.
+namespace sage {
+
+constexpr int kStaticStatsChannels = 32768;  // limit on B * Hkv * d
+constexpr size_t kStaticStatsBytes = (size_t)kStaticStatsChannels * 24;
+static __device__ __align__(256) unsigned char g_stats_scratch[kStaticStatsBytes];
+
+// The device address of g_stats_scratch on each device, looked up once per
+// device with that device current (host code cannot use the symbol's name as
+// a device pointer).  The first call on a device does this look-up.
+static void *static_scratch_address(int device) {
+  constexpr int kMaxDevices = 64;
+  static void *addr[kMaxDevices] = {};
+  static std::mutex mu;
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_stats_scratch) != cudaSuccess) return nullptr;
+    addr[device] = p;
+  }
+  return addr[device];
+}
+
+sage_status launch_quantize_q8_static_scratch(const sage_shape &s, int mode, int flags, int bq, int bk,
+                                              const void *q, const void *k, const void *v, void *ws,
+                                              const sage_ws_layout &L, cudaStream_t stream) {
+  (void)bq;
+  const int n = s.B * s.Hkv * s.d;
+  if (n > kStaticStatsChannels) return SAGE_ERR_UNSUPPORTED;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return SAGE_ERR_CUDA;
+  char *scratch = (char *)static_scratch_address(device);
+  if (!scratch) return SAGE_ERR_CUDA;
+  StatsView st;
+  st.ksum = (int64_t *)scratch;
+  st.vsum = (int64_t *)(scratch + (size_t)n * 8);
+  st.vmin = (int *)(scratch + (size_t)n * 16);
+  st.vmax = (int *)(scratch + (size_t)n * 20);
+
+  char *w = (char *)ws;
+  int *status = (int *)(w + L.status);
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
   dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
   if (s.d == 64)

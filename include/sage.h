@@ -117,6 +117,26 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
                               const void *q, const void *k, const void *v, void *workspace,
                               size_t workspace_bytes, sage_stream_t stream);
 
+/* The pre-pass of sage_quantize_qkv with its reduction scratch held in a fixed
+ * device array inside the library instead of the caller's workspace.  The
+ * pages have no counterpart: this is for callers that may not obtain device
+ * memory for scratch — a plug-in whose host framework owns every device
+ * allocation, or a latency-critical caller that must not call cudaMalloc
+ * because it can synchronise the device.  The caller still provides q, k, v
+ * and the output workspace (same size and layout as for sage_quantize_qkv, so
+ * sage_attn_fwd reads it unchanged; its stats region is left untouched).
+ * Limit: B * Hkv * d <= 32768 (a 768 KiB array, held on every GPU that loads
+ * the library until the process exits); larger requests return
+ * SAGE_ERR_UNSUPPORTED.  The first call on a device looks up the array's
+ * device address with that device current; make that first call before any
+ * stream capture.  The call allocates and frees nothing.  Every call shares
+ * the array and clears it before use; calls that overlap on the GPU race on
+ * it and must be serialised by the caller. */
+sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_mode, int flags, int bq,
+                                             int bk, const void *q, const void *k, const void *v,
+                                             void *workspace, size_t workspace_bytes,
+                                             sage_stream_t stream);
+
 /* Fused attention over the quantized workspace (SageAttention2 summary §3.4
  * "The Complete Algorithm", SageAttention3 summary §3.4 "FP4 Attention Kernel
  * Algorithm").  causal != 0 masks key j for query i when j > i + (M - N)
