@@ -357,7 +357,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llm_prefill")
-    ap.add_argument("--bk", type=int, default=None)
+    ap.add_argument("--bk", type=int, default=128, help="key tile = K scale block (the workload leaves it open)")
     ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -98,19 +98,24 @@ __global__ void init_kernel(StatsView st, int n, int *status) {
 
 // ------------------------------------------------------------------ stats
 // grid (ceil(M / kStatTokens), B*Hkv).  Column sums of K and V (fixed point),
-// column min / max of V, range check of K and V.
+// column min / max of V, range check of K and V.  Each thread owns 8 channels
+// of every RPP-th row; loads are issued in batches of kBatch rows so several
+// are in flight; partial results meet in warp shuffles, then shared memory.
 template <int D>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                          int M, StatsView st, int *status) {
-  constexpr int VPR = D / 8;               // 16-byte vectors per row
+  constexpr int VPR = D / 8;               // 16-byte vectors per row (threads per row)
   constexpr int RPP = kThreads / VPR;      // rows per pass
-  __shared__ long long sk[RPP][D];
-  __shared__ long long sv[RPP][D];
-  __shared__ int smin[RPP][D];
-  __shared__ int smax[RPP][D];
+  constexpr int kBatch = 4;
+  constexpr int NW = kThreads / 32;
+  __shared__ long long sk[NW][D];
+  __shared__ long long sv[NW][D];
+  __shared__ int smin[NW][D];
+  __shared__ int smax[NW][D];
   const int hb = blockIdx.y;
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
   const int t0 = blockIdx.x * kStatTokens;
+  const int t1 = min(M, t0 + kStatTokens);
   long long ks[8], vs[8];
   float vmn[8], vmx[8];
 #pragma unroll
@@ -121,35 +126,61 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
     vmx[e] = __int_as_float(0xFF800000);
   }
   bool bad_k = false, bad_v = false;
-  for (int t = t0 + rr; t < min(M, t0 + kStatTokens); t += RPP) {
-    const size_t off = ((size_t)hb * M + t) * VPR + vc;
-    float fk[8], fv[8];
-    unpack_bf16x8(k[off], fk);
-    unpack_bf16x8(v[off], fv);
+  for (int tb = t0 + rr; tb < t1; tb += kBatch * RPP) {
+    uint4 kb[kBatch], vb[kBatch];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      bad_k |= !in_range(fk[e]);
-      bad_v |= !in_range(fv[e]);
-      ks[e] += fixed24(fk[e]);
-      vs[e] += fixed24(fv[e]);
-      vmn[e] = fminf(vmn[e], fv[e]);
-      vmx[e] = fmaxf(vmx[e], fv[e]);
+    for (int i = 0; i < kBatch; ++i) {
+      const int t = tb + i * RPP;
+      const size_t off = ((size_t)hb * M + min(t, t1 - 1)) * VPR + vc;
+      kb[i] = k[off];
+      vb[i] = v[off];
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (tb + i * RPP >= t1) break;
+      float fk[8], fv[8];
+      unpack_bf16x8(kb[i], fk);
+      unpack_bf16x8(vb[i], fv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bad_k |= !in_range(fk[e]);
+        bad_v |= !in_range(fv[e]);
+        ks[e] += fixed24(fk[e]);
+        vs[e] += fixed24(fv[e]);
+        vmn[e] = fminf(vmn[e], fv[e]);
+        vmx[e] = fmaxf(vmx[e], fv[e]);
+      }
     }
   }
   if (bad_k) raise_status(status, SAGE_ERR_RANGE, 1);
   if (bad_v) raise_status(status, SAGE_ERR_RANGE, 2);
+  // lanes vc, vc + VPR, ... of a warp hold the same channels
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    sk[rr][vc * 8 + e] = ks[e];
-    sv[rr][vc * 8 + e] = vs[e];
-    smin[rr][vc * 8 + e] = order_key(vmn[e]);
-    smax[rr][vc * 8 + e] = order_key(vmx[e]);
+  for (int o = VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
+      vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
+      vmn[e] = fminf(vmn[e], __shfl_xor_sync(0xffffffffu, vmn[e], o));
+      vmx[e] = fmaxf(vmx[e], __shfl_xor_sync(0xffffffffu, vmx[e], o));
+    }
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l < VPR) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sk[w][vc * 8 + e] = ks[e];
+      sv[w][vc * 8 + e] = vs[e];
+      smin[w][vc * 8 + e] = order_key(vmn[e]);
+      smax[w][vc * 8 + e] = order_key(vmx[e]);
+    }
   }
   __syncthreads();
   for (int c = threadIdx.x; c < D; c += kThreads) {
     long long a = 0, b = 0;
     int mn = smin[0][c], mx = smax[0][c];
-    for (int r = 0; r < RPP; ++r) {
+#pragma unroll
+    for (int r = 0; r < NW; ++r) {
       a += sk[r][c];
       b += sv[r][c];
       mn = min(mn, smin[r][c]);
@@ -175,19 +206,43 @@ struct QuantArgs {
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
 };
 
+// rint(RN(x / d)) clamped to +-127, exactly as rint(__fdiv_rn(x, d)) gives it.
+// q = x * RN(1/d) is within about 1.5e-5 of x/d for |x/d| <= 127, and RN(x/d)
+// within 7.6e-6 of x/d; unless q lies within 1e-4 of a half-integer, both round
+// to the same integer.  Near a half-integer (and for a non-finite q) the exact
+// quotient decides.
+__device__ __forceinline__ float int8_code(float x, float d, float rcp) {
+  const float q = __fmul_rn(x, rcp);
+  float c = rintf(q);
+  if (!(fabsf(fabsf(__fsub_rn(q, c)) - 0.5f) > 1e-4f)) c = rintf(__fdiv_rn(x, d));
+  return fminf(fmaxf(c, -127.0f), 127.0f);
+}
+
+// E4M3 codes of RN(x0 / d0), RN(x1 / d1) (low byte first), exactly as
+// cvt(__fdiv_rn(x, d)) gives them: RN(x/d) lies between q(1 - 2^-19) and
+// q(1 + 2^-19) for q = x * RN(1/d), and the conversion is monotone, so when
+// both ends give the same code that is the code; otherwise the exact quotient
+// decides.
+__device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float d0, float d1, float rcp0, float rcp1) {
+  const float q0 = __fmul_rn(x0, rcp0), q1 = __fmul_rn(x1, rcp1);
+  const float lo = 1.0f - 0x1p-19f, hi = 1.0f + 0x1p-19f;
+  const uint16_t a = cvt_e4m3x2(__fmul_rn(q0, lo), __fmul_rn(q1, lo));
+  const uint16_t b = cvt_e4m3x2(__fmul_rn(q0, hi), __fmul_rn(q1, hi));
+  if (a == b && isfinite(q0) && isfinite(q1)) return a;
+  return cvt_e4m3x2(__fdiv_rn(x0, d0), __fdiv_rn(x1, d1));
+}
+
 // Codes of 8 smoothed values with scale delta: 8 fp16 integers (INT8 mode,
 // 16 bytes) or 8 E4M3 bytes (FP8 mode).
 template <bool kInt8>
-__device__ __forceinline__ void encode8(const float (&g)[8], float delta, bool valid, uint8_t *dst) {
+__device__ __forceinline__ void encode8(const float (&g)[8], float delta, float rcp, bool valid, uint8_t *dst) {
+  const bool on = valid && delta != 0.0f;
   if (kInt8) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float c0 = 0.0f, c1 = 0.0f;
-      if (valid && delta != 0.0f) {
-        c0 = fminf(fmaxf(rintf(__fdiv_rn(g[2 * i], delta)), -127.0f), 127.0f);
-        c1 = fminf(fmaxf(rintf(__fdiv_rn(g[2 * i + 1], delta)), -127.0f), 127.0f);
-      }
+      const float c0 = on ? int8_code(g[2 * i], delta, rcp) : 0.0f;
+      const float c1 = on ? int8_code(g[2 * i + 1], delta, rcp) : 0.0f;
       const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
       w[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
     }
@@ -196,12 +251,9 @@ __device__ __forceinline__ void encode8(const float (&g)[8], float delta, bool v
     uint32_t w[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid && delta != 0.0f) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) c[e] = __fdiv_rn(g[4 * i + e], delta);
-      }
-      w[i] = (uint32_t)cvt_e4m3x2(c[0], c[1]) | ((uint32_t)cvt_e4m3x2(c[2], c[3]) << 16);
+      const uint16_t c01 = on ? e4m3_code2(g[4 * i], g[4 * i + 1], delta, delta, rcp, rcp) : 0;
+      const uint16_t c23 = on ? e4m3_code2(g[4 * i + 2], g[4 * i + 3], delta, delta, rcp, rcp) : 0;
+      w[i] = (uint32_t)c01 | ((uint32_t)c23 << 16);
     }
     *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
   }
@@ -269,6 +321,7 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
   if (bad) raise_status(status, SAGE_ERR_RANGE, site);
   amax = block_max(amax, red);
   const float delta = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
+  const float rcp = __frcp_rn(delta);
   constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
@@ -278,7 +331,7 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
     unpack_bf16x8(x[p], f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = __fsub_rn(f[e], mu[e]);
-    encode8<kInt8>(g, delta, r < valid_rows, dst + ((size_t)r * D + vc * 8) * CB);
+    encode8<kInt8>(g, delta, rcp, r < valid_rows, dst + ((size_t)r * D + vc * 8) * CB);
   }
   if (threadIdx.x == 0) *delta_out = delta;
   if (mean_out)
@@ -321,12 +374,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   }
   cta -= a.nk;
   // ---- V token chunk (b, g, 128 tokens): per-channel scales from the stats,
-  // E4M3 codes written transposed (token-contiguous per channel).
+  // E4M3 codes written transposed (token-contiguous per channel).  Each work
+  // item is 4 consecutive tokens x 8 channels: the 4 codes of a channel pack
+  // into one 32-bit word of a shared [channel][token/4] tile (row pitch 33
+  // words: the 32 items of a warp, consecutive token groups, hit 32 banks),
+  // which is then written out as 128-byte channel rows.
   {
     const int nchunk = a.M_pad / 128;
     const int ch = cta % nchunk, hb = cta / nchunk;
-    __shared__ float vmean[D], vinv[D];
-    __shared__ uint8_t tile[D][128 + 16];
+    __shared__ float vmean[D], vdelta[D], vrcp[D];
+    __shared__ uint32_t tile[D][33];
     const bool smooth = (a.flags & SAGE_SMOOTH_V) != 0;
     for (int c = threadIdx.x; c < D; c += kThreads) {
       const size_t i = (size_t)hb * D + c;
@@ -335,44 +392,50 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
       const float amax = fmaxf(fabsf(__fsub_rn(hi, mu)), fabsf(__fsub_rn(lo, mu)));
       const float delta = __fdiv_rn(amax, 448.0f);
       vmean[c] = mu;
-      vinv[c] = delta;
+      vdelta[c] = delta;
+      vrcp[c] = __frcp_rn(delta);
       if (ch == 0) {
         a.vm[i] = mu;
         a.dv[i] = delta;
       }
     }
     __syncthreads();
-    constexpr int VPR = D / 8, RPP = kThreads / VPR;
-    const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+    constexpr int VPR = D / 8;
     const int t0 = ch * 128;
-    for (int r = rr; r < 128; r += RPP) {
-      const int t = t0 + r;
-      float f[8];
-      if (t < a.M)
-        unpack_bf16x8(a.v[((size_t)hb * a.M + t) * VPR + vc], f);
+    for (int item = threadIdx.x; item < 32 * VPR; item += kThreads) {
+      const int tg = item & 31, cg = item >> 5;   // 4 tokens from 4*tg, channels 8*cg..
+      uint4 raw[4];
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const int c = vc * 8 + e;
-        float c0 = 0.0f, c1 = 0.0f;
-        if (t < a.M) {
-          if (vinv[c] != 0.0f) c0 = __fdiv_rn(__fsub_rn(f[e], vmean[c]), vinv[c]);
-          if (vinv[c + 1] != 0.0f) c1 = __fdiv_rn(__fsub_rn(f[e + 1], vmean[c + 1]), vinv[c + 1]);
-        }
-        const uint16_t p = cvt_e4m3x2(c0, c1);
-        tile[c][r] = (uint8_t)(p & 0xFF);
-        tile[c + 1][r] = (uint8_t)(p >> 8);
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 4 * tg + u;
+        raw[u] = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + cg] : make_uint4(0, 0, 0, 0);
       }
+      uint32_t word[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (t0 + 4 * tg + u >= a.M) continue;
+        float f[8];
+        unpack_bf16x8(raw[u], f);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int c = cg * 8 + e;
+          const float g0 = __fsub_rn(f[e], vmean[c]), g1 = __fsub_rn(f[e + 1], vmean[c + 1]);
+          // a zero scale (an all-zero channel) gives zero codes
+          const uint16_t pr = e4m3_code2(vdelta[c] != 0.0f ? g0 : 0.0f, vdelta[c + 1] != 0.0f ? g1 : 0.0f,
+                                         vdelta[c], vdelta[c + 1], vrcp[c], vrcp[c + 1]);
+          const uint32_t lo0 = vdelta[c] != 0.0f ? (pr & 0xFF) : 0, lo1 = vdelta[c + 1] != 0.0f ? (pr >> 8) : 0;
+          word[e] |= lo0 << (8 * u);
+          word[e + 1] |= lo1 << (8 * u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[cg * 8 + e][tg] = word[e];
     }
     __syncthreads();
     // coalesced store: each channel row of 128 tokens is 128 contiguous bytes
     for (int idx = threadIdx.x; idx < D * 8; idx += kThreads) {
       const int c = idx / 8, part = idx % 8;
-      uint4 w;
-      const uint8_t *s = &tile[c][part * 16];
-      w.x = s[0] | (s[1] << 8) | (s[2] << 16) | ((uint32_t)s[3] << 24);
-      w.y = s[4] | (s[5] << 8) | (s[6] << 16) | ((uint32_t)s[7] << 24);
-      w.z = s[8] | (s[9] << 8) | (s[10] << 16) | ((uint32_t)s[11] << 24);
-      w.w = s[12] | (s[13] << 8) | (s[14] << 16) | ((uint32_t)s[15] << 24);
+      const uint4 w = make_uint4(tile[c][4 * part], tile[c][4 * part + 1], tile[c][4 * part + 2], tile[c][4 * part + 3]);
       *reinterpret_cast<uint4 *>(a.vhat + ((size_t)hb * D + c) * a.M_pad + t0 + part * 16) = w;
     }
   }
