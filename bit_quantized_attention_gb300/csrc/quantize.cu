@@ -51,7 +51,19 @@ __device__ __forceinline__ float order_val(int k) { return __int_as_float(k >= 0
 
 __device__ __forceinline__ bool in_range(float f) { return fabsf(f) < 65536.0f; }  // false for NaN too
 
-__device__ __forceinline__ long long fixed24(float f) { return __float2ll_rz(__fmul_rn(f, 16777216.0f)); }
+// trunc(x * 2^24) toward zero for a bf16 x (its fp32 value f), from the bits:
+// x = (-1)^s * (128 + mant) * 2^(e - 134), so x * 2^24 = (128 + mant) * 2^(e - 110);
+// a right shift truncates the magnitude toward zero.  Zero and subnormals give 0;
+// inf / NaN (rejected by the range check) are clamped to keep the shift defined.
+__device__ __forceinline__ long long fixed24(float f) {
+  const uint32_t b = __float_as_uint(f) >> 16;
+  const int e = (int)((b >> 7) & 0xFF);
+  const long long m = (long long)((b & 0x7F) | 0x80);
+  const int sh = min(e - 110, 40);
+  long long a = (sh >= 0) ? (m << sh) : (sh > -8 ? (m >> -sh) : 0);
+  if (e == 0) a = 0;
+  return (b & 0x8000) ? -a : a;
+}
 
 __device__ __forceinline__ float mean_from_sum(long long sum, int n) {
   return __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(sum), 0x1p-24), (double)n));
@@ -192,6 +204,20 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
     atomicMin(&st.vmin[i], mn);
     atomicMax(&st.vmax[i], mx);
   }
+}
+
+// ------------------------------------------------------------------ finalize
+// One thread per (b, kv-head, channel): k_bar and V_m from the fixed-point
+// sums (when smoothed), and delta_V = max_t |fl(V - V_m)| / 448 from the channel
+// min and max (rounded subtraction is monotone).
+__global__ void finalize_kernel(StatsView st, int n, int M, int flags, float *kbar, float *vm, float *dv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  kbar[i] = (flags & SAGE_SMOOTH_K) ? mean_from_sum(st.ksum[i], M) : 0.0f;
+  const float mu = (flags & SAGE_SMOOTH_V) ? mean_from_sum(st.vsum[i], M) : 0.0f;
+  const float hi = order_val(st.vmax[i]), lo = order_val(st.vmin[i]);
+  vm[i] = mu;
+  dv[i] = __fdiv_rn(fmaxf(fabsf(__fsub_rn(hi, mu)), fabsf(__fsub_rn(lo, mu))), 448.0f);
 }
 
 // ------------------------------------------------------------------ quantize
@@ -356,18 +382,11 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   }
   cta -= a.nq;
   if (cta < a.nk) {
-    // ---- K block (b, g, j): mean over all tokens from the statistics pass
+    // ---- K block (b, g, j): k_bar over all tokens from the finalize pass
     const int j = cta % a.Tn, hb = cta / a.Tn;
-    __shared__ float kmean[D];
-    const bool smooth = (a.flags & SAGE_SMOOTH_K) != 0;
-    for (int c = threadIdx.x; c < D; c += kThreads)
-      kmean[c] = smooth ? mean_from_sum(a.st.ksum[(size_t)hb * D + c], a.M) : 0.0f;
-    __syncthreads();
-    if (j == 0)
-      for (int c = threadIdx.x; c < D; c += kThreads) a.kbar[(size_t)hb * D + c] = kmean[c];
     const int t0 = j * a.bk;
     const int valid = max(0, min(a.bk, a.M - t0));
-    quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, kmean,
+    quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, a.kbar + (size_t)hb * D,
                           a.khat + ((size_t)hb * a.M_pad + t0) * D * CB, a.dk + (size_t)hb * a.Tn + j, nullptr,
                           a.status, 1);
     return;
@@ -384,20 +403,11 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
     const int ch = cta % nchunk, hb = cta / nchunk;
     __shared__ float vmean[D], vdelta[D], vrcp[D];
     __shared__ uint32_t tile[D][33];
-    const bool smooth = (a.flags & SAGE_SMOOTH_V) != 0;
     for (int c = threadIdx.x; c < D; c += kThreads) {
       const size_t i = (size_t)hb * D + c;
-      const float mu = smooth ? mean_from_sum(a.st.vsum[i], a.M) : 0.0f;
-      const float hi = order_val(a.st.vmax[i]), lo = order_val(a.st.vmin[i]);
-      const float amax = fmaxf(fabsf(__fsub_rn(hi, mu)), fabsf(__fsub_rn(lo, mu)));
-      const float delta = __fdiv_rn(amax, 448.0f);
-      vmean[c] = mu;
-      vdelta[c] = delta;
-      vrcp[c] = __frcp_rn(delta);
-      if (ch == 0) {
-        a.vm[i] = mu;
-        a.dv[i] = delta;
-      }
+      vmean[c] = a.vm[i];
+      vdelta[c] = a.dv[i];
+      vrcp[c] = __frcp_rn(vdelta[c]);
     }
     __syncthreads();
     constexpr int VPR = D / 8;
@@ -443,12 +453,11 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
 
 }  // namespace
 
-sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
-                               const void *k, const void *v, void *ws, const sage_ws_layout &L,
-                               cudaStream_t stream) {
-  (void)bq;
+// Enqueue init, statistics, finalize and quantize on `stream`, with the
+// statistics scratch at `st`.
+static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, const void *q, const void *k,
+                              const void *v, void *ws, const sage_ws_layout &L, StatsView st, cudaStream_t stream) {
   char *w = (char *)ws;
-  StatsView st = stats_view(ws, L, s);
   int *status = (int *)(w + L.status);
   const int n = s.B * s.Hkv * s.d;
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
@@ -457,7 +466,8 @@ sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq,
     stats_kernel<64><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
   else
     stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
-
+  finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, s.M, flags, (float *)(w + L.kbar),
+                                                        (float *)(w + L.vm), (float *)(w + L.dv));
   QuantArgs a;
   a.q = (const uint4 *)q;
   a.k = (const uint4 *)k;
@@ -502,6 +512,13 @@ sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq,
       quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
+sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
+                               const void *k, const void *v, void *ws, const sage_ws_layout &L,
+                               cudaStream_t stream) {
+  (void)bq;
+  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, stats_view(ws, L, s), stream);
 }
 
 }  // namespace sage
@@ -561,59 +578,7 @@ sage_status launch_quantize_q8_static_scratch(const sage_shape &s, int mode, int
   st.vmin = (int *)(scratch + (size_t)n * 16);
   st.vmax = (int *)(scratch + (size_t)n * 20);
 
-  char *w = (char *)ws;
-  int *status = (int *)(w + L.status);
-  init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
-  dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
-  if (s.d == 64)
-    stats_kernel<64><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
-  else
-    stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
-
-  QuantArgs a;
-  a.q = (const uint4 *)q;
-  a.k = (const uint4 *)k;
-  a.v = (const uint4 *)v;
-  a.B = s.B;
-  a.Hq = s.Hq;
-  a.Hkv = s.Hkv;
-  a.N = s.N;
-  a.M = s.M;
-  a.N_pad = L.N_pad;
-  a.M_pad = L.M_pad;
-  a.Tm = L.Tm;
-  a.Tn = L.Tn;
-  a.bk = bk;
-  a.mode = mode;
-  a.flags = flags;
-  a.qhat = (uint8_t *)(w + L.qhat);
-  a.khat = (uint8_t *)(w + L.khat);
-  a.vhat = (uint8_t *)(w + L.vhat);
-  a.dq = (float *)(w + L.dq);
-  a.qbar = (float *)(w + L.qbar);
-  a.dk = (float *)(w + L.dk);
-  a.kbar = (float *)(w + L.kbar);
-  a.dv = (float *)(w + L.dv);
-  a.vm = (float *)(w + L.vm);
-  a.st = st;
-  a.status = status;
-  a.nq = s.B * s.Hq * L.Tm;
-  a.nk = s.B * s.Hkv * L.Tn;
-  const int nv = s.B * s.Hkv * (L.M_pad / 128);
-  const unsigned grid = (unsigned)(a.nq + a.nk + nv);
-  const bool i8 = (mode == SAGE_Q8_PV8);
-  if (s.d == 64) {
-    if (i8)
-      quantize_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
-  } else {
-    if (i8)
-      quantize_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
-  }
-  return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, st, stream);
 }
 
 }  // namespace sage
