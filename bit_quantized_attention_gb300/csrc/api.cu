@@ -84,7 +84,6 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
-  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
   return launch_quantize_q8(*shape, quant_mode, flags, bq, bk, q, k, v, workspace, L, (cudaStream_t)stream);
 }
 

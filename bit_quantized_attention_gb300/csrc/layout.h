@@ -72,7 +72,9 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   const bool fp4 = (mode == SAGE_NVFP4);
   L->qsf = take(fp4 ? (size_t)(B * Hq * N_pad * (d / 16)) : 0);
   L->ksf = take(fp4 ? (size_t)(B * Hkv * M_pad * (d / 16)) : 0);
-  L->vsf = take(fp4 ? (size_t)(B * Hkv * d * (M_pad / 16)) : 0);
+  // V scales: per (b, kv-head) ceil(d/128) atoms of 128 channel rows, each
+  // holding M_pad/16 token blocks
+  L->vsf = take(fp4 ? (size_t)(B * Hkv * cdiv(d, 128) * 128 * (M_pad / 16)) : 0);
   L->stats = take(stats_bytes(*s));
   L->status = take(16);
   L->total = off;

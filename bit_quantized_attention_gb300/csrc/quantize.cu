@@ -451,6 +451,206 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ NVFP4
+// phi of the SageAttention3 summary §3.4: per 1x16 block along the reduction
+// dimension, s = max|X| / 6 stored as E4M3, X^ = E2M1(X / s) with the stored s.
+// Codes are packed two per byte (element 2i in the low nibble).  Scales are
+// written as 512-byte atoms, one per 128 rows x 64 reduction elements: row r's
+// four block scales at byte (r % 32) * 16 + (r / 32) * 4 (the layout the
+// block-scaled MMA's scale copy reads).
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t h2 = cvt_e4m3x2_to_f16x2((uint16_t)(code & 0xFF));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// E2M1 codes of RN(x0 / d), RN(x1 / d) as one byte, exactly as
+// cvt(__fdiv_rn(x, d)) gives them (same bracket argument as e4m3_code2).
+__device__ __forceinline__ uint32_t e2m1_code2(float x0, float x1, float d, float rcp) {
+  const float q0 = __fmul_rn(x0, rcp), q1 = __fmul_rn(x1, rcp);
+  const float lo = 1.0f - 0x1p-19f, hi = 1.0f + 0x1p-19f;
+  const uint32_t a = cvt_e2m1x2(__fmul_rn(q0, lo), __fmul_rn(q1, lo));
+  const uint32_t b = cvt_e2m1x2(__fmul_rn(q0, hi), __fmul_rn(q1, hi));
+  if (a == b && isfinite(q0) && isfinite(q1)) return a;
+  return cvt_e2m1x2(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+}
+
+// scale byte of a block with absolute maximum amax: E4M3(fl(amax / 6))
+__device__ __forceinline__ uint32_t nvfp4_scale(float amax) {
+  const float t = __fdiv_rn(amax, 6.0f);
+  return cvt_e4m3x2(t, t) & 0xFF;
+}
+
+__device__ __forceinline__ size_t atom_off(int r, int blk) { return (size_t)(r & 31) * 16 + (r >> 5) * 4 + blk; }
+
+// 128 rows of a [*, D] bf16 matrix -> codes [128][D/2] and scale atoms
+// [D/64][512].  Mean: per-block (own_mean) or given (per channel) or none.
+template <int D>
+__device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, bool own_mean,
+                              const float *__restrict__ given_mean, uint8_t *codes, uint8_t *atoms,
+                              float *mean_out, int *status, int site) {
+  constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
+  __shared__ long long ssum[RPP][D];
+  __shared__ float smean[D];
+  const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  uint4 x[PASSES];
+  bool bad = false;
+#pragma unroll
+  for (int pp = 0; pp < PASSES; ++pp) {
+    const int r = rr + pp * RPP;
+    x[pp] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+  }
+  if (own_mean) {
+    long long sacc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int pp = 0; pp < PASSES; ++pp) {
+      if (rr + pp * RPP >= valid_rows) continue;
+      float f[8];
+      unpack_bf16x8(x[pp], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sacc[e] += fixed24(f[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ssum[rr][vc * 8 + e] = sacc[e];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+      long long a = 0;
+      for (int r = 0; r < RPP; ++r) a += ssum[r][c];
+      smean[c] = mean_from_sum(a, valid_rows);
+    }
+  } else {
+    for (int c = threadIdx.x; c < D; c += kThreads) smean[c] = given_mean ? given_mean[c] : 0.0f;
+  }
+  __syncthreads();
+  float mu[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mu[e] = smean[vc * 8 + e];
+#pragma unroll
+  for (int pp = 0; pp < PASSES; ++pp) {
+    const int r = rr + pp * RPP;
+    const bool valid = r < valid_rows;
+    float f[8], g[8];
+    unpack_bf16x8(x[pp], f);
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bad |= valid && !in_range(f[e]);
+      g[e] = __fsub_rn(f[e], mu[e]);
+      amax = fmaxf(amax, fabsf(g[e]));
+    }
+    // the 16-channel block is this thread's 8 and its neighbour's
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const uint32_t sc = valid ? nvfp4_scale(amax) : 0;
+    const float d = e4m3_value(sc);
+    uint32_t w = 0;
+    if (valid && d != 0.0f) {
+      const float rcp = __frcp_rn(d);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) w |= e2m1_code2(g[e], g[e + 1], d, rcp) << (4 * e);
+    }
+    *reinterpret_cast<uint32_t *>(codes + (size_t)r * (D / 2) + vc * 4) = w;
+    if ((vc & 1) == 0) {
+      const int grp = vc >> 1;  // 16-channel block index along the row
+      atoms[(size_t)(grp >> 2) * 512 + atom_off(r, grp & 3)] = (uint8_t)sc;
+    }
+  }
+  if (bad) raise_status(status, SAGE_ERR_RANGE, site);
+  if (mean_out)
+    for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
+}
+
+struct Fp4Args {
+  const uint4 *q, *k, *v;
+  int N, M, N_pad, M_pad, Tm, flags;
+  uint8_t *qhat, *khat, *vhat, *qsf, *ksf, *vsf;
+  const float *kbar, *vm;
+  float *qbar;
+  int *status;
+  int nq, nk;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
+  int cta = blockIdx.x;
+  if (cta < a.nq) {
+    // ---- Q block (b, h, i) of 128 rows, optional per-block mean
+    const int i = cta % a.Tm, bh = cta / a.Tm;
+    const int r0 = i * 128;
+    const int valid = max(0, min(128, a.N - r0));
+    fp4_row_block<D>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, (a.flags & SAGE_SMOOTH_Q) && valid > 0,
+                     nullptr, a.qhat + ((size_t)bh * a.N_pad + r0) * (D / 2),
+                     a.qsf + ((size_t)bh * a.Tm + i) * (D / 64) * 512, a.qbar + ((size_t)bh * a.Tm + i) * D,
+                     a.status, 3);
+    return;
+  }
+  cta -= a.nq;
+  const int nchunk = a.M_pad / 128;
+  if (cta < a.nk) {
+    // ---- K block (b, g, 128 rows) with k_bar over all tokens
+    const int ch = cta % nchunk, hb = cta / nchunk;
+    const int t0 = ch * 128;
+    const int valid = max(0, min(128, a.M - t0));
+    fp4_row_block<D>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, false, a.kbar + (size_t)hb * D,
+                     a.khat + ((size_t)hb * a.M_pad + t0) * (D / 2),
+                     a.ksf + ((size_t)hb * nchunk + ch) * (D / 64) * 512, nullptr, a.status, 1);
+    return;
+  }
+  cta -= a.nk;
+  // ---- V chunk (b, g, 128 tokens): 1x16 blocks along tokens per channel,
+  // codes transposed (token-contiguous per channel, two tokens per byte)
+  {
+    const int ch = cta % nchunk, hb = cta / nchunk;
+    const int t0 = ch * 128;
+    constexpr int VPR = D / 8, RPP = kThreads / VPR;
+    constexpr int CA = (D + 127) / 128;  // channel atoms
+    __shared__ __nv_bfloat16 tile[128][D + 2];
+    __shared__ float vmean[D];
+    for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
+    const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+    for (int r = rr; r < 128; r += RPP) {
+      const int t = t0 + r;
+      const uint4 u = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + vc] : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        *reinterpret_cast<uint32_t *>(&tile[r][vc * 8 + 2 * e]) = w[e];
+    }
+    __syncthreads();
+    for (int item = threadIdx.x; item < D * 8; item += kThreads) {
+      const int c = item % D, tb = item / D;  // channel, 16-token block of the chunk
+      float g[16], amax = 0.0f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int t = t0 + tb * 16 + u;
+        g[u] = (t < a.M) ? __fsub_rn(__bfloat162float(tile[tb * 16 + u][c]), vmean[c]) : 0.0f;
+        amax = fmaxf(amax, fabsf(g[u]));
+      }
+      const bool any = t0 + tb * 16 < a.M;
+      const uint32_t sc = any ? nvfp4_scale(amax) : 0;
+      const float d = e4m3_value(sc);
+      uint32_t w0 = 0, w1 = 0;
+      if (d != 0.0f) {
+        const float rcp = __frcp_rn(d);
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+          const int t = t0 + tb * 16 + u;
+          w0 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * u);
+        }
+#pragma unroll
+        for (int u = 8; u < 16; u += 2) {
+          const int t = t0 + tb * 16 + u;
+          w1 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * (u - 8));
+        }
+      }
+      // a token past M inside a pair contributes a zero nibble (its value is 0 anyway)
+      *reinterpret_cast<uint2 *>(a.vhat + ((size_t)hb * D + c) * (a.M_pad / 2) + (t0 + tb * 16) / 2) =
+          make_uint2(w0, w1);
+      const int ts = (t0 + tb * 16) / 64, blk = ((t0 + tb * 16) % 64) / 16;
+      a.vsf[(((size_t)hb * CA + c / 128) * (a.M_pad / 64) + ts) * 512 + atom_off(c % 128, blk)] = (uint8_t)sc;
+    }
+  }
+}
+
 }  // namespace
 
 // Enqueue init, statistics, finalize and quantize on `stream`, with the
@@ -468,6 +668,38 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
     stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
   finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, s.M, flags, (float *)(w + L.kbar),
                                                         (float *)(w + L.vm), (float *)(w + L.dv));
+  if (mode == SAGE_NVFP4) {
+    Fp4Args f;
+    f.q = (const uint4 *)q;
+    f.k = (const uint4 *)k;
+    f.v = (const uint4 *)v;
+    f.N = s.N;
+    f.M = s.M;
+    f.N_pad = L.N_pad;
+    f.M_pad = L.M_pad;
+    f.Tm = L.Tm;
+    f.flags = flags;
+    f.qhat = (uint8_t *)(w + L.qhat);
+    f.khat = (uint8_t *)(w + L.khat);
+    f.vhat = (uint8_t *)(w + L.vhat);
+    f.qsf = (uint8_t *)(w + L.qsf);
+    f.ksf = (uint8_t *)(w + L.ksf);
+    f.vsf = (uint8_t *)(w + L.vsf);
+    f.kbar = (const float *)(w + L.kbar);
+    f.vm = (const float *)(w + L.vm);
+    f.qbar = (float *)(w + L.qbar);
+    f.status = status;
+    f.nq = s.B * s.Hq * L.Tm;
+    f.nk = s.B * s.Hkv * (L.M_pad / 128);
+    const unsigned g4 = (unsigned)(f.nq + 2 * f.nk);  // Q blocks, K blocks, V chunks
+    // the V-scale atoms of d = 64 use half their rows: clear them first
+    if (s.d % 128 != 0 && cudaMemsetAsync(f.vsf, 0, L.stats - L.vsf, stream) != cudaSuccess) return SAGE_ERR_CUDA;
+    if (s.d == 64)
+      quantize_fp4_kernel<64><<<g4, kThreads, 0, stream>>>(f);
+    else
+      quantize_fp4_kernel<128><<<g4, kThreads, 0, stream>>>(f);
+    return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+  }
   QuantArgs a;
   a.q = (const uint4 *)q;
   a.k = (const uint4 *)k;

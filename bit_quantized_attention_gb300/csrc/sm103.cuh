@@ -224,6 +224,16 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Two floats to one byte of two E2M1 codes (round to nearest even, saturate
+// to +-6): lo in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Two E4M3 bytes (low byte first) to two fp16 values.
 __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;

@@ -44,6 +44,73 @@ def read_workspace(ws, mode: int) -> dict:
     )
 
 
+def _nibbles(b: np.ndarray) -> np.ndarray:
+    """packed bytes [..., n] -> E2M1 codes [..., 2n] (element 2i in the low nibble)"""
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+def _atom_scales(atoms: np.ndarray, rows: int, groups: int) -> np.ndarray:
+    """scale atoms [tiles, groups/4, 512] -> scales [tiles*128 rows, groups]:
+    row r's four block scales of an atom sit at (r % 32) * 16 + (r / 32) * 4"""
+    tiles = atoms.shape[0]
+    r = np.arange(128)
+    out = np.empty((tiles, 128, groups), np.uint8)
+    for g in range(groups):
+        out[:, :, g] = atoms[:, g // 4, (r % 32) * 16 + (r // 32) * 4 + (g % 4)]
+    return out.reshape(tiles * 128, groups)[:rows]
+
+
+def read_workspace_fp4(ws) -> dict:
+    """NVFP4 workspace -> oracle logical layouts (qc/kc/vc nibbles, qs/ks/vs scales)."""
+    s, L = ws.shape, ws.layout
+    B, Hq, Hkv, N, M, d = s.B, s.Hq, s.Hkv, s.N, s.M, s.d
+    Np, Mp, Tm = L.N_pad, L.M_pad, L.Tm
+    G = d // 16
+    qc = _nibbles(_np(ws.region("qhat", B * Hq * Np * d // 2)).reshape(B, Hq, Np, d // 2))[:, :, :N]
+    kc = _nibbles(_np(ws.region("khat", B * Hkv * Mp * d // 2)).reshape(B, Hkv, Mp, d // 2))[:, :, :M]
+    vt = _nibbles(_np(ws.region("vhat", B * Hkv * d * Mp // 2)).reshape(B, Hkv, d, Mp // 2))[..., :M]
+    qa = _np(ws.region("qsf", B * Hq * Tm * (d // 64) * 512)).reshape(B * Hq, Tm, d // 64, 512)
+    qs = np.stack([_atom_scales(qa[i], N, G) for i in range(B * Hq)]).reshape(B, Hq, N, G)
+    ka = _np(ws.region("ksf", B * Hkv * (Mp // 128) * (d // 64) * 512)).reshape(B * Hkv, Mp // 128, d // 64, 512)
+    ks = np.stack([_atom_scales(ka[i], M, G) for i in range(B * Hkv)]).reshape(B, Hkv, M, G)
+    CA = -(-d // 128)
+    va = _np(ws.region("vsf", B * Hkv * CA * (Mp // 64) * 512)).reshape(B * Hkv, CA, Mp // 64, 512)
+    Mt16 = -(-M // 16)
+    vs = np.empty((B * Hkv, Mt16, d), np.uint8)
+    c = np.arange(d)
+    for tb in range(Mt16):
+        ts, blk = tb // 4, tb % 4
+        rr = c % 128
+        vs[:, tb, :] = va[:, c // 128, ts, (rr % 32) * 16 + (rr // 32) * 4 + blk]
+    f32 = lambda name, n: _np(ws.region(name, 4 * n).view(torch.float32))
+    return dict(qc=np.ascontiguousarray(qc), kc=np.ascontiguousarray(kc),
+                vc=np.ascontiguousarray(vt.transpose(0, 1, 3, 2)), qs=qs, ks=ks,
+                vs=vs.reshape(B, Hkv, Mt16, d),
+                qbar=f32("qbar", B * Hq * Tm * d).reshape(B, Hq, Tm, d),
+                kbar=f32("kbar", B * Hkv * d).reshape(B, Hkv, d),
+                vm=f32("vm", B * Hkv * d).reshape(B, Hkv, d))
+
+
+def compare_codes_fp4(got: dict, ref) -> dict:
+    def fold(c):  # -0 (0x8) and +0 both encode zero
+        c = c.copy()
+        c[c == 0x8] = 0
+        return c
+
+    def bits(a):
+        return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+    return dict(qc=np.array_equal(fold(got["qc"]), fold(ref.qc)), kc=np.array_equal(fold(got["kc"]), fold(ref.kc)),
+                vc=np.array_equal(fold(got["vc"]), fold(ref.vc)), qs=np.array_equal(got["qs"], ref.qs),
+                ks=np.array_equal(got["ks"], ref.ks), vs=np.array_equal(got["vs"], ref.vs),
+                qbar=np.array_equal(bits(got["qbar"]), bits(ref.qbar)),
+                kbar=np.array_equal(bits(got["kbar"]), bits(ref.kbar)),
+                vm=np.array_equal(bits(got["vm"]), bits(ref.vm)))
+
+
 def vt_pad(ws, B, Hkv, d, Mp, M):
     vt = _np(ws.region("vhat", B * Hkv * d * Mp)).reshape(B, Hkv, d, Mp)
     return vt[..., M:]

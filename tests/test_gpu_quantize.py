@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import compare_codes, read_workspace
+from gpu_helpers import compare_codes, compare_codes_fp4, read_workspace, read_workspace_fp4
 from workload import CONFIGS, make_inputs
 from workload.configs import Config
 
@@ -101,4 +101,40 @@ def test_quantize_bit_exact_full_size_sampled_heads(sage, name):
                      (val[b:b + 1, g:g + 1] if key in ("kc", "dk", "kbar", "vc", "dv", "vm") else val))
                for key, val in got.items()}
         res = compare_codes(sub, ref, cfg.mode, cfg.flags)
+        assert all(res.values()), (b, g, res)
+
+
+FP4_SMALL = [
+    _small("fp4_tiny", mode=2, flags=1, bk=128),
+    _small("fp4_ragged_all_smooth", mode=2, flags=7, N=200, M=333, bk=128),
+    _small("fp4_d128_gqa", mode=2, flags=3, B=2, Hq=4, Hkv=2, N=130, M=515, d=128, bk=128,
+           k_outliers=2, k_outlier_shift=20.0),
+    _small("fp4_single_token", mode=2, flags=5, N=1, M=1, bk=128),
+]
+
+
+@pytest.mark.parametrize("cfg", FP4_SMALL, ids=[c.name for c in FP4_SMALL])
+def test_quantize_fp4_bit_exact_small(sage, cfg):
+    q, k, v = make_inputs(cfg)
+    ws = _run(sage, cfg, q, k, v)
+    got = read_workspace_fp4(ws)
+    ref = oracle.quantize((cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d), cfg.mode, cfg.flags, cfg.bq, cfg.bk,
+                          q, k, v)
+    res = compare_codes_fp4(got, ref)
+    assert all(res.values()), res
+
+
+def test_quantize_fp4_bit_exact_full_size_sampled_heads(sage):
+    cfg = CONFIGS["nvfp4"].with_(bk=128)
+    q, k, v = make_inputs(cfg)
+    ws = _run(sage, cfg, q, k, v)
+    got = read_workspace_fp4(ws)
+    G = cfg.Hq // cfg.Hkv
+    for b, g in {(0, 0), (cfg.B - 1, cfg.Hkv - 1)}:
+        hs = slice(g * G, (g + 1) * G)
+        qs, ks, vs = q[b:b + 1, hs].contiguous(), k[b:b + 1, g:g + 1].contiguous(), v[b:b + 1, g:g + 1].contiguous()
+        ref = oracle.quantize((1, G, 1, cfg.N, cfg.M, cfg.d), cfg.mode, cfg.flags, cfg.bq, cfg.bk, qs, ks, vs)
+        sub = {key: (val[b:b + 1, hs] if key in ("qc", "qs", "qbar") else val[b:b + 1, g:g + 1])
+               for key, val in got.items()}
+        res = compare_codes_fp4(sub, ref)
         assert all(res.values()), (b, g, res)
