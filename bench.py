@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_FP8_OVER_BF16 = 2.0   # dense fp8 / dense bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+NOMINAL_FP4_OVER_BF16 = 6.0   # dense fp4 / dense bf16 tensor rate (13.5 / 2.25 PFLOP/s)
+LAUNCHES_PER_STEP = 5         # init, statistics, finalize, quantize, attention
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -55,7 +57,30 @@ def attention_peak(mode: int, bf16_tflops: float):
         return 2.0 / (1.0 / bf16_tflops + 1.0 / fp8), "kind::f16 (QK) + kind::f8f6f4 (PV)"
     if mode == 1:
         return fp8, "kind::f8f6f4"
-    return fp8 * 2.0, "kind::mxf4nvf4 (nominal 2x fp8)"
+    return bf16_tflops * NOMINAL_FP4_OVER_BF16, "kind::mxf4nvf4.block_scale (QK and PV)"
+
+
+def peak_source(mode: int, src: str, bf16: float) -> str:
+    ratio = {0: "nominal fp8/bf16 ratio %.0f (harmonic mean of bf16 and fp8)" % NOMINAL_FP8_OVER_BF16,
+             1: "nominal fp8/bf16 ratio %.0f" % NOMINAL_FP8_OVER_BF16,
+             2: "nominal fp4/bf16 ratio %.0f" % NOMINAL_FP4_OVER_BF16}[mode]
+    return "%s bf16 burst %.1f TFLOP/s x %s" % (src, bf16, ratio)
+
+
+ATTN_KERNEL = {0: "attn_q8_kernel", 1: "attn_q8_kernel", 2: "attn_fp4_kernel"}
+
+
+def read_traffic(key: str):
+    """DRAM bytes per attention launch recorded from an ncu capture, or None when
+    the kernel sources changed since (lines: key kernel_hash bytes)."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == key and parts[1] == kernel_hash():
+            return float(parts[2])
+    return None
 
 
 class ClockSampler:
@@ -306,12 +331,7 @@ def run_gpu(args, cfg):
     bf16, bf16_sus, hbm, src = peaks()
     peak, kinds = attention_peak(cfg.mode, bf16)
     achieved = cfg.ops / (attn_ms * 1e-3) / 1e12
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "attn_traffic.json")
-    if os.path.exists(tf):
-        rec = json.load(open(tf)).get(cfg.name + "_bk%d" % cfg.bk)
-        if rec and rec.get("kernel_hash") == kernel_hash():
-            traffic = rec["bytes_per_launch"]
+    traffic = read_traffic(cfg.name + "_bk%d" % cfg.bk)
     out = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -319,12 +339,11 @@ def run_gpu(args, cfg):
         "config": workload_config(cfg),
         "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "attn_q8_kernel (sage_attn_fwd)", "instructions": kinds,
-                     "peak_source": "%s bf16 burst %.1f TFLOP/s x nominal fp8/bf16 ratio %.0f" % (
-                         src, bf16, NOMINAL_FP8_OVER_BF16),
+                     "kernel": ATTN_KERNEL[cfg.mode] + " (sage_attn_fwd)", "instructions": kinds,
+                     "peak_source": peak_source(cfg.mode, src, bf16),
                      "attn_ms": attn_ms},
         "attn_only_tops": achieved,
         "prepass_ms": ms_per_step - attn_ms,
@@ -347,6 +366,8 @@ def kernel_hash() -> str:
     import hashlib
     h = hashlib.sha1()
     for f in sorted(os.listdir(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc"))):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         h.update(open(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 

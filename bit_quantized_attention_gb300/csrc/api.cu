@@ -97,7 +97,8 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
   if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
   if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
-  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  if (quant_mode == SAGE_NVFP4)
+    return launch_attn_fp4(*shape, causal, sm_scale, flags, bk, workspace, L, o, (cudaStream_t)stream);
   return launch_attn_q8(*shape, causal, sm_scale, quant_mode, flags, bk, workspace, L, o, (cudaStream_t)stream);
 }
 

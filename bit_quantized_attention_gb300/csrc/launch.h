@@ -22,6 +22,10 @@ sage_status launch_quantize_q8_static_scratch(const sage_shape &s, int mode, int
 sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
                            const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream);
 
+// Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
+sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
+                            const sage_ws_layout &L, void *o, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (api.cu).
 // A 2-D byte tensor [rows][cols] with row pitch `pitch` bytes, box {box_cols, box_rows}.
 sage_status make_tmap_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t pitch,

@@ -74,6 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
 }
 
 // ----------------------------------------------------------------- TMA
+// Plain bulk copy global -> shared completing on an mbarrier (both addresses
+// 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gmem), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
   asm volatile(
@@ -174,8 +182,8 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // Shared-memory matrix descriptor for a K-major operand in a swizzled layout:
 // start address, leading offset (unused for swizzled K-major, set to 1),
 // stride between 8-row groups, the fixed tcgen05 descriptor version bit, and
-// the layout type (2 = 128-byte swizzle, 4 = 64-byte swizzle).
-enum : int { kSwizzle128 = 2, kSwizzle64 = 4 };
+// the layout type (2 = 128-byte swizzle, 4 = 64-byte, 6 = 32-byte).
+enum : int { kSwizzle128 = 2, kSwizzle64 = 4, kSwizzle32 = 6 };
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes, int layout) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
@@ -209,6 +217,33 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
+// Block-scaled E2M1 x E2M1 MMA with one UE4M3 scale per 16 elements along K
+// (K = 64 per instruction): the scale factors of A and B are read from TMEM
+// at sfa / sfb, four columns each for 128 rows.
+__device__ __forceinline__ void mma_fp4_bs(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb));
+}
+// Block-scaled instruction descriptor for E2M1 operands (format code 1 at
+// bits 7-9 and 10-12) with UE4M3 scales (bit 23 clear) and scale-factor ids 0.
+__host__ __device__ constexpr uint32_t instr_desc_fp4(int n, int m) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// Copy 32 rows x 16 bytes of shared memory (rows 16 bytes apart) into four
+// TMEM columns of lanes 0-31, repeated in every lane quadrant.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(128u >> 4) << 32;  // 8-row groups 128 bytes apart
+  d |= (uint64_t)1u << 46;
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
 // Arrive (once) on `bar` when every MMA this thread issued so far has finished.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -234,6 +269,29 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return r;
 }
 
+// Eight floats to four bytes of E2M1 codes (element 2i in the low nibble of
+// byte i), round to nearest even, saturating to +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float x0, float x1, float x2, float x3, float x4, float x5, float x6,
+                                               float x7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(x4), "f"(x5), "f"(x6), "f"(x7));
+  return r;
+}
+// Four bytes of E2M1 codes to eight fp16 values (two per word, low nibble first).
+__device__ __forceinline__ void cvt_e2m1x8_to_f16(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
 // Two E4M3 bytes (low byte first) to two fp16 values.
 __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
@@ -245,6 +303,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

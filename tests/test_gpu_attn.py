@@ -1,10 +1,13 @@
-"""GPU attention parity against the oracle (INT8 / FP8 modes).
+"""GPU attention parity against the oracle (INT8 / FP8 / NVFP4 modes).
 
 Bar (per element, the method's output in bf16): max|dO| <= 1e-2 * max|O| and
 mean relative L1 <= 2e-3 against the oracle's output rounded to bf16, on the
 same quantized workspace; and cosine >= 0.999 against unquantized fp64
 attention for INT8 Q/K (0.998 for the E4M3 Q/K mode, whose 3-bit mantissas
-cost that much on these inputs in the oracle itself).
+cost that much on these inputs in the oracle itself).  NVFP4 keeps the same
+bar against the oracle; against fp64 attention its cosine must reach 0.975 and
+fall no more than 2e-3 below the oracle's own (E2M1 with 16-element blocks
+loses that much on Gaussian inputs in the oracle too).
 Small cases compare every row; the full-size workloads compare sampled rows:
 the first and last query blocks of two heads plus scattered rows.
 """
@@ -14,7 +17,7 @@ import torch
 
 import oracle
 from gpu_helpers import output_metrics
-from test_gpu_quantize import SMALL, _small
+from test_gpu_quantize import FP4_SMALL, SMALL, _small
 from workload import CONFIGS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +28,14 @@ ATTN_SMALL = SMALL + [
     _small("causal_gqa_ragged", B=1, Hq=4, Hkv=1, N=131, M=4000, causal=True, flags=7, d=128),
     _small("long_keys", N=128, M=8192, flags=1, d=64, bk=128),
     _small("fp8_causal", mode=1, N=256, M=300, causal=True, flags=7, d=128),
+]
+
+FP4_ATTN_SMALL = FP4_SMALL + [
+    _small("fp4_causal_square", mode=2, N=384, M=384, causal=True, flags=1, d=128, bk=128),
+    _small("fp4_causal_bottom_right", mode=2, N=200, M=777, causal=True, flags=3, d=128, bk=128),
+    _small("fp4_causal_gqa_ragged", mode=2, B=1, Hq=4, Hkv=1, N=131, M=2000, causal=True, flags=7, d=64,
+           bk=128),
+    _small("fp4_long_keys", mode=2, N=128, M=4096, flags=1, d=128, bk=128),
 ]
 
 
@@ -57,13 +68,23 @@ def check(cfg, got_rows, q, k, v, rows, threads=None):
     if exact is not None:
         e = output_metrics(got_rows, exact)
         o = output_metrics(ref, exact)
-        bar = 0.999 if cfg.mode == 0 else 0.998
+        bar = {0: 0.999, 1: 0.998, 2: 0.975}[cfg.mode]
         assert e["cos"] >= bar, (e, o)
+        if cfg.mode == 2:
+            assert e["cos"] >= o["cos"] - 2e-3, (e, o)
     return m
 
 
 @pytest.mark.parametrize("cfg", ATTN_SMALL, ids=[c.name for c in ATTN_SMALL])
 def test_attention_matches_oracle_small(sage, cfg):
+    q, k, v = make_inputs(cfg)
+    o = gpu_attention(sage, cfg, q, k, v)
+    rows = oracle.all_rows((cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d))
+    check(cfg, o.reshape(-1, cfg.d), q, k, v, rows)
+
+
+@pytest.mark.parametrize("cfg", FP4_ATTN_SMALL, ids=[c.name for c in FP4_ATTN_SMALL])
+def test_attention_fp4_matches_oracle_small(sage, cfg):
     q, k, v = make_inputs(cfg)
     o = gpu_attention(sage, cfg, q, k, v)
     rows = oracle.all_rows((cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d))
@@ -90,7 +111,7 @@ def sampled_rows(cfg, rng, extra=64):
 
 
 @pytest.mark.parametrize("name,bk", [("llm_prefill", 64), ("llm_prefill", 128), ("video", 64),
-                                     ("chunked_gqa", 64), ("chunked_gqa", 128)])
+                                     ("chunked_gqa", 64), ("chunked_gqa", 128), ("nvfp4", 128)])
 def test_attention_full_size_sampled_rows(sage, name, bk):
     cfg = CONFIGS[name].with_(bk=bk)
     q, k, v = make_inputs(cfg)
