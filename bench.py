@@ -382,6 +382,8 @@ def main():
     ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
+    ap.add_argument("--heads", type=int, default=0, help="override Hq (Hkv scaled to keep the group size)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -389,6 +391,13 @@ def main():
     cfg = CONFIGS[args.workload]
     if args.bk:
         cfg = cfg.with_(bk=args.bk)
+    if args.batch:
+        cfg = cfg.with_(B=args.batch)
+    if args.heads:
+        g = cfg.Hq // cfg.Hkv
+        if args.heads % g:
+            ap.error("--heads must be a multiple of the workload's group size %d" % g)
+        cfg = cfg.with_(Hq=args.heads, Hkv=args.heads // g)
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -19,12 +19,14 @@
 //
 // Warps: WG0 and WG1 run the softmax and the two-level P quantization of the
 // same 128 query rows, WG0 on keys 0-63 of each tile and WG1 on keys 64-127
-// (one row per thread, its TMEM lane; the two halves trade row maxima through
-// shared memory).  WG2 does the two-level accumulation O = alpha O + s_P1 R
-// with O held in TMEM, then the epilogue.  Warp 12 issues the TMA and bulk
-// copies, warp 13 (one thread) the tcgen05.cp of scale factors into TMEM and
-// the block-scaled tcgen05.mma.  The S/R region and the P^ buffer are
-// double-buffered so QK of tile j+1 runs under the softmax of tile j.
+// (one row per thread, its TMEM lane; the halves trade their maxima through
+// shared memory, late enough that neither waits).  WG2 does the two-level accumulation O = alpha O + s_P1 R
+// with its row of O held in registers, then the epilogue.  Warp 12 issues the
+// TMA and bulk copies; warp 13 issues QK (the scale-factor copies into TMEM
+// and the block-scaled tcgen05.mma) and warp 14 issues PV, one elected lane
+// each.  Three S/R regions in TMEM (R of tile j overwrites S of tile j) let
+// QK run up to three tiles ahead of the accumulation, so neither the MMAs nor
+// the accumulation sit on the softmax's critical path.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,17 +41,17 @@ namespace {
 
 constexpr int kWG = 128;
 constexpr int kThreads = 512;
-constexpr int kCorrWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
-constexpr int kLaunchRegs = 128, kSoftmaxRegs = 184, kCorrRegs = 88, kControlRegs = 56;
+constexpr int kCorrWarp0 = 8, kProducerWarp = 12, kQkWarp = 13, kPvWarp = 14;
+constexpr int kLaunchRegs = 128, kSoftmaxRegs = 136, kCorrRegs = 184, kControlRegs = 56;
 static_assert(kWG * (2 * kSoftmaxRegs + kCorrRegs + kControlRegs) <= kThreads * kLaunchRegs, "register split");
-static_assert(kSoftmaxRegs >= kLaunchRegs && kCorrRegs <= kLaunchRegs && kControlRegs <= kLaunchRegs,
+static_assert(kSoftmaxRegs >= kLaunchRegs && kCorrRegs >= kLaunchRegs && kControlRegs <= kLaunchRegs,
               "register split directions");
+constexpr int NB = 3;         // S/R regions, P^ buffers
 constexpr int BK = 128;       // keys per tile
 constexpr int HALF = BK / 2;  // keys per softmax warpgroup
 constexpr float kLog2_2688 = 11.392317422778762f;
-// named barriers (0 is __syncthreads)
-constexpr int kBarDs0 = 1;  // + half: dS of one warpgroup's keys
-constexpr int kBarMax = 3;  // both softmax warpgroups: row-max exchange
+// named barriers (0 is __syncthreads): 1 + half, one softmax warpgroup (dS)
+constexpr int kBarDs0 = 1;
 
 template <int D>
 struct Fp4Cfg {
@@ -64,21 +66,21 @@ struct Fp4Cfg {
   static constexpr int P_BYTES = 128 * (BK / 2);
   static constexpr int PSF_BYTES = (BK / 64) * 512;
   static constexpr int STAGE = K_BYTES + QSF_BYTES + V_BYTES + VSF_BYTES;
-  static constexpr int FIXED = Q_BYTES + QSF_BYTES + 2 * (P_BYTES + PSF_BYTES);
+  static constexpr int FIXED = Q_BYTES + QSF_BYTES + NB * (P_BYTES + PSF_BYTES);
   static constexpr int STAGES = 4;
-  static constexpr int NFLOAT = 2 * 128 /*alpha*/ + 2 * 128 /*s_P1*/ + 2 * 128 /*l*/ + 4 * 128 /*max*/ + 2 * D +
-                                2 * BK /*dS*/;
-  static constexpr int SMEM_TOTAL = 1024 + FIXED + STAGES * STAGE + NFLOAT * 4 + 256;
+  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 128 /*s_P1*/ + 2 * 128 /*l*/ + 4 * 128 /*max*/ +
+                                2 * D + 4 * BK /*dS*/;
+  static constexpr int SMEM_TOTAL = 1024 + FIXED + STAGES * STAGE + NFLOAT * 4 + 512;
   static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory");
-  // TMEM columns: two S/R regions, O, scale factors (4 columns per 64-wide K step)
+  // TMEM columns: NB S/R regions, then scale factors, 4 columns per 64-wide K
+  // step; K, P and V scale slots follow the S/R region of their tile
   static constexpr int SRW = 128;
-  static constexpr int T_O = 2 * SRW;
-  static constexpr int T_SFQ = 384;        // [D/64 steps]
-  static constexpr int T_SFK = T_SFQ + 8;  // [2 buffers][D/64 steps]
-  static constexpr int T_SFP = T_SFK + 16; // [2][BK/64]
-  static constexpr int T_SFV = T_SFP + 16; // [2][BK/64]
+  static constexpr int T_SFQ = NB * SRW;           // [D/64 steps]
+  static constexpr int T_SFK = T_SFQ + 8;          // [NB][D/64 steps]
+  static constexpr int T_SFP = T_SFK + 8 * NB;     // [NB][BK/64]
+  static constexpr int T_SFV = T_SFP + 8 * NB;     // [NB][BK/64]
   static constexpr int TMEM_COLS = 512;
-  static_assert(T_SFV + 16 <= TMEM_COLS, "TMEM columns");
+  static_assert(T_SFV + 8 * NB <= TMEM_COLS, "TMEM columns");
 };
 
 // byte offset of 16-byte chunk c of row r in a swizzled tile with SW-byte rows
@@ -111,31 +113,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sQ = base;
-  uint8_t *sP = sQ + C::Q_BYTES;              // [2]
-  uint8_t *sK = sP + 2 * C::P_BYTES;          // [ST]
+  uint8_t *sP = sQ + C::Q_BYTES;              // [NB]
+  uint8_t *sK = sP + NB * C::P_BYTES;         // [ST]
   uint8_t *sV = sK + ST * C::K_BYTES;         // [ST]
   uint8_t *sQsf = sV + ST * C::V_BYTES;
-  uint8_t *sPsf = sQsf + C::QSF_BYTES;        // [2]
-  uint8_t *sKsf = sPsf + 2 * C::PSF_BYTES;    // [ST]
+  uint8_t *sPsf = sQsf + C::QSF_BYTES;        // [NB]
+  uint8_t *sKsf = sPsf + NB * C::PSF_BYTES;   // [ST]
   uint8_t *sVsf = sKsf + ST * C::QSF_BYTES;   // [ST]
-  float *s_alpha = (float *)(sVsf + ST * C::VSF_BYTES);  // [2][128]
-  float *s_sp1 = s_alpha + 2 * 128;                      // [2][128]
-  float *s_l = s_sp1 + 2 * 128;                          // [2 halves][128]
-  float *s_mx = s_l + 2 * 128;                           // [2 buffers][2 halves][128]
+  float *s_alpha = (float *)(sVsf + ST * C::VSF_BYTES);  // [NB][128]
+  float *s_sp1 = s_alpha + NB * 128;                     // [NB][128]
+  float *s_l = s_sp1 + NB * 128;                         // [2 halves][128]
+  float *s_mx = s_l + 2 * 128;                           // [2 parities][2 halves][128]
   float *s_vm = s_mx + 4 * 128;                          // [D]
   float *s_qbar = s_vm + D;                              // [D]
-  float *s_dsc = s_qbar + D;                             // [2 buffers][BK]
-  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 2 * BK) + 7) & ~(uintptr_t)7);
+  float *s_dsc = s_qbar + D;                             // [2 buffers][2 halves][BK]
+  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 4 * BK) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
   uint64_t *k_full = q_full + 1;     // [ST]
   uint64_t *v_full = k_full + ST;    // [ST]
   uint64_t *kv_empty = v_full + ST;  // [ST]
-  uint64_t *s_full = kv_empty + ST;  // [2]
-  uint64_t *p_full = s_full + 2;     // [2]
-  uint64_t *r_full = p_full + 2;     // [2]
-  uint64_t *sr_free = r_full + 2;    // [2]
-  uint64_t *mma_done = sr_free + 2;
-  uint32_t *s_tmem = (uint32_t *)(mma_done + 1);
+  uint64_t *s_full = kv_empty + ST;  // [NB]
+  uint64_t *p_full = s_full + NB;    // [NB]
+  uint64_t *r_full = p_full + NB;    // [NB]
+  uint64_t *sr_free = r_full + NB;   // [NB]
+  uint64_t *mx_full = sr_free + NB;  // [2 parities][2 halves]
+  uint64_t *qk_done = mx_full + 4;
+  uint64_t *pv_done = qk_done + 1;
+  uint32_t *s_tmem = (uint32_t *)(pv_done + 1);
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,17 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < NB; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 2 * kWG);
       mbar_init(&r_full[x], 1);
       mbar_init(&sr_free[x], kWG);
     }
-    mbar_init(mma_done, 1);
+    for (int x = 0; x < 4; ++x) mbar_init(&mx_full[x], kWG);
+    mbar_init(qk_done, 1);
+    mbar_init(pv_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -211,128 +217,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&k_full[s], n & 1, status, 11, &no_abort, p.spin);
         mbar_wait(&v_full[s], n & 1, status, 11, &no_abort, p.spin);
       }
-    } else if (warp == kMmaWarp && lane == 0) {
-      // ---------------------------------------------------------- tcgen05 issuer
-      // Scale-factor columns are double-buffered by tile parity: the copy for
-      // tile j overwrites what tile j-2 used, and every MMA of tile j-2 has
-      // completed by then (the sr_free wait of tile j-2 implies it).
-      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV), p_base = smem_u32(sP);
-      bool ok = mbar_wait(q_full, 0, status, 23, s_abort, p.spin);
+    } else if (warp == kQkWarp) {
+      // ---------------------------------------------------------- QK issuer (whole warp, one lane issues)
+      // QK of tile j reuses S/R region j % NB and K scale slot j % NB once the
+      // accumulation has consumed R of tile j - NB, which also means every
+      // MMA that read them has completed.
+      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, status, 23, s_abort, p.spin));
       tc_fence_after();
-      if (ok)
+      if (ok && elect_one())
         for (int a = 0; a < D / 64; ++a) tmem_cp_32x128b_x4(tmem + C::T_SFQ + 4 * a, smem_u32(sQsf + a * 512));
-      auto issue_pv = [&](int jj) -> bool {
-        const int bb = jj & 1, s = jj % ST;
-        if (!mbar_wait(&p_full[bb], (jj >> 1) & 1, status, 20, s_abort, p.spin)) return false;
-        if (!mbar_wait(&v_full[s], (jj / ST) & 1, status, 21, s_abort, p.spin)) return false;
-        tc_fence_after();
-        const uint32_t sfp = tmem + C::T_SFP + bb * 8, sfv = tmem + C::T_SFV + bb * 8;
-#pragma unroll
-        for (int a = 0; a < BK / 64; ++a) {
-          tmem_cp_32x128b_x4(sfp + 4 * a, smem_u32(sPsf + bb * C::PSF_BYTES + a * 512));
-          tmem_cp_32x128b_x4(sfv + 4 * a, smem_u32(sVsf + s * C::VSF_BYTES + a * 512));
-        }
-#pragma unroll
-        for (int kk = 0; kk < BK / 64; ++kk) {
-          const uint64_t ad = smem_desc(p_base + bb * C::P_BYTES + kk * 32, 8 * 64, kSwizzle64);
-          const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * 64, kSwizzle64);
-          mma_fp4_bs(tmem + bb * C::SRW, ad, bd, instr_desc_fp4(D, 128), sfp + 4 * kk, sfv + 4 * kk, kk > 0);
-        }
-        mma_commit(&r_full[bb]);
-        mma_commit(&kv_empty[s]);
-        return true;
-      };
+      __syncwarp();
       for (int j = 0; ok && j < T; ++j) {
-        const int bs = j & 1, s = j % ST;
-        if (j >= 2 && !mbar_wait(&sr_free[bs], ((j - 2) >> 1) & 1, status, 24, s_abort, p.spin)) ok = false;
-        if (ok && !mbar_wait(&k_full[s], (j / ST) & 1, status, 26, s_abort, p.spin)) ok = false;
-        if (!ok) break;
+        const int b = j % NB, s = j % ST;
+        bool w = true;
+        if (j >= NB) w = mbar_wait(&sr_free[b], ((j - NB) / NB) & 1, status, 24, s_abort, p.spin);
+        w = w && mbar_wait(&k_full[s], (j / ST) & 1, status, 26, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, w)) break;
         tc_fence_after();
-        const uint32_t sfk = tmem + C::T_SFK + bs * 8;
-        for (int a = 0; a < D / 64; ++a) tmem_cp_32x128b_x4(sfk + 4 * a, smem_u32(sKsf + s * C::QSF_BYTES + a * 512));
+        if (elect_one()) {
+          const uint32_t sfk = tmem + C::T_SFK + b * 8;
+          for (int a = 0; a < D / 64; ++a)
+            tmem_cp_32x128b_x4(sfk + 4 * a, smem_u32(sKsf + s * C::QSF_BYTES + a * 512));
 #pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk) {
-          const uint64_t ad = smem_desc(q_base + kk * 32, 8 * C::QK_SW, C::QK_LAYOUT);
-          const uint64_t bd = smem_desc(k_base + s * C::K_BYTES + kk * 32, 8 * C::QK_SW, C::QK_LAYOUT);
-          mma_fp4_bs(tmem + bs * C::SRW, ad, bd, instr_desc_fp4(BK, 128), tmem + C::T_SFQ + 4 * kk, sfk + 4 * kk,
-                     kk > 0);
+          for (int kk = 0; kk < D / 64; ++kk) {
+            const uint64_t ad = smem_desc(q_base + kk * 32, 8 * C::QK_SW, C::QK_LAYOUT);
+            const uint64_t bd = smem_desc(k_base + s * C::K_BYTES + kk * 32, 8 * C::QK_SW, C::QK_LAYOUT);
+            mma_fp4_bs(tmem + b * C::SRW, ad, bd, instr_desc_fp4(BK, 128), tmem + C::T_SFQ + 4 * kk, sfk + 4 * kk,
+                       kk > 0);
+          }
+          mma_commit(&s_full[b]);
         }
-        mma_commit(&s_full[bs]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        __syncwarp();
       }
-      if (ok && T >= 1) issue_pv(T - 1);
-      mma_commit(mma_done);
+      // every MMA of this thread has finished before the CTA may leave
+      if (elect_one()) mma_commit(qk_done);
+      __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(mma_done, 0, status, 25, &no_abort, p.spin);
+      mbar_wait(qk_done, 0, status, 25, &no_abort, p.spin);
+    } else if (warp == kPvWarp) {
+      // ---------------------------------------------------------- PV issuer (whole warp, one lane issues)
+      // PV of tile j writes R into S/R region j % NB once the softmax has read
+      // S of tile j; P and V scale slot j % NB were last read by PV of tile
+      // j - NB, complete since QK of tile j was issued after its R was consumed.
+      const uint32_t v_base = smem_u32(sV), p_base = smem_u32(sP);
+      for (int j = 0; j < T; ++j) {
+        const int b = j % NB, s = j % ST;
+        const bool w = mbar_wait(&p_full[b], (j / NB) & 1, status, 20, s_abort, p.spin) &&
+                       mbar_wait(&v_full[s], (j / ST) & 1, status, 21, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, w)) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t sfp = tmem + C::T_SFP + b * 8, sfv = tmem + C::T_SFV + b * 8;
+#pragma unroll
+          for (int a = 0; a < BK / 64; ++a) {
+            tmem_cp_32x128b_x4(sfp + 4 * a, smem_u32(sPsf + b * C::PSF_BYTES + a * 512));
+            tmem_cp_32x128b_x4(sfv + 4 * a, smem_u32(sVsf + s * C::VSF_BYTES + a * 512));
+          }
+#pragma unroll
+          for (int kk = 0; kk < BK / 64; ++kk) {
+            const uint64_t ad = smem_desc(p_base + b * C::P_BYTES + kk * 32, 8 * 64, kSwizzle64);
+            const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * 64, kSwizzle64);
+            mma_fp4_bs(tmem + b * C::SRW, ad, bd, instr_desc_fp4(D, 128), sfp + 4 * kk, sfv + 4 * kk, kk > 0);
+          }
+          mma_commit(&r_full[b]);
+          mma_commit(&kv_empty[s]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) mma_commit(pv_done);
+      __syncwarp();
+      volatile int no_abort = 0;
+      mbar_wait(pv_done, 0, status, 27, &no_abort, p.spin);
     }
   } else if (warp >= kCorrWarp0) {
-    reg_dealloc<kCorrRegs>();
+    reg_alloc<kCorrRegs>();
     // ------------------------------------------------------------ two-level accumulation + epilogue
     const int r = threadIdx.x & (kWG - 1);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_off + C::T_O;
+    float o[D];  // this thread's row of the FP32 running output
+#pragma unroll
+    for (int c = 0; c < D; ++c) o[c] = 0.0f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const int bb = j & 1;
-      const bool waited = mbar_wait(&p_full[bb], (j >> 1) & 1, status, 40, s_abort, p.spin) &&
-                          mbar_wait(&r_full[bb], (j >> 1) & 1, status, 41, s_abort, p.spin);
-      // the TMEM accesses below are warp-collective: the warp decides together
+      const int b = j % NB;
+      const bool waited = mbar_wait(&p_full[b], (j / NB) & 1, status, 40, s_abort, p.spin) &&
+                          mbar_wait(&r_full[b], (j / NB) & 1, status, 41, s_abort, p.spin);
+      // the TMEM loads below are warp-collective: the warp decides together
       if (!__all_sync(0xffffffffu, waited)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float a = s_alpha[bb * 128 + r], sp1 = s_sp1[bb * 128 + r];
+      const float a = s_alpha[b * 128 + r], sp1 = s_sp1[b * 128 + r];
       const float2 a2 = make_float2(a, a), sp2 = make_float2(sp1, sp1);
-      const uint32_t tR = tmem + lane_off + bb * C::SRW;
+      const uint32_t tR = tmem + lane_off + b * C::SRW;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t rv[32], ov[32];
+        uint32_t rv[32];
         tmem_ld32(tR + ch * 32, rv);
-        if (j > 0) tmem_ld32(tO + ch * 32, ov);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 rr = make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]));
-          float2 o2 = make_float2(0.0f, 0.0f);
-          if (j > 0) o2 = __fmul2_rn(make_float2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2);
-          o2 = __ffma2_rn(rr, sp2, o2);
-          ov[e] = __float_as_uint(o2.x);
-          ov[e + 1] = __float_as_uint(o2.y);
+          const float2 o2 = __ffma2_rn(rr, sp2, __fmul2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2));
+          o[ch * 32 + e] = o2.x;
+          o[ch * 32 + e + 1] = o2.y;
         }
-        tmem_st32(tO + ch * 32, ov);
       }
-      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sr_free[bb]);
+      mbar_arrive(&sr_free[b]);
     }
-    // epilogue: O / l + V_m in bf16; every lane takes part in the TMEM loads,
-    // only the stores are predicated
+    // epilogue: O / l + V_m in bf16
     if (ok && T >= 1) {
       const int row = row0 + r;
-      const bool live = row < p.N;
-      const float inv_l = live ? 1.0f / (s_l[r] + s_l[128 + r]) : 0.0f;
-      __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + (live ? row : 0)) * D;
+      if (row < p.N) {
+        const float inv_l = 1.0f / (s_l[r] + s_l[128 + r]);
+        __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + row) * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t ov[32];
-        __syncwarp();
-        tmem_ld32(tO + ch * 32, ov);
-        tmem_wait_ld();
-        if (live) {
+        for (int c = 0; c < D; c += 8) {
+          uint32_t w[4];
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = ch * 32 + c + 2 * e;
-              const __nv_bfloat162 v2 =
-                  __floats2bfloat162_rn(fmaf(__uint_as_float(ov[c + 2 * e]), inv_l, s_vm[cc]),
-                                        fmaf(__uint_as_float(ov[c + 2 * e + 1]), inv_l, s_vm[cc + 1]));
-              w[e] = *reinterpret_cast<const uint32_t *>(&v2);
-            }
-            *reinterpret_cast<uint4 *>(dst + ch * 32 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(fmaf(o[c + 2 * e], inv_l, s_vm[c + 2 * e]),
+                                                            fmaf(o[c + 2 * e + 1], inv_l, s_vm[c + 2 * e + 1]));
+            w[e] = *reinterpret_cast<const uint32_t *>(&v2);
           }
+          *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -341,21 +352,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + two-level P quantization
     const int r = threadIdx.x & (kWG - 1);
     const int hf = warp >> 2;  // which half of the key tile
-    const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + hf * HALF;
+    const uint32_t tS0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
     float m = -INFINITY, l = 0.0f;
-    for (int j = 0; j < T; ++j) {
-      const int bb = j & 1;
-      float *dsc = s_dsc + bb * BK;
-      bool fail = false;
+    bool stop = false;  // a wait failed late in the previous tile
+    for (int j = 0, bb = 0, pj = 0; j < T; ++j, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
+      // this warpgroup's copy of dS for all BK keys of the tile
+      float *dsc = s_dsc + ((j & 1) * 2 + hf) * BK;
+      // the TMEM loads are warp-collective: the warp decides together
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin));
       if (smooth_q) {
-        // dS_j[c] = sum_d q_bar[d] deq(K^_j)[c, d]: thread r < 64 of half hf
-        // takes key 64 hf + r from the K tile in shared memory
+        // dS_j[c] = sum_d q_bar[d] deq(K^_j)[c, d]: thread r takes key r from
+        // the K tile in shared memory (each warpgroup keeps its own copy)
         const int s = j % ST;
-        fail = !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
-        if (!fail && r < HALF) {
-          const int key = hf * HALF + r;
+        const bool fail = !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
+        if (!fail) {
+          const int key = r;
           const uint8_t *kt = sK + s * C::K_BYTES;
           const uint8_t *ksf = sKsf + s * C::QSF_BYTES;
           float acc = 0.0f;
@@ -385,76 +398,102 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           dsc[key] = acc * c2;
         }
-        // every thread of the warpgroup reaches this barrier; a failure is
-        // carried to the row-max barrier below, where both halves leave together
-        named_bar_sync(kBarDs0 + hf, kWG);
+        // the warpgroup leaves together: a warp that stops alone would strand
+        // the others at this barrier in the next tile
+        if (named_bar_any(kBarDs0 + hf, kWG, stop || fail || !okw || *s_abort)) break;
+      } else if (stop || !okw) {
+        break;
       }
-      // the TMEM loads are warp-collective: the warp decides together
-      const bool ok =
-          __all_sync(0xffffffffu, !fail && mbar_wait(&s_full[bb], (j >> 1) & 1, status, 32, s_abort, p.spin));
-      float t[HALF];
+      tc_fence_after();
+      // x: this half's raw scores S (t = x c2), or t itself when dS is added
+      // (then c2 is already applied); maxima are taken in x, which orders
+      // like t.  Each half publishes its maximum at once and takes its
+      // exponentials against it, e = exp2(t - m_half); the tile maximum
+      // m_tile then enters as one factor, P2 = 2688 exp2(t - m_tile) =
+      // e * 2688 exp2(m_half - m_tile), so neither half waits on the other
+      // before its exponentials.
+      const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // tile keys >= lim are invisible
+      const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N);
+      const int oh = hf ^ 1;
+      float x[HALF];
       float bm[HALF / 16];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < HALF / 16; ++g) bm[g] = -INFINITY;
-      if (ok) {
-        tc_fence_after();
+      {
         uint32_t v[HALF];
 #pragma unroll
         for (int ch = 0; ch < HALF / 32; ++ch)
-          tmem_ld32(tS + bb * C::SRW + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
+          tmem_ld32(tS0 + bb * C::SRW + hf * HALF + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
         tmem_wait_ld();
-        const int k0 = j * BK + hf * HALF;
-        const bool need_mask = (k0 + HALF > p.M) || (p.causal && k0 + HALF - 1 > row0 + p.M - p.N);
 #pragma unroll
-        for (int e = 0; e < HALF; ++e) {
-          float x = smooth_q ? fmaf(__uint_as_float(v[e]), c2, dsc[hf * HALF + e]) : __uint_as_float(v[e]) * c2;
-          if (need_mask) {
-            const int key = k0 + e;
-            if (key >= p.M || (p.causal && key > diag)) x = -INFINITY;
-          }
-          t[e] = x;
-        }
-#pragma unroll
-        for (int g = 0; g < HALF / 16; ++g) {
-          float a = fmax3(t[16 * g], t[16 * g + 1], t[16 * g + 2]);
-#pragma unroll
-          for (int u = 3; u < 15; u += 2) a = fmax3(a, t[16 * g + u], t[16 * g + u + 1]);
-          bm[g] = fmaxf(a, t[16 * g + 15]);
-        }
-        mx = fmax3(fmaxf(bm[0], bm[1]), bm[2], bm[3]);
+        for (int e = 0; e < HALF; ++e) x[e] = __uint_as_float(v[e]);
       }
-      s_mx[(bb * 2 + hf) * 128 + r] = mx;
-      if (named_bar_any(kBarMax, 2 * kWG, !ok || *s_abort)) break;
-      mx = fmaxf(mx, s_mx[(bb * 2 + (hf ^ 1)) * 128 + r]);
-
-      const float m_new = fmaxf(m, mx);
+      if (smooth_q) {
+#pragma unroll
+        for (int e = 0; e < HALF; ++e) x[e] = fmaf(x[e], c2, dsc[hf * HALF + e]);
+      }
+      if (edge) {
+#pragma unroll
+        for (int e = 0; e < HALF; ++e) x[e] = (hf * HALF + e < lim) ? x[e] : -INFINITY;
+      }
+#pragma unroll
+      for (int g = 0; g < HALF / 16; ++g) {
+        float a = fmax3(x[16 * g], x[16 * g + 1], x[16 * g + 2]);
+#pragma unroll
+        for (int u = 3; u < 15; u += 2) a = fmax3(a, x[16 * g + u], x[16 * g + u + 1]);
+        bm[g] = fmaxf(a, x[16 * g + 15]);
+      }
+      const float mh = fmax3(fmaxf(bm[0], bm[1]), bm[2], bm[3]);
+      s_mx[((j & 1) * 2 + hf) * 128 + r] = mh;
+      mbar_arrive(&mx_full[(j & 1) * 2 + hf]);
+      const float xs = smooth_q ? 1.0f : c2;  // x -> t
+      const float mht = (mh == -INFINITY) ? 0.0f : mh * xs;
+      const float2 xs2 = make_float2(xs, xs), nm2 = make_float2(-mht, -mht);
+      float2 se2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int u = 0; u < HALF; u += 2) {
+        const float2 arg = __ffma2_rn(make_float2(x[u], x[u + 1]), xs2, nm2);
+        x[u] = ex2_approx(arg.x);
+        x[u + 1] = ex2_approx(arg.y);
+        se2 = __fadd2_rn(se2, make_float2(x[u], x[u + 1]));
+      }
+      // the other half's maximum
+      if (!__all_sync(0xffffffffu, mbar_wait(&mx_full[(j & 1) * 2 + oh], (j >> 1) & 1, status, 33, s_abort, p.spin))) {
+        stop = true;
+        if (!smooth_q) break;
+        continue;  // leave with the warpgroup at the next dS barrier
+      }
+      const float mt = fmaxf(mh, s_mx[((j & 1) * 2 + oh) * 128 + r]) * xs;  // row max of t over the tile
+      const float m_new = fmaxf(m, mt);
       const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
-      const bool any = mx != -INFINITY;
-      const float sp1 = any ? ex2_approx(mx - m_new) * (1.0f / 2688.0f) : 0.0f;
-      const float shift = any ? kLog2_2688 - mx : 0.0f;
+      const bool any = mt != -INFINITY;
+      const float sp1 = any ? ex2_approx(mt - m_new) * (1.0f / 2688.0f) : 0.0f;
+      const float f = (any && mh != -INFINITY) ? ex2_approx(mht - mt) * 2688.0f : 0.0f;  // P2 = e f
       uint8_t *prow = sP + bb * C::P_BYTES;
       uint32_t scw = 0;
       uint32_t pk[8];
-      float rs = 0.0f;
+      float mult[HALF / 16];
 #pragma unroll
       for (int g = 0; g < HALF / 16; ++g) {
-        // s_P2 = E4M3(max P2 / 6) with max P2 = exp2(block max t + shift)
-        const float amax = ex2_approx(bm[g] + shift);
+        // s_P2 = E4M3(max P2 / 6); the block's largest e is exp2 of its largest t
+        const float amax = ex2_approx(fmaf(bm[g], xs, -mht)) * f;
         const uint32_t sc = cvt_e4m3x2(amax * (1.0f / 6.0f), 0.0f) & 0xFF;
         const float s2 = e4m3_to_float(sc);
-        const float sb = s2 > 0.0f ? shift - lg2_approx(s2) : -INFINITY;
-        float qv[16], bs = 0.0f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          qv[u] = ex2_approx(t[16 * g + u] + sb);
-          bs += qv[u];
-        }
-        rs = fmaf(s2, bs, rs);
+        mult[g] = s2 > 0.0f ? __fdividef(f, s2) : 0.0f;  // P2 / s_P2 = e f / s_P2
         scw |= sc << (8 * g);
+      }
+#pragma unroll
+      for (int g = 0; g < HALF / 16; ++g) {
+        const float2 mu2 = make_float2(mult[g], mult[g]);
+        float qv[16];
+#pragma unroll
+        for (int u = 0; u < 16; u += 2) {
+          const float2 q2 = __fmul2_rn(make_float2(x[16 * g + u], x[16 * g + u + 1]), mu2);
+          qv[u] = q2.x;
+          qv[u + 1] = q2.y;
+        }
         pk[2 * g] = cvt_e2m1x8(qv[0], qv[1], qv[2], qv[3], qv[4], qv[5], qv[6], qv[7]);
         pk[2 * g + 1] = cvt_e2m1x8(qv[8], qv[9], qv[10], qv[11], qv[12], qv[13], qv[14], qv[15]);
       }
+      const float rs = f * (se2.x + se2.y);  // this half's sum of P2
       // keys 64 hf .. 64 hf + 63 are bytes 32 hf .. 32 hf + 31 of row r
       *reinterpret_cast<uint4 *>(prow + swz_off<64>(r, 2 * hf)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       *reinterpret_cast<uint4 *>(prow + swz_off<64>(r, 2 * hf + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -475,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == kQkWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int D>

@@ -133,6 +133,15 @@ __device__ __forceinline__ void reg_dealloc() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// One lane of the (fully converged) warp is elected; it returns true there.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ----------------------------------------------------------------- TMEM
 // Allocation is a warp-wide operation; the base address lands in *dst (smem).
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
