@@ -11,31 +11,32 @@
 //   R_ij  = P^_ij V^_j        (tile partial, accumulated over this tile only)
 //   O_ij  = e^(m_i,j-1 - m_ij) O_i,j-1 + R_ij        (FP32 running output)
 //   O_i   = O / l * delta_V / 448 (+ V_m)
-// Scores are handled in the base-2 domain (sm_scale * log2 e folded into the
-// dequantization multiply) and the 448 of P^ is folded into the exponent, so
-// l carries 448 * sum P~ and the final scale is delta_V / l.
+// Scores are handled in the base-2 domain, t = S sm_scale log2 e, and the 448
+// of P^ is folded into the exponent, so l carries 448 * sum P~ and the final
+// scale is delta_V / l.
 //
-// GB300 mapping (the pages' Ada/Hopper register-level design is prior art).
-// Each CTA owns two query blocks (tiles t = 0, 1) of one head; every K^/V^
-// tile is loaded once for both.  Four warpgroups:
-//   WG0, WG1   softmax of tile 0 / tile 1, one query row per thread (its TMEM
-//              lane): the whole score row in one TMEM read, dequant + dS, mask,
-//              online max / sum, P^ to shared memory (the swizzled K-major A
-//              operand of the next MMA), alpha and l to shared memory
-//   WG2        two-level accumulation for both tiles: R from TMEM, O from TMEM,
-//              O = alpha O + R in FP32, O back to TMEM; then the epilogue
-//   WG3        warp 12: TMA producer (Q^ tiles once, K^_j / V^T_j into a ring
-//              of shared-memory stages); warp 13: the tcgen05 MMA issuer (one
-//              thread): S_t = Q^_t K^_j^T (kind::f16 on INT8 codes held as
-//              exact fp16 integers — sm_103a has no INT8 tensor path — or
-//              kind::f8f6f4 on E4M3 codes) and R_t = P^_t V^_j (kind::f8f6f4)
-// TMEM (512 columns): per tile one region that holds S_t(j) and then, once the
-// softmax has read it, the tile partial R_t(j) (a fresh accumulator, zeroed by
-// its first k-step), and the FP32 running output O_t.  While one tile is in its
-// softmax or correction, the tensor core runs the other tile's MMAs.
-// Waits suspend the waiting thread instead of polling and are bounded: on
-// timeout the kernel records SAGE_ERR_TIMEOUT and the site, drains its own TMA
-// loads and MMAs, frees TMEM and returns.
+// GB300 mapping (the pages' Ada/Hopper register-level design is prior art):
+// one query block per CTA and 16 warps.
+//   warps 0-7   two warpgroups on the same 128 query rows (one row per thread,
+//               its TMEM lane); warpgroup h takes keys [h BK/2, (h+1) BK/2) of
+//               every tile: dequantize, dS, mask, exponentials, P^ into the
+//               swizzled K-major A operand of the PV MMA in shared memory.
+//               Each half publishes its own maximum at once and takes its
+//               exponentials against it, e = exp2(t - m_half); the new running
+//               maximum enters afterwards as one factor, P^ = e4m3(e * 448
+//               exp2(m_half - m_new)), so neither half waits on the other
+//               before its exponentials.
+//   warps 8-11  two-level accumulation O = alpha O + R with the thread's row
+//               of O in registers, then the epilogue
+//   warp 12     TMA producer: Q^ once, K^_j and V^T_j into a ring of stages
+//   warp 13     QK issuer: S(j) = Q^ K^_j^T (kind::f16 on INT8 codes held as
+//               exact fp16 integers -- sm_103a has no INT8 tensor path -- or
+//               kind::f8f6f4 on E4M3 codes)
+//   warp 14     PV issuer: R(j) = P^(j) V^_j (kind::f8f6f4)
+// TMEM: three S/R regions (R of tile j overwrites S of tile j once the softmax
+// has read it), so QK runs up to three tiles ahead of the accumulation.
+// Waits are bounded: on timeout the kernel records SAGE_ERR_TIMEOUT and the
+// site, drains its own TMA loads and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -49,19 +50,19 @@ namespace sage {
 namespace {
 
 constexpr int kWG = 128;       // threads per warpgroup
-constexpr int kThreads = 512;  // softmax x2, correction, control
-constexpr int kCorrWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
-// Register split (setmaxnreg) from the 128 per thread the block launches with:
-// the softmax warpgroups rise, the correction and control warpgroups drop.
-constexpr int kLaunchRegs = 128, kSoftmaxRegs = 184, kCorrRegs = 88, kControlRegs = 56;
-static_assert(2 * kWG * kSoftmaxRegs + kWG * kCorrRegs + kWG * kControlRegs <= kThreads * kLaunchRegs,
-              "register split");
-static_assert(kSoftmaxRegs >= kLaunchRegs && kCorrRegs <= kLaunchRegs && kControlRegs <= kLaunchRegs,
+constexpr int kThreads = 512;  // softmax x2, accumulation, control
+constexpr int kCorrWarp0 = 8, kProducerWarp = 12, kQkWarp = 13, kPvWarp = 14;
+// Register split (setmaxnreg) from the 128 per thread the block launches with.
+constexpr int kLaunchRegs = 128, kSoftmaxRegs = 136, kCorrRegs = 184, kControlRegs = 56;
+static_assert(kWG * (2 * kSoftmaxRegs + kCorrRegs + kControlRegs) <= kThreads * kLaunchRegs, "register split");
+static_assert(kSoftmaxRegs >= kLaunchRegs && kCorrRegs >= kLaunchRegs && kControlRegs <= kLaunchRegs,
               "register split directions");
+constexpr int NB = 3;  // S/R regions and P^ buffers
 constexpr float kLog2_448 = 8.807354922057604f;
 
 template <int D, int BK, bool kQK16>
 struct Cfg {
+  static constexpr int HALF = BK / 2;                    // keys per softmax warpgroup
   static constexpr int QK_EB = kQK16 ? 2 : 1;           // bytes per stored Q/K code
   static constexpr int ROWB = D * QK_EB;                 // bytes per Q/K row
   static constexpr int QK_SW = ROWB >= 128 ? 128 : 64;   // swizzle span of Q/K tiles
@@ -73,25 +74,26 @@ struct Cfg {
   static constexpr int P_BYTES = 128 * BK;
   static constexpr int QK_KSTEPS = ROWB / 32;            // one MMA consumes 32 bytes of K
   static constexpr int PV_KSTEPS = BK / 32;
-  static constexpr int FIXED = 2 * Q_BYTES + 2 * P_BYTES;
-  static constexpr int ST_FIT = (216 * 1024 - FIXED) / (K_BYTES + V_BYTES);
-  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static_assert(STAGES >= 2, "shared memory budget");
-  static constexpr int SRW = BK > D ? BK : D;            // columns of the S / R region of a tile
-  static constexpr int TMEM_O = 2 * SRW;                 // O_t at TMEM_O + t * D
-  static constexpr int TMEM_NEED = 2 * SRW + 2 * D;
-  static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  static_assert(TMEM_NEED <= 512, "tensor memory budget");
-  static constexpr int SMEM_TILES = FIXED + STAGES * (K_BYTES + V_BYTES);
-  static constexpr int SMEM_MISC = (4 * BK + 4 * D + 4 * 128) * 4 + (1 + 3 * STAGES + 8 + 1) * 8 + 16;
-  static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC;
+  static constexpr int NFLOAT = NB * 128 /*alpha*/ + 2 * 128 /*l*/ + 4 * 128 /*max*/ + 3 * D + 4 * BK /*dS*/;
+  static constexpr int FIXED = Q_BYTES + NB * P_BYTES;
+  static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
+  // K and V have rings of their own: a K tile is free once its QK has run
+  // (and, with dS, once the softmax has read it); a V tile once its PV has
+  static constexpr int BUDGET = 225 * 1024 - 1024 - FIXED - MISC;
+  static constexpr int VST = 2 * (K_BYTES + V_BYTES) <= BUDGET - K_BYTES ? 3 : 2;
+  static constexpr int KST_FIT = (BUDGET - VST * V_BYTES) / K_BYTES;
+  static constexpr int KST = KST_FIT > 4 ? 4 : KST_FIT;
+  static_assert(KST >= 2 && VST >= 2, "shared memory budget");
+  static constexpr int SRW = BK > D ? BK : D;            // columns of one S / R region
+  static constexpr int TMEM_COLS = NB * SRW <= 256 ? 256 : 512;
+  static constexpr int SMEM_TOTAL = 1024 + FIXED + KST * K_BYTES + VST * V_BYTES + MISC;
   static constexpr uint32_t IDESC_QK =
       instr_desc(kFmtF32, kQK16 ? kFmtF16 : kFmtE4M3, kQK16 ? kFmtF16 : kFmtE4M3, BK, 128);
   static constexpr uint32_t IDESC_PV = instr_desc(kFmtF32, kFmtE4M3, kFmtE4M3, D, 128);
 };
 
 struct AttnParams {
-  int N, M, N_pad, M_pad, Tm, Tm2, Tn, Hq, Hkv, causal, flags;
+  int N, M, N_pad, M_pad, Tm, Tn, Hq, Hkv, causal, flags;
   float sm_log2;  // sm_scale * log2(e)
   const float *dq, *qbar, *dk, *dv, *vm;
   __nv_bfloat16 *o;
@@ -107,90 +109,82 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c) {
   return (uint32_t)((r >> 3) * (8 * SW) + (r & 7) * SW + ((c ^ x) << 4));
 }
 
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-
 template <int D, int BK, bool kQK16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using C = Cfg<D, BK, kQK16>;
-  constexpr int ST = C::STAGES;
+  constexpr int KST = C::KST, VST = C::VST;
+  constexpr int HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *sQ = base;                        // 2 query tiles
-  uint8_t *sP = sQ + 2 * C::Q_BYTES;         // P^ of each query tile
-  uint8_t *sK = sP + 2 * C::P_BYTES;         // ST stages
-  uint8_t *sV = sK + ST * C::K_BYTES;        // ST stages
-  float *s_dsc = (float *)(sV + ST * C::V_BYTES);  // [2 tiles][2 buffers][BK]
-  float *s_qbar = s_dsc + 4 * BK;                  // [2][D]
-  float *s_dv = s_qbar + 2 * D;                    // [D]
-  float *s_vm = s_dv + D;                          // [D]
-  float *s_alpha = s_vm + D;                       // [2][128] rescale factor of the current tile
-  float *s_l = s_alpha + 2 * 128;                  // [2][128] final row sums
-  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_l + 2 * 128) + 7) & ~(uintptr_t)7);
+  uint8_t *sQ = base;
+  uint8_t *sP = sQ + C::Q_BYTES;        // [NB]
+  uint8_t *sK = sP + NB * C::P_BYTES;   // [KST]
+  uint8_t *sV = sK + KST * C::K_BYTES;  // [VST]
+  float *s_alpha = (float *)(sV + VST * C::V_BYTES);  // [NB][128]
+  float *s_l = s_alpha + NB * 128;                   // [2 halves][128]
+  float *s_mx = s_l + 2 * 128;                       // [2 parities][2 halves][128]
+  float *s_qbar = s_mx + 4 * 128;                    // [D]
+  float *s_dv = s_qbar + D;                          // [D]
+  float *s_vm = s_dv + D;                            // [D]
+  float *s_dsc = s_vm + D;                           // [2 buffers][2 halves][BK]
+  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 4 * BK) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
-  uint64_t *k_full = q_full + 1;
-  uint64_t *v_full = k_full + ST;
-  uint64_t *kv_empty = v_full + ST;
-  uint64_t *s_full = kv_empty + ST;  // [2] S_t ready in TMEM
-  uint64_t *p_full = s_full + 2;     // [2] P^_t, alpha_t written; S_t read
-  uint64_t *r_full = p_full + 2;     // [2] R_t ready in TMEM
-  uint64_t *sr_free = r_full + 2;    // [2] R_t folded into O_t; region free
-  uint64_t *mma_done = sr_free + 2;
-  uint32_t *s_tmem = (uint32_t *)(mma_done + 1);
+  uint64_t *k_full = q_full + 1;     // [KST]
+  uint64_t *k_empty = k_full + KST;  // [KST]
+  uint64_t *v_full = k_empty + KST;  // [VST]
+  uint64_t *v_empty = v_full + VST;  // [VST]
+  uint64_t *s_full = v_empty + VST;  // [NB] S(j) in TMEM
+  uint64_t *p_full = s_full + NB;    // [NB] P^(j), alpha(j) written; S(j) read
+  uint64_t *r_full = p_full + NB;    // [NB] R(j) in TMEM
+  uint64_t *sr_free = r_full + NB;   // [NB] R(j) folded into O; region free
+  uint64_t *mx_full = sr_free + NB;  // [2 parities][2 halves] half maxima
+  uint64_t *qk_done = mx_full + 4;
+  uint64_t *pv_done = qk_done + 1;
+  uint32_t *s_tmem = (uint32_t *)(pv_done + 1);
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.Tm2;
-  const int pair = p.Tm2 - 1 - blockIdx.x % p.Tm2;  // heaviest causal blocks first
+  const int bh = blockIdx.x / p.Tm;
+  const int qi = p.Tm - 1 - blockIdx.x % p.Tm;  // longest causal rows first
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int hkv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  // key tiles each query tile needs (0 when the tile is past the last block)
-  int Tt[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qi = 2 * pair + t;
-    if (qi >= p.Tm) {
-      Tt[t] = 0;
-    } else {
-      const int last_row = min(p.N, qi * 128 + 128) - 1;
-      Tt[t] = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
-    }
-  }
-  const int T = max(Tt[0], Tt[1]);
+  const int row0 = qi * 128;
+  const int last_row = min(p.N, row0 + 128) - 1;
+  const int T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
   const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kWG);
-      mbar_init(&r_full[t], 1);
-      mbar_init(&sr_free[t], kWG);
+    for (int x = 0; x < NB; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 2 * kWG);
+      mbar_init(&r_full[x], 1);
+      mbar_init(&sr_free[x], kWG);
     }
-    mbar_init(mma_done, 1);
+    for (int x = 0; x < 4; ++x) mbar_init(&mx_full[x], kWG);
+    mbar_init(qk_done, 1);
+    mbar_init(pv_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (threadIdx.x < 2 * kWG) {
-    const int t = threadIdx.x / kWG, c0 = threadIdx.x % kWG;
-    const int qi = min(2 * pair + t, p.Tm - 1);
-    for (int c = c0; c < D; c += kWG) {
-      s_qbar[t * D + c] = smooth_q ? p.qbar[((size_t)bh * p.Tm + qi) * D + c] : 0.0f;
-      if (t == 0) {
-        s_dv[c] = p.dv[(size_t)hkv * D + c];
-        s_vm[c] = p.vm[(size_t)hkv * D + c];
-      }
-    }
+  for (int c = threadIdx.x; c < D; c += kThreads) {
+    s_qbar[c] = smooth_q ? p.qbar[((size_t)bh * p.Tm + qi) * D + c] : 0.0f;
+    s_dv[c] = p.dv[(size_t)hkv * D + c];
+    s_vm[c] = p.vm[(size_t)hkv * D + c];
   }
   tc_fence_before();
   __syncthreads();
@@ -205,189 +199,194 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int nq = Tt[1] > 0 ? 2 : 1;
-      mbar_expect_tx(q_full, nq * C::Q_BYTES);
-      for (int t = 0; t < nq; ++t)
+      mbar_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::QK_CHUNKS; ++c)
-          tma_load_2d(sQ + t * C::Q_BYTES + c * 128 * C::QK_SW, &tm_q, q_full, c * C::QK_SW,
-                      bh * p.N_pad + (2 * pair + t) * 128);
-      int issued = 0;
-      for (int j = 0; j < T; ++j) {
-        const int s = j % ST, n = j / ST;
-        if (j >= ST && !mbar_wait(&kv_empty[s], (n - 1) & 1, status, 10, s_abort, p.spin)) break;
-        mbar_expect_tx(&k_full[s], C::K_BYTES);
+      for (int c = 0; c < C::QK_CHUNKS; ++c)
+        tma_load_2d(sQ + c * 128 * C::QK_SW, &tm_q, q_full, c * C::QK_SW, bh * p.N_pad + row0);
+      // K runs ahead of V: the QK issuer can start tile j+1 while tile j waits for its PV
+      int kj = 0, vj = 0;
+      bool fail = false;
+      while (!fail && (kj < T || vj < T)) {
+        if (kj < T && (kj < vj + KST)) {
+          const int s = kj % KST, n = kj / KST;
+          if (kj >= KST && !mbar_wait(&k_empty[s], (n - 1) & 1, status, 10, s_abort, p.spin)) {
+            fail = true;
+            break;
+          }
+          mbar_expect_tx(&k_full[s], C::K_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::QK_CHUNKS; ++c)
-          tma_load_2d(sK + s * C::K_BYTES + c * BK * C::QK_SW, &tm_k, &k_full[s], c * C::QK_SW,
-                      hkv * p.M_pad + j * BK);
-        mbar_expect_tx(&v_full[s], C::V_BYTES);
-        tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], j * BK, hkv * D);
-        issued = j + 1;
+          for (int c = 0; c < C::QK_CHUNKS; ++c)
+            tma_load_2d(sK + s * C::K_BYTES + c * BK * C::QK_SW, &tm_k, &k_full[s], c * C::QK_SW,
+                        hkv * p.M_pad + kj * BK);
+          ++kj;
+        }
+        if (vj < T && (vj < kj || kj == T)) {
+          const int s = vj % VST, n = vj / VST;
+          // a V stage frees later than a K stage: only wait when K cannot go on
+          if (vj >= VST && kj < T && kj < vj + KST && !mbar_try_wait(&v_empty[s], (n - 1) & 1)) continue;
+          if (vj >= VST && !mbar_wait(&v_empty[s], (n - 1) & 1, status, 12, s_abort, p.spin)) {
+            fail = true;
+            break;
+          }
+          mbar_expect_tx(&v_full[s], C::V_BYTES);
+          tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], vj * BK, hkv * D);
+          ++vj;
+        }
       }
-      // drain: every load this warp issued must land before the CTA exits
+      // drain: every load this warp issued lands before the CTA exits
       volatile int no_abort = 0;
       mbar_wait(q_full, 0, status, 11, &no_abort, p.spin);
-      for (int j = max(0, issued - ST); j < issued; ++j) {
-        const int s = j % ST, n = j / ST;
-        mbar_wait(&k_full[s], n & 1, status, 11, &no_abort, p.spin);
-        mbar_wait(&v_full[s], n & 1, status, 11, &no_abort, p.spin);
-      }
-    } else if (warp == kMmaWarp && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
-      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV), p_base = smem_u32(sP);
-      bool ok = mbar_wait(q_full, 0, status, 23, s_abort, p.spin);
-      tc_fence_after();
+      for (int j = max(0, kj - KST); j < kj; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, status, 11, &no_abort, p.spin);
+      for (int j = max(0, vj - VST); j < vj; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, status, 11, &no_abort, p.spin);
+    } else if (warp == kQkWarp) {
+      // ---------------------------------------------------------- QK issuer (whole warp, one lane issues)
+      // S(j) goes to S/R region j % NB once the accumulation has consumed R of
+      // tile j - NB there.
+      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, status, 23, s_abort, p.spin));
       for (int j = 0; ok && j < T; ++j) {
-        const int s = j % ST;
-        // S_t(j) = Q^_t K^_j^T into the tile's S/R region, once R_t(j-1) is folded into O_t
-        for (int t = 0; ok && t < 2; ++t) {
-          if (j >= Tt[t]) continue;
-          if (j >= 1 && !mbar_wait(&sr_free[t], (j - 1) & 1, status, 20, s_abort, p.spin)) ok = false;
-          if (ok && !mbar_wait(&k_full[s], (j / ST) & 1, status, 21, s_abort, p.spin)) ok = false;
-          if (!ok) break;
-          tc_fence_after();
+        const int b = j % NB, s = j % KST;
+        bool w = true;
+        if (j >= NB) w = mbar_wait(&sr_free[b], ((j - NB) / NB) & 1, status, 20, s_abort, p.spin);
+        w = w && mbar_wait(&k_full[s], (j / KST) & 1, status, 21, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, w)) break;
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
             const int byte = kk * 32;
-            const uint32_t aq = q_base + t * C::Q_BYTES + (byte / C::QK_SW) * 128 * C::QK_SW + (byte % C::QK_SW);
+            const uint32_t aq = q_base + (byte / C::QK_SW) * 128 * C::QK_SW + (byte % C::QK_SW);
             const uint32_t bk = k_base + s * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
             const uint64_t ad = smem_desc(aq, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
             const uint64_t bd = smem_desc(bk, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
             if (kQK16)
-              mma_f16(tmem + t * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+              mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
             else
-              mma_f8(tmem + t * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+              mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
           }
-          mma_commit(&s_full[t]);
+          mma_commit(&s_full[b]);
+          if (!smooth_q) mma_commit(&k_empty[s]);  // with dS the softmax still reads K^_j
         }
-        // R_t(j) = P^_t V^_j, a fresh accumulator over this key tile only
-        for (int t = 0; ok && t < 2; ++t) {
-          if (j >= Tt[t]) continue;
-          if (!mbar_wait(&p_full[t], j & 1, status, 22, s_abort, p.spin)) ok = false;
-          if (ok && !mbar_wait(&v_full[s], (j / ST) & 1, status, 24, s_abort, p.spin)) ok = false;
-          if (!ok) break;
-          tc_fence_after();
+        __syncwarp();
+      }
+      // every MMA of this thread has finished before the CTA may leave
+      if (elect_one()) mma_commit(qk_done);
+      __syncwarp();
+      volatile int no_abort = 0;
+      mbar_wait(qk_done, 0, status, 25, &no_abort, p.spin);
+    } else if (warp == kPvWarp) {
+      // ---------------------------------------------------------- PV issuer (whole warp, one lane issues)
+      // R(j) = P^(j) V^_j, a fresh accumulator over this key tile only, into
+      // S/R region j % NB once the softmax has read S(j) there
+      const uint32_t v_base = smem_u32(sV), p_base = smem_u32(sP);
+      for (int j = 0; j < T; ++j) {
+        const int b = j % NB, s = j % VST;
+        const bool w = mbar_wait(&p_full[b], (j / NB) & 1, status, 22, s_abort, p.spin) &&
+                       mbar_wait(&v_full[s], (j / VST) & 1, status, 24, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, w)) break;
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
-            const uint64_t ad = smem_desc(p_base + t * C::P_BYTES + kk * 32, 8 * C::PV_SW,
+            const uint64_t ad = smem_desc(p_base + b * C::P_BYTES + kk * 32, 8 * C::PV_SW,
                                           C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
             const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * C::PV_SW,
                                           C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
-            mma_f8(tmem + t * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
+            mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
           }
-          mma_commit(&r_full[t]);
+          mma_commit(&r_full[b]);
+          mma_commit(&v_empty[s]);
+          if (smooth_q) mma_commit(&k_empty[j % KST]);  // the softmax has read K^_j (p_full)
         }
-        if (ok) mma_commit(&kv_empty[s]);
+        __syncwarp();
       }
-      // drain: all MMAs this thread issued complete before TMEM is freed
-      mma_commit(mma_done);
+      if (elect_one()) mma_commit(pv_done);
+      __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(mma_done, 0, status, 25, &no_abort, p.spin);
+      mbar_wait(pv_done, 0, status, 27, &no_abort, p.spin);
     }
   } else if (warp >= kCorrWarp0) {
-    reg_dealloc<kCorrRegs>();
+    reg_alloc<kCorrRegs>();
     // ------------------------------------------------------------ two-level accumulation + epilogue
     const int r = threadIdx.x & (kWG - 1);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float o[D];  // this thread's row of the FP32 running output
+#pragma unroll
+    for (int c = 0; c < D; ++c) o[c] = 0.0f;
     bool ok = true;
-    for (int j = 0; ok && j < T; ++j) {
-      for (int t = 0; ok && t < 2; ++t) {
-        if (j >= Tt[t]) continue;
-        // alpha_t(j) is in shared memory once p_full says so; R_t(j) once r_full does.
-        // The TMEM loads and stores below are warp-collective, so the warp decides
-        // together whether to go on.
-        const bool waited = mbar_wait(&p_full[t], j & 1, status, 40, s_abort, p.spin) &&
-                            mbar_wait(&r_full[t], j & 1, status, 41, s_abort, p.spin);
-        if (!__all_sync(0xffffffffu, waited)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float a = s_alpha[t * 128 + r];
-        const uint32_t tR = tmem + lane_off + t * C::SRW;
-        const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t rv[32], ov[32];
-          tmem_ld32(tR + ch * 32, rv);
-          if (j > 0) tmem_ld32(tO + ch * 32, ov);
-          tmem_wait_ld();
-          if (j > 0) {
-            const float2 aa = f2(a, a);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 o2 = __ffma2_rn(f2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), aa,
-                                           f2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1])));
-              ov[e] = __float_as_uint(o2.x);
-              ov[e + 1] = __float_as_uint(o2.y);
-            }
-            tmem_st32(tO + ch * 32, ov);
-          } else {
-            tmem_st32(tO + ch * 32, rv);  // O_t(0) = R_t(0)
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&sr_free[t]);
+    for (int j = 0; j < T; ++j) {
+      const int b = j % NB;
+      // alpha(j) is in shared memory once p_full says so, R(j) in TMEM once
+      // r_full does; the TMEM loads are warp-collective, so the warp decides together
+      const bool waited = mbar_wait(&p_full[b], (j / NB) & 1, status, 40, s_abort, p.spin) &&
+                          mbar_wait(&r_full[b], (j / NB) & 1, status, 41, s_abort, p.spin);
+      if (!__all_sync(0xffffffffu, waited)) {
+        ok = false;
+        break;
       }
-    }
-    // epilogue: O / l * delta_V (+ V_m) in bf16, one row per thread.  Every lane
-    // takes part in the (warp-collective) TMEM loads; only rows < N are stored.
-    for (int t = 0; ok && t < 2; ++t) {
-      if (Tt[t] == 0) continue;
-      const int row = (2 * pair + t) * 128 + r;
-      const bool live = row < p.N;
-      const float inv_l = live ? 1.0f / s_l[t * 128 + r] : 0.0f;
-      const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
-      __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + (live ? row : 0)) * D;
+      tc_fence_after();
+      const float a = s_alpha[b * 128 + r];
+      const float2 a2 = make_float2(a, a);
+      const uint32_t tR = tmem + lane_off + b * C::SRW;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t ov[32];
-        tmem_ld32(tO + ch * 32, ov);
+        uint32_t rv[32];
+        tmem_ld32(tR + ch * 32, rv);
         tmem_wait_ld();
-        if (!live) continue;
 #pragma unroll
-        for (int c = 0; c < 32; c += 8) {
+        for (int e = 0; e < 32; e += 2) {
+          const float2 o2 = __ffma2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2,
+                                       make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1])));
+          o[ch * 32 + e] = o2.x;
+          o[ch * 32 + e + 1] = o2.y;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sr_free[b]);
+    }
+    // epilogue: O / l * delta_V (+ V_m) in bf16
+    if (ok && T >= 1) {
+      const int row = row0 + r;
+      if (row < p.N) {
+        const float inv_l = 1.0f / (s_l[r] + s_l[128 + r]);
+        __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + row) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 8) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cc = ch * 32 + c + 2 * e;
-            const float o0 = fmaf(__uint_as_float(ov[c + 2 * e]), s_dv[cc] * inv_l, s_vm[cc]);
-            const float o1 = fmaf(__uint_as_float(ov[c + 2 * e + 1]), s_dv[cc + 1] * inv_l, s_vm[cc + 1]);
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(o0, o1);
+            const int cc = c + 2 * e;
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(fmaf(o[cc], s_dv[cc] * inv_l, s_vm[cc]),
+                                                            fmaf(o[cc + 1], s_dv[cc + 1] * inv_l, s_vm[cc + 1]));
             w[e] = *reinterpret_cast<const uint32_t *>(&v2);
           }
-          *reinterpret_cast<uint4 *>(dst + ch * 32 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
   } else {
     reg_alloc<kSoftmaxRegs>();
-    // ------------------------------------------------------------ softmax of tile t
-    const int t = warp >> 2;                 // query tile of this warpgroup
-    const int r = threadIdx.x & (kWG - 1);   // query row within the tile == TMEM lane
-    const int T_t = Tt[t];
-    const uint32_t sS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + t * C::SRW;
-    const int qi = 2 * pair + t;
-    const int row0 = qi * 128;
+    // ------------------------------------------------------------ softmax of one half of each key tile
+    const int r = threadIdx.x & (kWG - 1);  // query row within the block == TMEM lane
+    const int hf = warp >> 2;               // which half of the key tile
+    const int oh = hf ^ 1;
+    const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + hf * HALF;
     const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
-    const float dq = (T_t > 0) ? p.dq[(size_t)bh * p.Tm + qi] : 0.0f;
-    // dS of key tile j lives in buffer j & 1: a thread writing tile j+1 cannot
-    // overwrite values a slower thread of the warpgroup still reads for tile j
-    float *dsc_t = s_dsc + t * 2 * BK;
-    const float *qbar = s_qbar + t * D;
-    uint8_t *prow = sP + t * C::P_BYTES;
+    const float dq = p.dq[(size_t)bh * p.Tm + qi];
     float m = -INFINITY, l = 0.0f;
-    for (int j = 0; j < T_t; ++j) {
-      const int s = j % ST;
+    bool stop = false;  // a wait failed late in the previous tile
+    for (int j = 0, bb = 0, pj = 0; j < T; ++j, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
       const float dkj = p.dk[(size_t)hkv * p.Tn + j];
-      const float k1 = dq * dkj * c2;
-      float *dsc = dsc_t + (j & 1) * BK;
+      const float k1 = dq * dkj * c2;  // S code -> t
+      // this warpgroup's copy of dS for all BK keys of the tile
+      float *dsc = s_dsc + ((j & 1) * 2 + hf) * BK;
+      // the TMEM loads are warp-collective: the warp decides together
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin));
       if (smooth_q) {
-        // dS_j[c] = delta_K,j * sum_d q_bar[d] K^_j[c, d]: one key column per thread
-        bool fail = !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
+        // dS_j[c] = delta_K,j * sum_d q_bar[d] K^_j[c, d]: thread r < BK takes key r
+        const int s = j % KST;
+        const bool fail = !mbar_wait(&k_full[s], (j / KST) & 1, status, 31, s_abort, p.spin);
         if (!fail && r < BK) {
           const uint8_t *kt = sK + s * C::K_BYTES;
           float acc = 0.0f;
@@ -402,94 +401,124 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
-                  acc = fmaf(qbar[d0 + 2 * e], f.x, acc);
-                  acc = fmaf(qbar[d0 + 2 * e + 1], f.y, acc);
+                  acc = fmaf(s_qbar[d0 + 2 * e], f.x, acc);
+                  acc = fmaf(s_qbar[d0 + 2 * e + 1], f.y, acc);
                 }
               } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                   const uint32_t h2 = cvt_e4m3x2_to_f16x2((uint16_t)(ww[e >> 1] >> ((e & 1) * 16)));
                   const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                  acc = fmaf(qbar[d0 + 2 * e], f.x, acc);
-                  acc = fmaf(qbar[d0 + 2 * e + 1], f.y, acc);
+                  acc = fmaf(s_qbar[d0 + 2 * e], f.x, acc);
+                  acc = fmaf(s_qbar[d0 + 2 * e + 1], f.y, acc);
                 }
               }
             }
           }
           dsc[r] = acc * dkj * c2;
         }
-        // leave together: a thread that stops here must not strand the others
-        // at this barrier in the next tile
-        if (named_bar_any(1 + t, kWG, fail || *s_abort)) break;
+        // the warpgroup leaves together: a warp that stops alone would strand
+        // the others at this barrier in the next tile
+        if (named_bar_any(1 + hf, kWG, stop || fail || !okw || *s_abort)) break;
+      } else if (stop || !okw) {
+        break;
       }
-      // the TMEM loads below are warp-collective: the warp decides together
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, status, 32, s_abort, p.spin))) break;
       tc_fence_after();
-      // the whole score row in one TMEM read
-      uint32_t v[BK];
+      // x: this half's scores in a domain that orders like t.  Without dS and
+      // with k1 > 0 that is the raw MMA output (t = x k1, the scale folded
+      // into the exponent below); otherwise t itself (xs = 1), so a masked
+      // -inf never meets a zero scale.
+      const bool raw = !smooth_q && k1 > 0.0f;
+      const float xs = raw ? k1 : 1.0f;
+      float x[HALF];
+      {
+        uint32_t v[HALF];
 #pragma unroll
-      for (int ch = 0; ch < BK / 32; ++ch) tmem_ld32(sS + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
-      tmem_wait_ld();
-      const bool need_mask = ((j + 1) * BK > p.M) || (p.causal && (j + 1) * BK - 1 > row0 + p.M - p.N);
-      if (smooth_q) {
+        for (int ch = 0; ch < HALF / 32; ++ch)
+          tmem_ld32(tS + bb * C::SRW + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
+        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < BK; ++e) v[e] = __float_as_uint(fmaf(__uint_as_float(v[e]), k1, dsc[e]));
+        for (int e = 0; e < HALF; ++e) x[e] = __uint_as_float(v[e]);
       }
-      if (need_mask) {
+      if (!raw) {
+        if (smooth_q) {
 #pragma unroll
-        for (int e = 0; e < BK; ++e) {
-          const int key = j * BK + e;
-          if (key >= p.M || (p.causal && key > diag)) v[e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < HALF; ++e) x[e] = fmaf(x[e], k1, dsc[hf * HALF + e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < HALF; ++e) x[e] *= k1;
         }
       }
-      // row max; without dS, k1 >= 0 makes max(k1 s) = k1 max(s)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if ((j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N)) {
+        // edge tile: keys at or past lim are invisible to this row
+        const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK - hf * HALF;
 #pragma unroll
-      for (int e = 0; e < BK; e += 8) {
-        mx[0] = fmax3(mx[0], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        mx[1] = fmax3(mx[1], __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-        mx[2] = fmax3(mx[2], __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-        mx[3] = fmax3(mx[3], __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+        for (int e = 0; e < HALF; ++e) x[e] = (e < lim) ? x[e] : -INFINITY;
       }
-      const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float mt = smooth_q ? mraw : (mraw == -INFINITY ? -INFINITY : mraw * k1);
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < HALF; e += 8) {
+        mq[0] = fmax3(mq[0], x[e], x[e + 1]);
+        mq[1] = fmax3(mq[1], x[e + 2], x[e + 3]);
+        mq[2] = fmax3(mq[2], x[e + 4], x[e + 5]);
+        mq[3] = fmax3(mq[3], x[e + 6], x[e + 7]);
+      }
+      const float mh = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+      s_mx[((j & 1) * 2 + hf) * 128 + r] = mh;
+      mbar_arrive(&mx_full[(j & 1) * 2 + hf]);
+      // e = exp2(t - m_half) in place
+      const float mht = (mh == -INFINITY) ? 0.0f : mh * xs;
+      const float2 xs2 = make_float2(xs, xs), nm2 = make_float2(-mht, -mht);
+      float2 se2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int u = 0; u < HALF; u += 2) {
+        const float2 arg = __ffma2_rn(make_float2(x[u], x[u + 1]), xs2, nm2);
+        x[u] = ex2_approx(arg.x);
+        x[u + 1] = ex2_approx(arg.y);
+        se2 = __fadd2_rn(se2, make_float2(x[u], x[u + 1]));
+      }
+      // the other half's maximum
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&mx_full[(j & 1) * 2 + oh], (j >> 1) & 1, status, 33, s_abort, p.spin))) {
+        stop = true;
+        if (!smooth_q) break;
+        continue;  // leave with the warpgroup at the next dS barrier
+      }
+      const float mt = fmaxf(mh * xs, s_mx[((j & 1) * 2 + oh) * 128 + r] * xs);  // row max of t over the tile
       const float m_new = fmaxf(m, mt);
-      const float alpha = ex2_approx(m - m_new);
-      const float mb = m_new - kLog2_448;
-      // P^ = e4m3(448 exp2(t - m_new)); row sum of the unquantized values
-      const float2 kk2 = smooth_q ? f2(1.0f, 1.0f) : f2(k1, k1);
-      const float2 nb2 = f2(-mb, -mb);
-      float2 rs2 = f2(0.0f, 0.0f);
+      const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
+      // P^ = e4m3(448 exp2(t - m_new)) = e4m3(e g)
+      const float g = (mh == -INFINITY) ? 0.0f : ex2_approx(mht - m_new + kLog2_448);
+      const float2 g2 = make_float2(g, g);
+      uint8_t *prow = sP + bb * C::P_BYTES;
 #pragma unroll
-      for (int ch = 0; ch < BK / 32; ++ch) {
-        uint32_t pk[8];
+      for (int ch = 0; ch < HALF / 16; ++ch) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int i0 = ch * 32 + e;
-          const float2 x01 = __ffma2_rn(f2(__uint_as_float(v[i0]), __uint_as_float(v[i0 + 1])), kk2, nb2);
-          const float2 x23 = __ffma2_rn(f2(__uint_as_float(v[i0 + 2]), __uint_as_float(v[i0 + 3])), kk2, nb2);
-          const float2 p01 = f2(ex2_approx(x01.x), ex2_approx(x01.y));
-          const float2 p23 = f2(ex2_approx(x23.x), ex2_approx(x23.y));
-          rs2 = __fadd2_rn(rs2, __fadd2_rn(p01, p23));
+        for (int e = 0; e < 16; e += 4) {
+          const int i0 = ch * 16 + e;
+          const float2 p01 = __fmul2_rn(make_float2(x[i0], x[i0 + 1]), g2);
+          const float2 p23 = __fmul2_rn(make_float2(x[i0 + 2], x[i0 + 3]), g2);
           pk[e / 4] = (uint32_t)cvt_e4m3x2(p01.x, p01.y) | ((uint32_t)cvt_e4m3x2(p23.x, p23.y) << 16);
         }
-        *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, 2 * ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, 2 * ch + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        // keys hf HALF + 16 ch .. +15 are 16-byte chunk (hf HALF / 16 + ch) of row r
+        *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, hf * (HALF / 16) + ch)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l = fmaf(alpha, l, rs2.x + rs2.y);
+      l = fmaf(alpha, l, g * (se2.x + se2.y));  // 448 times this half's sum of P~
       m = m_new;
-      s_alpha[t * 128 + r] = alpha;
-      if (j == T_t - 1) s_l[t * 128 + r] = l;
+      if (hf == 0) s_alpha[bb * 128 + r] = alpha;
+      if (j == T - 1) s_l[hf * 128 + r] = l;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&p_full[bb]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == kQkWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int D, int BK, bool kQK16>
@@ -511,7 +540,6 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.N_pad = L.N_pad;
   p.M_pad = L.M_pad;
   p.Tm = L.Tm;
-  p.Tm2 = (L.Tm + 1) / 2;
   p.Tn = L.Tn;
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;
@@ -530,11 +558,10 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   // the register split needs the launch allocation it was computed for
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (fa.numRegs < kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
+  if (fa.numRegs != kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL) != cudaSuccess)
     return SAGE_ERR_CUDA;
-  const unsigned grid = (unsigned)(s.B * s.Hq * p.Tm2);
-  kern<<<grid, kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  kern<<<(unsigned)(s.B * s.Hq * L.Tm), kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
