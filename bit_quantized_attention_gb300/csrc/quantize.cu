@@ -51,19 +51,10 @@ __device__ __forceinline__ float order_val(int k) { return __int_as_float(k >= 0
 
 __device__ __forceinline__ bool in_range(float f) { return fabsf(f) < 65536.0f; }  // false for NaN too
 
-// trunc(x * 2^24) toward zero for a bf16 x (its fp32 value f), from the bits:
-// x = (-1)^s * (128 + mant) * 2^(e - 134), so x * 2^24 = (128 + mant) * 2^(e - 110);
-// a right shift truncates the magnitude toward zero.  Zero and subnormals give 0;
-// inf / NaN (rejected by the range check) are clamped to keep the shift defined.
-__device__ __forceinline__ long long fixed24(float f) {
-  const uint32_t b = __float_as_uint(f) >> 16;
-  const int e = (int)((b >> 7) & 0xFF);
-  const long long m = (long long)((b & 0x7F) | 0x80);
-  const int sh = min(e - 110, 40);
-  long long a = (sh >= 0) ? (m << sh) : (sh > -8 ? (m >> -sh) : 0);
-  if (e == 0) a = 0;
-  return (b & 0x8000) ? -a : a;
-}
+// trunc(x * 2^24) toward zero for a bf16 x (its fp32 value f): the scaling by
+// 2^24 is exact in binary32 (a bf16 value times 2^24 stays a normal number),
+// and the conversion truncates toward zero; any |x| < 2^39 fits the result.
+__device__ __forceinline__ long long fixed24(float f) { return __float2ll_rz(f * 0x1p24f); }
 
 __device__ __forceinline__ float mean_from_sum(long long sum, int n) {
   return __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(sum), 0x1p-24), (double)n));
@@ -109,19 +100,21 @@ __global__ void init_kernel(StatsView st, int n, int *status) {
 }
 
 // ------------------------------------------------------------------ stats
-// grid (ceil(M / kStatTokens), B*Hkv).  Column sums of K and V (fixed point),
-// column min / max of V, range check of K and V.  Each thread owns 8 channels
-// of every RPP-th row; loads are issued in batches of kBatch rows so several
-// are in flight; partial results meet in warp shuffles, then shared memory.
-template <int D>
+// grid (ceil(M / kStatTokens), B*Hkv).  Fixed-point column sums of K (when K
+// is smoothed) and V (when V is smoothed), column min / max of V, range check
+// of K and V.  Each thread owns 8 channels of every RPP-th row; loads are
+// issued in batches of kBatch rows so several are in flight.  Min / max run
+// on packed bf16 pairs with NaN propagation (they are exact, and a NaN or an
+// out-of-range value shows in the extremes).
+template <int D, bool kSumK, bool kSumV>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                          int M, StatsView st, int *status) {
   constexpr int VPR = D / 8;               // 16-byte vectors per row (threads per row)
   constexpr int RPP = kThreads / VPR;      // rows per pass
   constexpr int kBatch = 4;
   constexpr int NW = kThreads / 32;
-  __shared__ long long sk[NW][D];
-  __shared__ long long sv[NW][D];
+  __shared__ long long sk[kSumK ? NW : 1][D];
+  __shared__ long long sv[kSumV ? NW : 1][D];
   __shared__ int smin[NW][D];
   __shared__ int smax[NW][D];
   const int hb = blockIdx.y;
@@ -129,15 +122,21 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   const int t0 = blockIdx.x * kStatTokens;
   const int t1 = min(M, t0 + kStatTokens);
   long long ks[8], vs[8];
-  float vmn[8], vmx[8];
+  __nv_bfloat162 kmn[4], kmx[4], vmn[4], vmx[4];
+  const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80), __ushort_as_bfloat16(0x7F80));
+  const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     ks[e] = 0;
     vs[e] = 0;
-    vmn[e] = __int_as_float(0x7F800000);
-    vmx[e] = __int_as_float(0xFF800000);
   }
-  bool bad_k = false, bad_v = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    kmn[i] = pinf;
+    vmn[i] = pinf;
+    kmx[i] = ninf;
+    vmx[i] = ninf;
+  }
   for (int tb = t0 + rr; tb < t1; tb += kBatch * RPP) {
     uint4 kb[kBatch], vb[kBatch];
 #pragma unroll
@@ -150,19 +149,42 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       if (tb + i * RPP >= t1) break;
-      float fk[8], fv[8];
-      unpack_bf16x8(kb[i], fk);
-      unpack_bf16x8(vb[i], fv);
+      const uint32_t kw[4] = {kb[i].x, kb[i].y, kb[i].z, kb[i].w};
+      const uint32_t vw[4] = {vb[i].x, vb[i].y, vb[i].z, vb[i].w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bad_k |= !in_range(fk[e]);
-        bad_v |= !in_range(fv[e]);
-        ks[e] += fixed24(fk[e]);
-        vs[e] += fixed24(fv[e]);
-        vmn[e] = fminf(vmn[e], fv[e]);
-        vmx[e] = fmaxf(vmx[e], fv[e]);
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 kx = *reinterpret_cast<const __nv_bfloat162 *>(&kw[q]);
+        const __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(&vw[q]);
+        kmn[q] = __hmin2_nan(kmn[q], kx);
+        kmx[q] = __hmax2_nan(kmx[q], kx);
+        vmn[q] = __hmin2_nan(vmn[q], vx);
+        vmx[q] = __hmax2_nan(vmx[q], vx);
+        if (kSumK) {
+          ks[2 * q] += fixed24(__uint_as_float(kw[q] << 16));
+          ks[2 * q + 1] += fixed24(__uint_as_float(kw[q] & 0xFFFF0000u));
+        }
+        if (kSumV) {
+          vs[2 * q] += fixed24(__uint_as_float(vw[q] << 16));
+          vs[2 * q + 1] += fixed24(__uint_as_float(vw[q] & 0xFFFF0000u));
+        }
       }
     }
+  }
+  // range: every |x| < 2^16 and no NaN (a NaN fails both comparisons)
+  float vmnf[8], vmxf[8];
+  bool bad_k = false, bad_v = false;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 a = __bfloat1622float2(kmn[q]), b = __bfloat1622float2(kmx[q]);
+    const float2 c = __bfloat1622float2(vmn[q]), d = __bfloat1622float2(vmx[q]);
+    if (t0 + rr < t1) {
+      bad_k |= !(a.x > -65536.0f && a.y > -65536.0f && b.x < 65536.0f && b.y < 65536.0f);
+      bad_v |= !(c.x > -65536.0f && c.y > -65536.0f && d.x < 65536.0f && d.y < 65536.0f);
+    }
+    vmnf[2 * q] = c.x;
+    vmnf[2 * q + 1] = c.y;
+    vmxf[2 * q] = d.x;
+    vmxf[2 * q + 1] = d.y;
   }
   if (bad_k) raise_status(status, SAGE_ERR_RANGE, 1);
   if (bad_v) raise_status(status, SAGE_ERR_RANGE, 2);
@@ -171,20 +193,20 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   for (int o = VPR; o < 32; o <<= 1) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
-      vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
-      vmn[e] = fminf(vmn[e], __shfl_xor_sync(0xffffffffu, vmn[e], o));
-      vmx[e] = fmaxf(vmx[e], __shfl_xor_sync(0xffffffffu, vmx[e], o));
+      if (kSumK) ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
+      if (kSumV) vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
+      vmnf[e] = fminf(vmnf[e], __shfl_xor_sync(0xffffffffu, vmnf[e], o));
+      vmxf[e] = fmaxf(vmxf[e], __shfl_xor_sync(0xffffffffu, vmxf[e], o));
     }
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l < VPR) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      sk[w][vc * 8 + e] = ks[e];
-      sv[w][vc * 8 + e] = vs[e];
-      smin[w][vc * 8 + e] = order_key(vmn[e]);
-      smax[w][vc * 8 + e] = order_key(vmx[e]);
+      if (kSumK) sk[w][vc * 8 + e] = ks[e];
+      if (kSumV) sv[w][vc * 8 + e] = vs[e];
+      smin[w][vc * 8 + e] = order_key(vmnf[e]);
+      smax[w][vc * 8 + e] = order_key(vmxf[e]);
     }
   }
   __syncthreads();
@@ -193,17 +215,32 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
     int mn = smin[0][c], mx = smax[0][c];
 #pragma unroll
     for (int r = 0; r < NW; ++r) {
-      a += sk[r][c];
-      b += sv[r][c];
+      if (kSumK) a += sk[r][c];
+      if (kSumV) b += sv[r][c];
       mn = min(mn, smin[r][c]);
       mx = max(mx, smax[r][c]);
     }
     const size_t i = (size_t)hb * D + c;
-    atomicAdd((unsigned long long *)&st.ksum[i], (unsigned long long)a);
-    atomicAdd((unsigned long long *)&st.vsum[i], (unsigned long long)b);
+    if (kSumK) atomicAdd((unsigned long long *)&st.ksum[i], (unsigned long long)a);
+    if (kSumV) atomicAdd((unsigned long long *)&st.vsum[i], (unsigned long long)b);
     atomicMin(&st.vmin[i], mn);
     atomicMax(&st.vmax[i], mx);
   }
+}
+
+template <int D>
+void launch_stats(dim3 grid, int flags, const void *k, const void *v, int M, StatsView st, int *status,
+                  cudaStream_t stream) {
+  const bool sk = (flags & SAGE_SMOOTH_K) != 0, sv = (flags & SAGE_SMOOTH_V) != 0;
+  const uint4 *k4 = (const uint4 *)k, *v4 = (const uint4 *)v;
+  if (sk && sv)
+    stats_kernel<D, true, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+  else if (sk)
+    stats_kernel<D, true, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+  else if (sv)
+    stats_kernel<D, false, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+  else
+    stats_kernel<D, false, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
 }
 
 // ------------------------------------------------------------------ finalize
@@ -663,9 +700,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
   dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
   if (s.d == 64)
-    stats_kernel<64><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+    launch_stats<64>(sg, flags, k, v, s.M, st, status, stream);
   else
-    stats_kernel<128><<<sg, kThreads, 0, stream>>>((const uint4 *)k, (const uint4 *)v, s.M, st, status);
+    launch_stats<128>(sg, flags, k, v, s.M, st, status, stream);
   finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, s.M, flags, (float *)(w + L.kbar),
                                                         (float *)(w + L.vm), (float *)(w + L.dv));
   if (mode == SAGE_NVFP4) {
