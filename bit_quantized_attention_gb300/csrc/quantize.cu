@@ -41,7 +41,7 @@ namespace sage {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kStatTokens = 256;  // tokens per statistics CTA
+constexpr int kStatTokens = 256;  // tokens per statistics CTA (at most 64 rows per thread)
 
 __device__ __forceinline__ int order_key(float f) {
   int i = __float_as_int(f);
@@ -51,10 +51,37 @@ __device__ __forceinline__ float order_val(int k) { return __int_as_float(k >= 0
 
 __device__ __forceinline__ bool in_range(float f) { return fabsf(f) < 65536.0f; }  // false for NaN too
 
-// trunc(x * 2^24) toward zero for a bf16 x (its fp32 value f): the scaling by
-// 2^24 is exact in binary32 (a bf16 value times 2^24 stays a normal number),
-// and the conversion truncates toward zero; any |x| < 2^39 fits the result.
-__device__ __forceinline__ long long fixed24(float f) { return __float2ll_rz(f * 0x1p24f); }
+// trunc(x * 2^24) toward zero for a bf16 x (its fp32 value f), from the bits:
+// x = (-1)^s * (128 + mant) * 2^(e - 134), so x * 2^24 = (128 + mant) * 2^(e - 110);
+// a right shift truncates the magnitude toward zero.  Zero and subnormals give 0;
+// inf / NaN (rejected by the range check) are clamped to keep the shift defined.
+__device__ __forceinline__ long long fixed24(float f) {
+  const uint32_t b = __float_as_uint(f) >> 16;
+  const int e = (int)((b >> 7) & 0xFF);
+  const long long m = (long long)((b & 0x7F) | 0x80);
+  const int sh = min(e - 110, 40);
+  long long a = (sh >= 0) ? (m << sh) : (sh > -8 ? (m >> -sh) : 0);
+  if (e == 0) a = 0;
+  return (b & 0x8000) ? -a : a;
+}
+
+// The same value accumulated into two 32-bit buckets, in units of 1 (lo) and
+// of 2^16 (hi): with e - 110 = sh, m << sh for 0 <= sh < 16 and
+// (m << (sh - 16)) * 2^16 for sh >= 16.  For |x| < 2^16 a term is below 2^24 in
+// either bucket, so 64 terms fit in an int; the shift is clamped for inf / NaN.
+__device__ __forceinline__ void fixed24_acc(uint32_t b, int &lo, int &hi) {
+  const int e = (int)((b >> 7) & 0xFF);
+  const int m = (int)((b & 0x7F) | 0x80);
+  const int sh = e - 110;
+  const bool big = sh >= 16;
+  const int t = big ? min(sh - 16, 16) : sh;
+  int v = t >= 0 ? (m << t) : (t > -9 ? (m >> -t) : 0);
+  v = (b & 0x8000) ? -v : v;
+  if (big)
+    hi += v;
+  else
+    lo += v;
+}
 
 __device__ __forceinline__ float mean_from_sum(long long sum, int n) {
   return __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(sum), 0x1p-24), (double)n));
@@ -121,14 +148,13 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
   const int t0 = blockIdx.x * kStatTokens;
   const int t1 = min(M, t0 + kStatTokens);
-  long long ks[8], vs[8];
+  int klo[8], khi[8], vlo[8], vhi[8];
   __nv_bfloat162 kmn[4], kmx[4], vmn[4], vmx[4];
   const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80), __ushort_as_bfloat16(0x7F80));
   const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    ks[e] = 0;
-    vs[e] = 0;
+    klo[e] = khi[e] = vlo[e] = vhi[e] = 0;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -160,12 +186,12 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
         vmn[q] = __hmin2_nan(vmn[q], vx);
         vmx[q] = __hmax2_nan(vmx[q], vx);
         if (kSumK) {
-          ks[2 * q] += fixed24(__uint_as_float(kw[q] << 16));
-          ks[2 * q + 1] += fixed24(__uint_as_float(kw[q] & 0xFFFF0000u));
+          fixed24_acc(kw[q] & 0xFFFF, klo[2 * q], khi[2 * q]);
+          fixed24_acc(kw[q] >> 16, klo[2 * q + 1], khi[2 * q + 1]);
         }
         if (kSumV) {
-          vs[2 * q] += fixed24(__uint_as_float(vw[q] << 16));
-          vs[2 * q + 1] += fixed24(__uint_as_float(vw[q] & 0xFFFF0000u));
+          fixed24_acc(vw[q] & 0xFFFF, vlo[2 * q], vhi[2 * q]);
+          fixed24_acc(vw[q] >> 16, vlo[2 * q + 1], vhi[2 * q + 1]);
         }
       }
     }
@@ -188,6 +214,12 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   }
   if (bad_k) raise_status(status, SAGE_ERR_RANGE, 1);
   if (bad_v) raise_status(status, SAGE_ERR_RANGE, 2);
+  long long ks[8], vs[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ks[e] = (long long)khi[e] * 65536 + klo[e];
+    vs[e] = (long long)vhi[e] * 65536 + vlo[e];
+  }
   // lanes vc, vc + VPR, ... of a warp hold the same channels
 #pragma unroll
   for (int o = VPR; o < 32; o <<= 1) {
@@ -295,28 +327,54 @@ __device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float d0, flo
   return cvt_e4m3x2(__fdiv_rn(x0, d0), __fdiv_rn(x1, d1));
 }
 
-// Codes of 8 smoothed values with scale delta: 8 fp16 integers (INT8 mode,
-// 16 bytes) or 8 E4M3 bytes (FP8 mode).
+// Codes of 8 smoothed values g = fl(f - mu) with scale delta: 8 fp16 integers
+// (INT8 mode, 16 bytes) or 8 E4M3 bytes (FP8 mode).  INT8: q = g * RN(1/delta)
+// is rounded to the nearest integer; when no q of the group lies within 1e-4 of
+// a half-integer that is rint(RN(g / delta)) (see int8_code), otherwise the
+// group takes the exact path.  |g| <= amax keeps |q| below 127.5, so no clamp
+// is reached.
 template <bool kInt8>
-__device__ __forceinline__ void encode8(const float (&g)[8], float delta, float rcp, bool valid, uint8_t *dst) {
-  const bool on = valid && delta != 0.0f;
+__device__ __forceinline__ void encode8(const float (&f)[8], const float (&mu)[8], float delta, float rcp, bool on,
+                                        uint8_t *dst) {
   if (kInt8) {
-    uint32_t w[4];
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (on) {
+      float g[8], c[8];
+      float dmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float c0 = on ? int8_code(g[2 * i], delta, rcp) : 0.0f;
-      const float c1 = on ? int8_code(g[2 * i + 1], delta, rcp) : 0.0f;
-      const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
-      w[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+      for (int i = 0; i < 4; ++i) {
+        const float2 g2 = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), make_float2(-mu[2 * i], -mu[2 * i + 1]));
+        const float2 q2 = __fmul2_rn(g2, make_float2(rcp, rcp));
+        g[2 * i] = g2.x;
+        g[2 * i + 1] = g2.y;
+        c[2 * i] = rintf(q2.x);
+        c[2 * i + 1] = rintf(q2.y);
+        const float2 d2 = __fadd2_rn(q2, make_float2(-c[2 * i], -c[2 * i + 1]));
+        dmax = fmaxf(dmax, fmaxf(fabsf(d2.x), fabsf(d2.y)));
+      }
+      if (!(dmax < 0.4999f)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = int8_code(g[e], delta, rcp);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(c[2 * i], c[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&h);
+      }
     }
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   } else {
-    uint32_t w[2];
+    uint32_t w[2] = {0, 0};
+    if (on) {
+      float g[8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint16_t c01 = on ? e4m3_code2(g[4 * i], g[4 * i + 1], delta, delta, rcp, rcp) : 0;
-      const uint16_t c23 = on ? e4m3_code2(g[4 * i + 2], g[4 * i + 3], delta, delta, rcp, rcp) : 0;
-      w[i] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+      for (int e = 0; e < 8; ++e) g[e] = __fsub_rn(f[e], mu[e]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint16_t c01 = e4m3_code2(g[4 * i], g[4 * i + 1], delta, delta, rcp, rcp);
+        const uint16_t c23 = e4m3_code2(g[4 * i + 2], g[4 * i + 3], delta, delta, rcp, rcp);
+        w[i] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+      }
     }
     *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
   }
@@ -325,6 +383,9 @@ __device__ __forceinline__ void encode8(const float (&g)[8], float delta, float 
 // One block of `rows` rows (<= 128) of a [*, D] bf16 matrix: optional
 // per-block mean (fixed point over the valid rows) or a given mean, then the
 // per-block absmax scale and the codes.  Rows past `valid_rows` get code 0.
+// The absmax max_r |fl(x_r - mu)| of a channel is taken from the channel's
+// extremes (rounded subtraction is monotone), which packed bf16 min / max
+// track exactly; they also carry the range check (NaN propagates).
 template <int D, bool kInt8>
 __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
                             const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
@@ -334,12 +395,27 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
   __shared__ float smean[D];
   __shared__ float red[kThreads / 32];
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80), __ushort_as_bfloat16(0x7F80));
+  const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
   uint4 x[PASSES];
-  bool bad = false;
+  __nv_bfloat162 mn[4] = {pinf, pinf, pinf, pinf}, mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
     x[p] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int r = rr + p * RPP;
+    if (r < valid_rows) {
+      const uint32_t w[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
+        mn[q] = __hmin2_nan(mn[q], b2);
+        mx[q] = __hmax2_nan(mx[q], b2);
+      }
+    }
   }
   if (own_mean) {
     long long s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -349,10 +425,7 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
       float f[8];
       unpack_bf16x8(x[p], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bad |= !in_range(f[e]);
-        s[e] += fixed24(f[e]);
-      }
+      for (int e = 0; e < 8; ++e) s[e] += fixed24(f[e]);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) ssum[rr][vc * 8 + e] = s[e];
@@ -370,18 +443,17 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 #pragma unroll
   for (int e = 0; e < 8; ++e) mu[e] = smean[vc * 8 + e];
   float amax = 0.0f;
+  if (rr < valid_rows) {  // this thread saw at least one row
+    bool bad = false;
 #pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    if (rr + p * RPP >= valid_rows) continue;
-    float f[8];
-    unpack_bf16x8(x[p], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      bad |= !in_range(f[e]);
-      amax = fmaxf(amax, fabsf(__fsub_rn(f[e], mu[e])));
+    for (int q = 0; q < 4; ++q) {
+      const float2 lo = __bfloat1622float2(mn[q]), hi = __bfloat1622float2(mx[q]);
+      bad |= !(lo.x > -65536.0f && lo.y > -65536.0f && hi.x < 65536.0f && hi.y < 65536.0f);
+      amax = fmaxf(amax, fmaxf(fabsf(__fsub_rn(hi.x, mu[2 * q])), fabsf(__fsub_rn(lo.x, mu[2 * q]))));
+      amax = fmaxf(amax, fmaxf(fabsf(__fsub_rn(hi.y, mu[2 * q + 1])), fabsf(__fsub_rn(lo.y, mu[2 * q + 1]))));
     }
+    if (bad) raise_status(status, SAGE_ERR_RANGE, site);
   }
-  if (bad) raise_status(status, SAGE_ERR_RANGE, site);
   amax = block_max(amax, red);
   const float delta = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
   const float rcp = __frcp_rn(delta);
@@ -390,11 +462,9 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
     if (r >= rows) continue;
-    float f[8], g[8];
+    float f[8];
     unpack_bf16x8(x[p], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = __fsub_rn(f[e], mu[e]);
-    encode8<kInt8>(g, delta, rcp, r < valid_rows, dst + ((size_t)r * D + vc * 8) * CB);
+    encode8<kInt8>(f, mu, delta, rcp, r < valid_rows && delta != 0.0f, dst + ((size_t)r * D + vc * 8) * CB);
   }
   if (threadIdx.x == 0) *delta_out = delta;
   if (mean_out)
