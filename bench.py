@@ -84,8 +84,9 @@ def read_traffic(key: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms in the background while running."""
-    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+    """nvidia-smi sampled every 50 ms in the background; summary() keeps the
+    samples whose timestamps fall inside the timed window."""
+    FIELDS = "timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
 
@@ -93,6 +94,7 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.path = None
+        self.window = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -100,13 +102,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark(self, t0: float, t1: float):
+        """wall-clock bounds of the timed region"""
+        self.window = (t0, t1)
+
     def __exit__(self, *a):
+        time.sleep(0.1)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -115,30 +122,35 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
             except ValueError:
                 continue
         os.unlink(self.path)
-        if not rows:
+        inside = [r for r in rows if self.window and self.window[0] <= r["ts"] <= self.window[1]]
+        use = inside or rows
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sms = sorted(r["sm"] for r in rows)
+        sms = sorted(r["sm"] for r in use)
         reasons = set()
-        for r in rows:
+        for r in use:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in rows),
-                "samples": len(rows), "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in use),
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max(r["power"] for r in use), "reasons": sorted(reasons)}
 
 
 def dist_env():
@@ -151,16 +163,18 @@ def dist_env():
 # --------------------------------------------------------------------------- reference arm
 class OracleSample:
     """The oracle (as it stands) on a bounded sample of the workload: the
-    pre-pass of one (batch, kv-head) and the attention rows of a spread of
-    query rows of its heads, on all host cores."""
+    pre-pass of some (batch, kv-head) groups and the attention rows of a spread
+    of query rows of their heads, on all host cores."""
 
-    def __init__(self, cfg, threads: int | None = None):
+    def __init__(self, cfg, threads: int | None = None, groups: int = 1):
         import oracle
         from workload import make_inputs
         self.oracle = oracle
         self.cfg = cfg
         self.threads = threads or os.cpu_count() or 1
-        self.sub = cfg.with_(B=1, Hq=cfg.Hq // cfg.Hkv, Hkv=1)   # one kv-head and its query heads
+        g = max(1, min(cfg.Hkv, groups))
+        # g kv-heads of batch 0 and their query heads
+        self.sub = cfg.with_(B=1, Hq=(cfg.Hq // cfg.Hkv) * g, Hkv=g)
         self.q, self.k, self.v = make_inputs(self.sub)
         s = self.sub
         self.shape = (s.B, s.Hq, s.Hkv, s.N, s.M, s.d)
@@ -188,22 +202,28 @@ class OracleSample:
         t_total = ta + tq * (len(rows) / (s.Hq * s.N))
         return 4.0 * s.d * pairs * lit_over_exact / t_total / 1e12, t_total, len(rows)
 
-    def calibrated_rows(self, budget_s: float) -> int:
-        _, secs, n = self.run(32)
-        return int(max(32, min(self.sub.Hq * self.sub.N, budget_s / max(secs / n, 1e-6))))
+    @classmethod
+    def calibrated(cls, cfg, budget_s: float):
+        """A sample sized to about budget_s seconds of oracle work."""
+        smp = cls(cfg)
+        _, secs, n = smp.run(32)
+        want = int(max(32, budget_s / max(secs / n, 1e-6)))
+        per_group = smp.sub.Hq * smp.sub.N
+        if want > per_group and cfg.Hkv > 1:
+            smp = cls(cfg, groups=-(-want // per_group))
+        return smp, int(min(want, smp.sub.Hq * smp.sub.N))
 
     def describe(self, nrows: int) -> str:
-        return ("oracle pre-pass of 1 kv-head (%d query heads, time prorated) + attention of %d query rows "
-                "spread over them" % (self.sub.Hq, nrows))
+        return ("oracle pre-pass of %d kv-head(s) (%d query heads, time prorated) + attention of %d query rows "
+                "spread over them" % (self.sub.Hkv, self.sub.Hq, nrows))
 
 
 def run_reference(args, cfg):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    smp = OracleSample(cfg)
     per_step = max(1.0, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
-    nrows = smp.calibrated_rows(per_step)
+    smp, nrows = OracleSample.calibrated(cfg, per_step)
     vals = []
     for i in range(args.warmup + args.steps):
         tops, secs, _ = smp.run(nrows)
@@ -283,11 +303,13 @@ def run_gpu(args, cfg):
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize(dev)
+        w0 = time.time()
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark(w0, time.time())
         barrier()
     clocks = clk.summary()
     total_ms = t_start.elapsed_time(t_end)
@@ -351,8 +373,7 @@ def run_gpu(args, cfg):
         "device_status": list(code),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        smp = OracleSample(cfg)
-        nrows = smp.calibrated_rows(args.ref_budget)
+        smp, nrows = OracleSample.calibrated(cfg, args.ref_budget)
         tops, secs, _ = smp.run(nrows)
         out["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": smp.threads, "kind": "oracle",
                                "sample": smp.describe(nrows), "seconds": secs}
@@ -375,7 +396,7 @@ def kernel_hash() -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llm_prefill")
     ap.add_argument("--bk", type=int, default=128, help="key tile = K scale block (the workload leaves it open)")

@@ -91,6 +91,20 @@ def test_attention_fp4_matches_oracle_small(sage, cfg):
     check(cfg, o.reshape(-1, cfg.d), q, k, v, rows)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_zero_scale_key_tile(sage, mode):
+    """The last key tile (keys 256..332, ragged and causal-masked) is all zero
+    without K smoothing, so its K scale is 0: every visible score of that tile
+    is 0 and the masked keys must still drop out (no 0 * inf)."""
+    cfg = _small("zero_tile", mode=mode, N=200, M=333, causal=True, flags=0, d=128, bk=128, k_offset_std=0.0)
+    q, k, v = make_inputs(cfg)
+    k[:, :, 256:, :] = 0
+    o = gpu_attention(sage, cfg, q, k, v)
+    assert np.isfinite(o).all()
+    rows = oracle.all_rows((cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d))
+    check(cfg, o.reshape(-1, cfg.d), q, k, v, rows)
+
+
 def test_attention_deterministic(sage):
     cfg = ATTN_SMALL[-2]
     q, k, v = make_inputs(cfg)
