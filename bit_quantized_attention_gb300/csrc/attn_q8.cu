@@ -16,7 +16,11 @@
 // scale is delta_V / l.
 //
 // GB300 mapping (the pages' Ada/Hopper register-level design is prior art):
-// one query block per CTA and 16 warps.
+// a persistent CTA per SM walks its share of the work items (one query block
+// of one head each, longest causal rows first, round robin over the CTAs) with
+// 16 warps; every ring and barrier phase runs on tile counters that continue
+// across items, so the next item's loads and first MMAs overlap the previous
+// item's last tiles and epilogue.
 //   warps 0-7   two warpgroups on the same 128 query rows (one row per thread,
 //               its TMEM lane); warpgroup h takes keys [h BK/2, (h+1) BK/2) of
 //               every tile: dequantize, dS, mask, exponentials, P^ into the
@@ -74,7 +78,7 @@ struct Cfg {
   static constexpr int P_BYTES = 128 * BK;
   static constexpr int QK_KSTEPS = ROWB / 32;            // one MMA consumes 32 bytes of K
   static constexpr int PV_KSTEPS = BK / 32;
-  static constexpr int NFLOAT = NB * 128 /*alpha*/ + 2 * 128 /*l*/ + 4 * 128 /*max*/ + 3 * D + 4 * BK /*dS*/;
+  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + 2 * D /*q_bar*/ + 4 * BK /*dS*/;
   static constexpr int FIXED = Q_BYTES + NB * P_BYTES;
   static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
   // K and V have rings of their own: a K tile is free once its QK has run
@@ -94,6 +98,7 @@ struct Cfg {
 
 struct AttnParams {
   int N, M, N_pad, M_pad, Tm, Tn, Hq, Hkv, causal, flags;
+  int items;      // B * Hq * Tm work items (one query block of one head each)
   float sm_log2;  // sm_scale * log2(e)
   const float *dq, *qbar, *dk, *dv, *vm;
   __nv_bfloat16 *o;
@@ -107,6 +112,23 @@ template <int SW>
 __device__ __forceinline__ uint32_t swz_off(int r, int c) {
   const int x = (SW == 128) ? (r & 7) : ((r & 7) >> 1);
   return (uint32_t)((r >> 3) * (8 * SW) + (r & 7) * SW + ((c ^ x) << 4));
+}
+
+// Work item idx of the grid-wide list: longest causal rows first.
+struct Item {
+  int bh, qi, hkv, row0, T;
+};
+__device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
+  Item it;
+  const int BH = p.items / p.Tm;
+  it.qi = p.Tm - 1 - idx / BH;
+  it.bh = idx % BH;
+  const int b = it.bh / p.Hq, h = it.bh % p.Hq;
+  it.hkv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  it.row0 = it.qi * 128;
+  const int last_row = min(p.N, it.row0 + 128) - 1;
+  it.T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
+  return it;
 }
 
 template <int D, int BK, bool kQK16>
@@ -123,22 +145,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sK = sP + NB * C::P_BYTES;   // [KST]
   uint8_t *sV = sK + KST * C::K_BYTES;  // [VST]
   float *s_alpha = (float *)(sV + VST * C::V_BYTES);  // [NB][128]
-  float *s_l = s_alpha + NB * 128;                   // [2 halves][128]
-  float *s_mx = s_l + 2 * 128;                       // [2 parities][2 halves][128]
-  float *s_qbar = s_mx + 4 * 128;                    // [D]
-  float *s_dv = s_qbar + D;                          // [D]
-  float *s_vm = s_dv + D;                            // [D]
-  float *s_dsc = s_vm + D;                           // [2 buffers][2 halves][BK]
+  float *s_l = s_alpha + NB * 128;                   // [NB][2 halves][128], at an item's last tile
+  float *s_mx = s_l + NB * 256;                      // [2 parities][2 halves][128]
+  float *s_qbar = s_mx + 4 * 128;                    // [2 halves][D]
+  float *s_dsc = s_qbar + 2 * D;                     // [2 buffers][2 halves][BK]
   uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 4 * BK) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
-  uint64_t *k_full = q_full + 1;     // [KST]
+  uint64_t *q_empty = q_full + 1;
+  uint64_t *k_full = q_empty + 1;    // [KST]
   uint64_t *k_empty = k_full + KST;  // [KST]
   uint64_t *v_full = k_empty + KST;  // [VST]
   uint64_t *v_empty = v_full + VST;  // [VST]
-  uint64_t *s_full = v_empty + VST;  // [NB] S(j) in TMEM
-  uint64_t *p_full = s_full + NB;    // [NB] P^(j), alpha(j) written; S(j) read
-  uint64_t *r_full = p_full + NB;    // [NB] R(j) in TMEM
-  uint64_t *sr_free = r_full + NB;   // [NB] R(j) folded into O; region free
+  uint64_t *s_full = v_empty + VST;  // [NB] S in TMEM
+  uint64_t *p_full = s_full + NB;    // [NB] P^, alpha written; S read
+  uint64_t *r_full = p_full + NB;    // [NB] R in TMEM
+  uint64_t *sr_free = r_full + NB;   // [NB] R folded into O; region free
   uint64_t *mx_full = sr_free + NB;  // [2 parities][2 halves] half maxima
   uint64_t *qk_done = mx_full + 4;
   uint64_t *pv_done = qk_done + 1;
@@ -146,17 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.Tm;
-  const int qi = p.Tm - 1 - blockIdx.x % p.Tm;  // longest causal rows first
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int hkv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int row0 = qi * 128;
-  const int last_row = min(p.N, row0 + 128) - 1;
-  const int T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
+  const int G = gridDim.x;
   const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -181,11 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  for (int c = threadIdx.x; c < D; c += kThreads) {
-    s_qbar[c] = smooth_q ? p.qbar[((size_t)bh * p.Tm + qi) * D + c] : 0.0f;
-    s_dv[c] = p.dv[(size_t)hkv * D + c];
-    s_vm[c] = p.vm[(size_t)hkv * D + c];
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -196,78 +207,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_dealloc<kControlRegs>();
     if (warp == kProducerWarp && lane == 0) {
       // ---------------------------------------------------------- TMA producer
+      // Three streams walk the CTA's items: Q once per item (after the previous
+      // item's last QK has run), K tiles up to KST ahead of V, V tiles.  The
+      // thread never blocks on one stream while another could move; a stretch
+      // of spin_limit cycles without progress is a timeout.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_expect_tx(q_full, C::Q_BYTES);
+      int qn = 0, kn = 0, vn = 0;            // local item of the Q, K, V streams
+      int kj = 0, vj = 0, gk = 0, gv = 0;    // tile within the item; global tile counters
+      Item qit, kit, vit;
+      if (blockIdx.x < p.items) qit = kit = vit = item_of(p, blockIdx.x, BK);
+      bool q_more = blockIdx.x < p.items, k_more = q_more, v_more = q_more;
+      long long idle_since = clock64();
+      while (k_more || v_more || q_more) {
+        bool moved = false;
+        if (q_more && qn <= kn && (qn == 0 || mbar_try_wait(q_empty, (qn - 1) & 1))) {
+          mbar_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-      for (int c = 0; c < C::QK_CHUNKS; ++c)
-        tma_load_2d(sQ + c * 128 * C::QK_SW, &tm_q, q_full, c * C::QK_SW, bh * p.N_pad + row0);
-      // K runs ahead of V: the QK issuer can start tile j+1 while tile j waits for its PV
-      int kj = 0, vj = 0;
-      bool fail = false;
-      while (!fail && (kj < T || vj < T)) {
-        if (kj < T && (kj < vj + KST)) {
-          const int s = kj % KST, n = kj / KST;
-          if (kj >= KST && !mbar_wait(&k_empty[s], (n - 1) & 1, status, 10, s_abort, p.spin)) {
-            fail = true;
-            break;
-          }
+          for (int c = 0; c < C::QK_CHUNKS; ++c)
+            tma_load_2d(sQ + c * 128 * C::QK_SW, &tm_q, q_full, c * C::QK_SW, qit.bh * p.N_pad + qit.row0);
+          ++qn;
+          const int nx = blockIdx.x + qn * G;
+          q_more = nx < p.items;
+          if (q_more) qit = item_of(p, nx, BK);
+          moved = true;
+        }
+        if (k_more && gk < gv + KST && (gk < KST || mbar_try_wait(&k_empty[gk % KST], ((gk / KST) - 1) & 1))) {
+          const int s = gk % KST;
           mbar_expect_tx(&k_full[s], C::K_BYTES);
 #pragma unroll
           for (int c = 0; c < C::QK_CHUNKS; ++c)
             tma_load_2d(sK + s * C::K_BYTES + c * BK * C::QK_SW, &tm_k, &k_full[s], c * C::QK_SW,
-                        hkv * p.M_pad + kj * BK);
-          ++kj;
+                        kit.hkv * p.M_pad + kj * BK);
+          ++gk;
+          if (++kj == kit.T) {
+            kj = 0;
+            const int nx = blockIdx.x + (++kn) * G;
+            k_more = nx < p.items;
+            if (k_more) kit = item_of(p, nx, BK);
+          }
+          moved = true;
         }
-        if (vj < T && (vj < kj || kj == T)) {
-          const int s = vj % VST, n = vj / VST;
-          // a V stage frees later than a K stage: only wait when K cannot go on
-          if (vj >= VST && kj < T && kj < vj + KST && !mbar_try_wait(&v_empty[s], (n - 1) & 1)) continue;
-          if (vj >= VST && !mbar_wait(&v_empty[s], (n - 1) & 1, status, 12, s_abort, p.spin)) {
-            fail = true;
+        if (v_more && gv < gk && (gv < VST || mbar_try_wait(&v_empty[gv % VST], ((gv / VST) - 1) & 1))) {
+          const int s = gv % VST;
+          mbar_expect_tx(&v_full[s], C::V_BYTES);
+          tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], vj * BK, vit.hkv * D);
+          ++gv;
+          if (++vj == vit.T) {
+            vj = 0;
+            const int nx = blockIdx.x + (++vn) * G;
+            v_more = nx < p.items;
+            if (v_more) vit = item_of(p, nx, BK);
+          }
+          moved = true;
+        }
+        if (moved) {
+          idle_since = clock64();
+        } else {
+          if (*s_abort) break;
+          if (clock64() - idle_since > p.spin) {
+            if (atomicCAS(status, 0, SAGE_ERR_TIMEOUT) == 0) status[1] = 10;
+            *s_abort = 1;
             break;
           }
-          mbar_expect_tx(&v_full[s], C::V_BYTES);
-          tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], vj * BK, hkv * D);
-          ++vj;
+          __nanosleep(32);
         }
       }
       // drain: every load this warp issued lands before the CTA exits
       volatile int no_abort = 0;
-      mbar_wait(q_full, 0, status, 11, &no_abort, p.spin);
-      for (int j = max(0, kj - KST); j < kj; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, status, 11, &no_abort, p.spin);
-      for (int j = max(0, vj - VST); j < vj; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, status, 11, &no_abort, p.spin);
+      if (qn > 0) mbar_wait(q_full, (qn - 1) & 1, status, 11, &no_abort, p.spin);
+      for (int j = max(0, gk - KST); j < gk; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, status, 11, &no_abort, p.spin);
+      for (int j = max(0, gv - VST); j < gv; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, status, 11, &no_abort, p.spin);
     } else if (warp == kQkWarp) {
       // ---------------------------------------------------------- QK issuer (whole warp, one lane issues)
-      // S(j) goes to S/R region j % NB once the accumulation has consumed R of
-      // tile j - NB there.
+      // S goes to S/R region gt % NB once the accumulation has consumed the R of
+      // tile gt - NB there; the Q buffer is released after an item's last QK.
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, status, 23, s_abort, p.spin));
-      for (int j = 0; ok && j < T; ++j) {
-        const int b = j % NB, s = j % KST;
-        bool w = true;
-        if (j >= NB) w = mbar_wait(&sr_free[b], ((j - NB) / NB) & 1, status, 20, s_abort, p.spin);
-        w = w && mbar_wait(&k_full[s], (j / KST) & 1, status, 21, s_abort, p.spin);
-        if (!__all_sync(0xffffffffu, w)) break;
-        tc_fence_after();
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
-            const int byte = kk * 32;
-            const uint32_t aq = q_base + (byte / C::QK_SW) * 128 * C::QK_SW + (byte % C::QK_SW);
-            const uint32_t bk = k_base + s * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
-            const uint64_t ad = smem_desc(aq, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
-            const uint64_t bd = smem_desc(bk, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
-            if (kQK16)
-              mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
-            else
-              mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+      bool ok = true;
+      int gt = 0;
+      for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
+        const Item it = item_of(p, blockIdx.x + n * G, BK);
+        if (!__all_sync(0xffffffffu, mbar_wait(q_full, n & 1, status, 23, s_abort, p.spin))) break;
+        for (int j = 0; j < it.T; ++j, ++gt) {
+          const int b = gt % NB, s = gt % KST;
+          bool w = true;
+          if (gt >= NB) w = mbar_wait(&sr_free[b], ((gt - NB) / NB) & 1, status, 20, s_abort, p.spin);
+          w = w && mbar_wait(&k_full[s], (gt / KST) & 1, status, 21, s_abort, p.spin);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
           }
-          mma_commit(&s_full[b]);
-          if (!smooth_q) mma_commit(&k_empty[s]);  // with dS the softmax still reads K^_j
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
+              const int byte = kk * 32;
+              const uint32_t aq = q_base + (byte / C::QK_SW) * 128 * C::QK_SW + (byte % C::QK_SW);
+              const uint32_t bk = k_base + s * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
+              const uint64_t ad = smem_desc(aq, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
+              const uint64_t bd = smem_desc(bk, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
+              if (kQK16)
+                mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+              else
+                mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+            }
+            mma_commit(&s_full[b]);
+            if (!smooth_q) mma_commit(&k_empty[s]);  // with dS the softmax still reads K^
+            if (j == it.T - 1) mma_commit(q_empty);  // Q^ may be replaced once these MMAs are done
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       // every MMA of this thread has finished before the CTA may leave
       if (elect_one()) mma_commit(qk_done);
@@ -276,29 +326,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(qk_done, 0, status, 25, &no_abort, p.spin);
     } else if (warp == kPvWarp) {
       // ---------------------------------------------------------- PV issuer (whole warp, one lane issues)
-      // R(j) = P^(j) V^_j, a fresh accumulator over this key tile only, into
-      // S/R region j % NB once the softmax has read S(j) there
+      // R = P^ V^, a fresh accumulator over one key tile, into S/R region gt % NB
+      // once the softmax has read S there
       const uint32_t v_base = smem_u32(sV), p_base = smem_u32(sP);
-      for (int j = 0; j < T; ++j) {
-        const int b = j % NB, s = j % VST;
-        const bool w = mbar_wait(&p_full[b], (j / NB) & 1, status, 22, s_abort, p.spin) &&
-                       mbar_wait(&v_full[s], (j / VST) & 1, status, 24, s_abort, p.spin);
-        if (!__all_sync(0xffffffffu, w)) break;
-        tc_fence_after();
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
-            const uint64_t ad = smem_desc(p_base + b * C::P_BYTES + kk * 32, 8 * C::PV_SW,
-                                          C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
-            const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * C::PV_SW,
-                                          C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
-            mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
+      int gt = 0;
+      bool ok = true;
+      for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
+        const Item it = item_of(p, blockIdx.x + n * G, BK);
+        for (int j = 0; j < it.T; ++j, ++gt) {
+          const int b = gt % NB, s = gt % VST;
+          const bool w = mbar_wait(&p_full[b], (gt / NB) & 1, status, 22, s_abort, p.spin) &&
+                         mbar_wait(&v_full[s], (gt / VST) & 1, status, 24, s_abort, p.spin);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
           }
-          mma_commit(&r_full[b]);
-          mma_commit(&v_empty[s]);
-          if (smooth_q) mma_commit(&k_empty[j % KST]);  // the softmax has read K^_j (p_full)
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+              const uint64_t ad = smem_desc(p_base + b * C::P_BYTES + kk * 32, 8 * C::PV_SW,
+                                            C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
+              const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * C::PV_SW,
+                                            C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
+              mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
+            }
+            mma_commit(&r_full[b]);
+            mma_commit(&v_empty[s]);
+            if (smooth_q) mma_commit(&k_empty[gt % KST]);  // the softmax has read K^ (p_full)
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       if (elect_one()) mma_commit(pv_done);
       __syncwarp();
@@ -310,54 +368,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ two-level accumulation + epilogue
     const int r = threadIdx.x & (kWG - 1);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float o[D];  // this thread's row of the FP32 running output
-#pragma unroll
-    for (int c = 0; c < D; ++c) o[c] = 0.0f;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j % NB;
-      // alpha(j) is in shared memory once p_full says so, R(j) in TMEM once
-      // r_full does; the TMEM loads are warp-collective, so the warp decides together
-      const bool waited = mbar_wait(&p_full[b], (j / NB) & 1, status, 40, s_abort, p.spin) &&
-                          mbar_wait(&r_full[b], (j / NB) & 1, status, 41, s_abort, p.spin);
-      if (!__all_sync(0xffffffffu, waited)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float a = s_alpha[b * 128 + r];
-      const float2 a2 = make_float2(a, a);
-      const uint32_t tR = tmem + lane_off + b * C::SRW;
+    int gt = 0;
+    for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
+      const Item it = item_of(p, blockIdx.x + n * G, BK);
+      float o[D];  // this thread's row of the FP32 running output
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t rv[32];
-        tmem_ld32(tR + ch * 32, rv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 o2 = __ffma2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2,
-                                       make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1])));
-          o[ch * 32 + e] = o2.x;
-          o[ch * 32 + e + 1] = o2.y;
+      for (int c = 0; c < D; ++c) o[c] = 0.0f;
+      float lsum = 0.0f;
+      for (int j = 0; j < it.T; ++j, ++gt) {
+        const int b = gt % NB;
+        // alpha in shared memory once p_full says so, R in TMEM once r_full
+        // does; the TMEM loads are warp-collective, so the warp decides together
+        const bool waited = mbar_wait(&p_full[b], (gt / NB) & 1, status, 40, s_abort, p.spin) &&
+                            mbar_wait(&r_full[b], (gt / NB) & 1, status, 41, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const float a = s_alpha[b * 128 + r];
+        if (j == it.T - 1) lsum = s_l[(b * 2 + 0) * 128 + r] + s_l[(b * 2 + 1) * 128 + r];
+        const float2 a2 = make_float2(a, a);
+        const uint32_t tR = tmem + lane_off + b * C::SRW;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t rv[32];
+          tmem_ld32(tR + ch * 32, rv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 o2 = __ffma2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2,
+                                         make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1])));
+            o[ch * 32 + e] = o2.x;
+            o[ch * 32 + e + 1] = o2.y;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sr_free[b]);
       }
-      tc_fence_before();
-      mbar_arrive(&sr_free[b]);
-    }
-    // epilogue: O / l * delta_V (+ V_m) in bf16
-    if (ok && T >= 1) {
-      const int row = row0 + r;
+      if (!ok) break;
+      // epilogue of this item: O / l * delta_V (+ V_m) in bf16
+      const int row = it.row0 + r;
       if (row < p.N) {
-        const float inv_l = 1.0f / (s_l[r] + s_l[128 + r]);
-        __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + row) * D;
+        const float inv_l = 1.0f / lsum;
+        const float *dv = p.dv + (size_t)it.hkv * D, *vm = p.vm + (size_t)it.hkv * D;
+        __nv_bfloat16 *dst = p.o + ((size_t)it.bh * p.N + row) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 8) {
+          const float4 dv0 = __ldg(reinterpret_cast<const float4 *>(dv + c));
+          const float4 dv1 = __ldg(reinterpret_cast<const float4 *>(dv + c + 4));
+          const float4 vm0 = __ldg(reinterpret_cast<const float4 *>(vm + c));
+          const float4 vm1 = __ldg(reinterpret_cast<const float4 *>(vm + c + 4));
+          const float dvs[8] = {dv0.x, dv0.y, dv0.z, dv0.w, dv1.x, dv1.y, dv1.z, dv1.w};
+          const float vms[8] = {vm0.x, vm0.y, vm0.z, vm0.w, vm1.x, vm1.y, vm1.z, vm1.w};
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cc = c + 2 * e;
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(fmaf(o[cc], s_dv[cc] * inv_l, s_vm[cc]),
-                                                            fmaf(o[cc + 1], s_dv[cc + 1] * inv_l, s_vm[cc + 1]));
+            const __nv_bfloat162 v2 =
+                __floats2bfloat162_rn(fmaf(o[c + 2 * e], dvs[2 * e] * inv_l, vms[2 * e]),
+                                      fmaf(o[c + 2 * e + 1], dvs[2 * e + 1] * inv_l, vms[2 * e + 1]));
             w[e] = *reinterpret_cast<const uint32_t *>(&v2);
           }
           *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -371,22 +441,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hf = warp >> 2;               // which half of the key tile
     const int oh = hf ^ 1;
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + hf * HALF;
-    const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
-    const float dq = p.dq[(size_t)bh * p.Tm + qi];
-    float m = -INFINITY, l = 0.0f;
-    bool stop = false;  // a wait failed late in the previous tile
-    for (int j = 0, bb = 0, pj = 0; j < T; ++j, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
-      const float dkj = p.dk[(size_t)hkv * p.Tn + j];
-      const float k1 = dq * dkj * c2;  // S code -> t
-      // this warpgroup's copy of dS for all BK keys of the tile
-      float *dsc = s_dsc + ((j & 1) * 2 + hf) * BK;
-      // the TMEM loads are warp-collective: the warp decides together
-      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin));
+    bool stop = false;  // a wait failed; leave with the warpgroup
+    int gt = 0, bb = 0, pj = 0;
+    // With dS a warp that stopped still comes to the warpgroup's next barrier,
+    // where the whole warpgroup leaves together; without dS there is none.
+    for (int n = 0; (smooth_q || !stop) && blockIdx.x + n * G < p.items; ++n) {
+      const Item it = item_of(p, blockIdx.x + n * G, BK);
+      const int diag = it.row0 + r + p.M - p.N;  // last key visible to this row (causal)
+      const float dq = p.dq[(size_t)it.bh * p.Tm + it.qi];
       if (smooth_q) {
-        // dS_j[c] = delta_K,j * sum_d q_bar[d] K^_j[c, d]: thread r < BK takes key r
-        const int s = j % KST;
-        const bool fail = !mbar_wait(&k_full[s], (j / KST) & 1, status, 31, s_abort, p.spin);
+        // this warpgroup's copy of q_bar for the item; the last dS barrier of the
+        // previous item has every reader of the old values behind it
+        if (!stop && r < D) s_qbar[hf * D + r] = p.qbar[((size_t)it.bh * p.Tm + it.qi) * D + r];
+        if (named_bar_any(1 + hf, kWG, stop || *s_abort)) {
+          stop = true;
+          break;
+        }
+      }
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < it.T; ++j, ++gt, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
+        const float dkj = p.dk[(size_t)it.hkv * p.Tn + j];
+        const float k1 = dq * dkj * c2;  // S code -> t
+        // this warpgroup's copy of dS for all BK keys of the tile
+        float *dsc = s_dsc + ((gt & 1) * 2 + hf) * BK;
+        // the TMEM loads are warp-collective: the warp decides together
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin));
+        if (smooth_q) {
+          // dS_j[c] = delta_K,j * sum_d q_bar[d] K^_j[c, d]: thread r < BK takes key r
+          const int s = gt % KST;
+          const bool fail = !mbar_wait(&k_full[s], (gt / KST) & 1, status, 31, s_abort, p.spin);
         if (!fail && r < BK) {
           const uint8_t *kt = sK + s * C::K_BYTES;
           float acc = 0.0f;
@@ -401,117 +485,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
-                  acc = fmaf(s_qbar[d0 + 2 * e], f.x, acc);
-                  acc = fmaf(s_qbar[d0 + 2 * e + 1], f.y, acc);
+                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e], f.x, acc);
+                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e + 1], f.y, acc);
                 }
               } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                   const uint32_t h2 = cvt_e4m3x2_to_f16x2((uint16_t)(ww[e >> 1] >> ((e & 1) * 16)));
                   const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                  acc = fmaf(s_qbar[d0 + 2 * e], f.x, acc);
-                  acc = fmaf(s_qbar[d0 + 2 * e + 1], f.y, acc);
+                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e], f.x, acc);
+                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e + 1], f.y, acc);
                 }
               }
             }
           }
           dsc[r] = acc * dkj * c2;
         }
-        // the warpgroup leaves together: a warp that stops alone would strand
-        // the others at this barrier in the next tile
-        if (named_bar_any(1 + hf, kWG, stop || fail || !okw || *s_abort)) break;
-      } else if (stop || !okw) {
-        break;
-      }
-      tc_fence_after();
-      // x: this half's scores in a domain that orders like t.  Without dS and
-      // with k1 > 0 that is the raw MMA output (t = x k1, the scale folded
-      // into the exponent below); otherwise t itself (xs = 1), so a masked
-      // -inf never meets a zero scale.
-      const bool raw = !smooth_q && k1 > 0.0f;
-      const float xs = raw ? k1 : 1.0f;
-      float x[HALF];
-      {
-        uint32_t v[HALF];
-#pragma unroll
-        for (int ch = 0; ch < HALF / 32; ++ch)
-          tmem_ld32(tS + bb * C::SRW + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < HALF; ++e) x[e] = __uint_as_float(v[e]);
-      }
-      if (!raw) {
-        if (smooth_q) {
-#pragma unroll
-          for (int e = 0; e < HALF; ++e) x[e] = fmaf(x[e], k1, dsc[hf * HALF + e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < HALF; ++e) x[e] *= k1;
+          // the warpgroup leaves together: a warp that stops alone would strand
+          // the others at this barrier in the next tile
+          if (named_bar_any(1 + hf, kWG, stop || fail || !okw || *s_abort)) {
+            stop = true;
+            break;
+          }
+        } else if (stop || !okw) {
+          stop = true;
+          break;
         }
-      }
-      if ((j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N)) {
-        // edge tile: keys at or past lim are invisible to this row
-        const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK - hf * HALF;
+        tc_fence_after();
+        // x: this half's scores in a domain that orders like t.  Without dS and
+        // with k1 > 0 that is the raw MMA output (t = x k1, the scale folded
+        // into the exponent below); otherwise t itself (xs = 1), so a masked
+        // -inf never meets a zero scale.
+        const bool raw = !smooth_q && k1 > 0.0f;
+        const float xs = raw ? k1 : 1.0f;
+        float x[HALF];
+        {
+          uint32_t v[HALF];
 #pragma unroll
-        for (int e = 0; e < HALF; ++e) x[e] = (e < lim) ? x[e] : -INFINITY;
-      }
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          for (int ch = 0; ch < HALF / 32; ++ch)
+            tmem_ld32(tS + bb * C::SRW + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[ch * 32]));
+          tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < HALF; e += 8) {
-        mq[0] = fmax3(mq[0], x[e], x[e + 1]);
-        mq[1] = fmax3(mq[1], x[e + 2], x[e + 3]);
-        mq[2] = fmax3(mq[2], x[e + 4], x[e + 5]);
-        mq[3] = fmax3(mq[3], x[e + 6], x[e + 7]);
-      }
-      const float mh = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
-      s_mx[((j & 1) * 2 + hf) * 128 + r] = mh;
-      mbar_arrive(&mx_full[(j & 1) * 2 + hf]);
-      // e = exp2(t - m_half) in place
-      const float mht = (mh == -INFINITY) ? 0.0f : mh * xs;
-      const float2 xs2 = make_float2(xs, xs), nm2 = make_float2(-mht, -mht);
-      float2 se2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int u = 0; u < HALF; u += 2) {
-        const float2 arg = __ffma2_rn(make_float2(x[u], x[u + 1]), xs2, nm2);
-        x[u] = ex2_approx(arg.x);
-        x[u + 1] = ex2_approx(arg.y);
-        se2 = __fadd2_rn(se2, make_float2(x[u], x[u + 1]));
-      }
-      // the other half's maximum
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&mx_full[(j & 1) * 2 + oh], (j >> 1) & 1, status, 33, s_abort, p.spin))) {
-        stop = true;
-        if (!smooth_q) break;
-        continue;  // leave with the warpgroup at the next dS barrier
-      }
-      const float mt = fmaxf(mh * xs, s_mx[((j & 1) * 2 + oh) * 128 + r] * xs);  // row max of t over the tile
-      const float m_new = fmaxf(m, mt);
-      const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
-      // P^ = e4m3(448 exp2(t - m_new)) = e4m3(e g)
-      const float g = (mh == -INFINITY) ? 0.0f : ex2_approx(mht - m_new + kLog2_448);
-      const float2 g2 = make_float2(g, g);
-      uint8_t *prow = sP + bb * C::P_BYTES;
-#pragma unroll
-      for (int ch = 0; ch < HALF / 16; ++ch) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const int i0 = ch * 16 + e;
-          const float2 p01 = __fmul2_rn(make_float2(x[i0], x[i0 + 1]), g2);
-          const float2 p23 = __fmul2_rn(make_float2(x[i0 + 2], x[i0 + 3]), g2);
-          pk[e / 4] = (uint32_t)cvt_e4m3x2(p01.x, p01.y) | ((uint32_t)cvt_e4m3x2(p23.x, p23.y) << 16);
+          for (int e = 0; e < HALF; ++e) x[e] = __uint_as_float(v[e]);
         }
-        // keys hf HALF + 16 ch .. +15 are 16-byte chunk (hf HALF / 16 + ch) of row r
-        *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, hf * (HALF / 16) + ch)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (!raw) {
+          if (smooth_q) {
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) x[e] = fmaf(x[e], k1, dsc[hf * HALF + e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) x[e] *= k1;
+          }
+        }
+        if ((j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > it.row0 + p.M - p.N)) {
+          // edge tile: keys at or past lim are invisible to this row
+          const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK - hf * HALF;
+#pragma unroll
+          for (int e = 0; e < HALF; ++e) x[e] = (e < lim) ? x[e] : -INFINITY;
+        }
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < HALF; e += 8) {
+          mq[0] = fmax3(mq[0], x[e], x[e + 1]);
+          mq[1] = fmax3(mq[1], x[e + 2], x[e + 3]);
+          mq[2] = fmax3(mq[2], x[e + 4], x[e + 5]);
+          mq[3] = fmax3(mq[3], x[e + 6], x[e + 7]);
+        }
+        const float mh = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+        s_mx[((gt & 1) * 2 + hf) * 128 + r] = mh;
+        mbar_arrive(&mx_full[(gt & 1) * 2 + hf]);
+        // e = exp2(t - m_half) in place
+        const float mht = (mh == -INFINITY) ? 0.0f : mh * xs;
+        const float2 xs2 = make_float2(xs, xs), nm2 = make_float2(-mht, -mht);
+        float2 se2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int u = 0; u < HALF; u += 2) {
+          const float2 arg = __ffma2_rn(make_float2(x[u], x[u + 1]), xs2, nm2);
+          x[u] = ex2_approx(arg.x);
+          x[u + 1] = ex2_approx(arg.y);
+          se2 = __fadd2_rn(se2, make_float2(x[u], x[u + 1]));
+        }
+        // the other half's maximum
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&mx_full[(gt & 1) * 2 + oh], (gt >> 1) & 1, status, 33, s_abort, p.spin))) {
+          stop = true;
+          if (!smooth_q) break;
+          continue;  // leave with the warpgroup at the next dS barrier
+        }
+        const float mt = fmaxf(mh * xs, s_mx[((gt & 1) * 2 + oh) * 128 + r] * xs);  // row max of t over the tile
+        const float m_new = fmaxf(m, mt);
+        const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
+        // P^ = e4m3(448 exp2(t - m_new)) = e4m3(e g)
+        const float g = (mh == -INFINITY) ? 0.0f : ex2_approx(mht - m_new + kLog2_448);
+        const float2 g2 = make_float2(g, g);
+        uint8_t *prow = sP + bb * C::P_BYTES;
+#pragma unroll
+        for (int ch = 0; ch < HALF / 16; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const int i0 = ch * 16 + e;
+            const float2 p01 = __fmul2_rn(make_float2(x[i0], x[i0 + 1]), g2);
+            const float2 p23 = __fmul2_rn(make_float2(x[i0 + 2], x[i0 + 3]), g2);
+            pk[e / 4] = (uint32_t)cvt_e4m3x2(p01.x, p01.y) | ((uint32_t)cvt_e4m3x2(p23.x, p23.y) << 16);
+          }
+          // keys hf HALF + 16 ch .. +15 are 16-byte chunk (hf HALF / 16 + ch) of row r
+          *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, hf * (HALF / 16) + ch)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l = fmaf(alpha, l, g * (se2.x + se2.y));  // 448 times this half's sum of P~
+        m = m_new;
+        if (hf == 0) s_alpha[bb * 128 + r] = alpha;
+        if (j == it.T - 1) s_l[(bb * 2 + hf) * 128 + r] = l;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[bb]);
       }
-      l = fmaf(alpha, l, g * (se2.x + se2.y));  // 448 times this half's sum of P~
-      m = m_new;
-      if (hf == 0) s_alpha[bb * 128 + r] = alpha;
-      if (j == T - 1) s_l[hf * 128 + r] = l;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[bb]);
     }
   }
 
@@ -541,6 +630,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.M_pad = L.M_pad;
   p.Tm = L.Tm;
   p.Tn = L.Tn;
+  p.items = s.B * s.Hq * L.Tm;
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;
   p.causal = causal ? 1 : 0;
@@ -561,7 +651,16 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   if (fa.numRegs != kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL) != cudaSuccess)
     return SAGE_ERR_CUDA;
-  kern<<<(unsigned)(s.B * s.Hq * L.Tm), kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  // one persistent CTA per SM (fewer when there are fewer items)
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return SAGE_ERR_CUDA;
+  }
+  const int grid = p.items < sms ? p.items : sms;
+  kern<<<(unsigned)grid, kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
