@@ -41,6 +41,7 @@ namespace sage {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kQuantCtas = 4;  // resident quantize CTAs per SM (caps registers at 64)
 constexpr int kStatTokens = 256;  // tokens per statistics CTA (at most 64 rows per thread)
 
 __device__ __forceinline__ int order_key(float f) {
@@ -386,14 +387,22 @@ __device__ __forceinline__ void encode8(const float (&f)[8], const float (&mu)[8
 // The absmax max_r |fl(x_r - mu)| of a channel is taken from the channel's
 // extremes (rounded subtraction is monotone), which packed bf16 min / max
 // track exactly; they also carry the range check (NaN propagates).
+// Shared memory of the Q/K role (fixed-point partial sums, mean, reduction)
+// and of the V role (per-channel mean / scale / reciprocal, transpose tile):
+// one pool, since a CTA takes one role.
+template <int D>
+__host__ __device__ constexpr int qk_pool_bytes() { return (kThreads / (D / 8)) * D * 8 + D * 4 + (kThreads / 32) * 4; }
+template <int D>
+__host__ __device__ constexpr int v_pool_bytes() { return 3 * D * 4 + D * 33 * 4; }
+
 template <int D, bool kInt8>
 __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
                             const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
-                            float *mean_out, int *status, int site) {
+                            float *mean_out, int *status, int site, unsigned char *pool) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
-  __shared__ long long ssum[RPP][D];
-  __shared__ float smean[D];
-  __shared__ float red[kThreads / 32];
+  long long (*ssum)[D] = reinterpret_cast<long long (*)[D]>(pool);
+  float *smean = reinterpret_cast<float *>(pool + RPP * D * 8);
+  float *red = smean + D;
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
   const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80), __ushort_as_bfloat16(0x7F80));
   const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
@@ -472,8 +481,10 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 }
 
 template <int D, bool kInt8>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArgs a) {
   constexpr int CB = kInt8 ? 2 : 1;
+  constexpr int kPool = qk_pool_bytes<D>() > v_pool_bytes<D>() ? qk_pool_bytes<D>() : v_pool_bytes<D>();
+  __shared__ __align__(16) unsigned char pool[kPool];
   int cta = blockIdx.x;
   if (cta < a.nq) {
     // ---- Q block (b, h, i)
@@ -484,7 +495,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
     float *qbar = a.qbar + ((size_t)bh * a.Tm + i) * D;
     quant_block<D, kInt8>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0, nullptr,
                           a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i, qbar,
-                          a.status, 3);
+                          a.status, 3, pool);
     return;
   }
   cta -= a.nq;
@@ -495,7 +506,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
     const int valid = max(0, min(a.bk, a.M - t0));
     quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, a.kbar + (size_t)hb * D,
                           a.khat + ((size_t)hb * a.M_pad + t0) * D * CB, a.dk + (size_t)hb * a.Tn + j, nullptr,
-                          a.status, 1);
+                          a.status, 1, pool);
     return;
   }
   cta -= a.nk;
@@ -508,8 +519,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   {
     const int nchunk = a.M_pad / 128;
     const int ch = cta % nchunk, hb = cta / nchunk;
-    __shared__ float vmean[D], vdelta[D], vrcp[D];
-    __shared__ uint32_t tile[D][33];
+    float *vmean = reinterpret_cast<float *>(pool), *vdelta = vmean + D, *vrcp = vdelta + D;
+    uint32_t (*tile)[33] = reinterpret_cast<uint32_t (*)[33]>(vrcp + D);
     for (int c = threadIdx.x; c < D; c += kThreads) {
       const size_t i = (size_t)hb * D + c;
       vmean[c] = a.vm[i];
