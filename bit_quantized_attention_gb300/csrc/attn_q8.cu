@@ -23,7 +23,7 @@
 // item's last tiles and epilogue.
 //   warps 0-7   two warpgroups on the same 128 query rows (one row per thread,
 //               its TMEM lane); warpgroup h takes keys [h BK/2, (h+1) BK/2) of
-//               every tile: dequantize, dS, mask, exponentials, P^ into the
+//               every tile: dequantize, add dS, mask, exponentials, P^ into the
 //               swizzled K-major A operand of the PV MMA in shared memory.
 //               Each half publishes its own maximum at once and takes its
 //               exponentials against it, e = exp2(t - m_half); the new running
@@ -31,7 +31,9 @@
 //               exp2(m_half - m_new)), so neither half waits on the other
 //               before its exponentials.
 //   warps 8-11  two-level accumulation O = alpha O + R with the thread's row
-//               of O in registers, then the epilogue
+//               of O in registers, then the epilogue; with Q smoothing also
+//               dS of the tile two ahead (one key per thread, from the K^ tile
+//               in shared memory), off the softmax's per-tile chain
 //   warp 12     TMA producer: Q^ once, K^_j and V^T_j into a ring of stages
 //   warp 13     QK issuer: S(j) = Q^ K^_j^T (kind::f16 on INT8 codes held as
 //               exact fp16 integers -- sm_103a has no INT8 tensor path -- or
@@ -78,11 +80,11 @@ struct Cfg {
   static constexpr int P_BYTES = 128 * BK;
   static constexpr int QK_KSTEPS = ROWB / 32;            // one MMA consumes 32 bytes of K
   static constexpr int PV_KSTEPS = BK / 32;
-  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + 2 * D /*q_bar*/ + 4 * BK /*dS*/;
+  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + NB * BK /*dS*/ + 2 * D /*q_bar*/;
   static constexpr int FIXED = Q_BYTES + NB * P_BYTES;
   static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
   // K and V have rings of their own: a K tile is free once its QK has run
-  // (and, with dS, once the softmax has read it); a V tile once its PV has
+  // (and, with dS, once the accumulation warpgroup has read it); a V tile once its PV has
   static constexpr int BUDGET = 225 * 1024 - 1024 - FIXED - MISC;
   static constexpr int VST = 2 * (K_BYTES + V_BYTES) <= BUDGET - K_BYTES ? 3 : 2;
   static constexpr int KST_FIT = (BUDGET - VST * V_BYTES) / K_BYTES;
@@ -131,7 +133,47 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
   return it;
 }
 
+// sum_d q_bar[d] K^[r, d] for key r of a K^ tile in shared memory (the codes
+// are exact in fp16 / E4M3; q_bar in shared memory too, every lane the same word)
 template <int D, int BK, bool kQK16>
+__device__ __forceinline__ float qbar_dot_key(const uint8_t *kt, const float *qbar, int r) {
+  using C = Cfg<D, BK, kQK16>;
+  constexpr int kSpan = C::QK_SW / 16;  // 16-byte chunks per swizzle span
+  // four independent chains; a short unroll: the caller keeps its row of O live
+  // in registers meanwhile
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+#pragma unroll 2
+  for (int k = 0; k < C::ROWB / 16; ++k) {
+    const int cc = k / kSpan, c16 = k % kSpan;
+    const uint4 w = *reinterpret_cast<const uint4 *>(kt + cc * BK * C::QK_SW + swz_off<C::QK_SW>(r, c16));
+    const int d0 = k * 16 / C::QK_EB;
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    if (kQK16) {
+      const float4 qa = *reinterpret_cast<const float4 *>(qbar + d0);
+      const float4 qb = *reinterpret_cast<const float4 *>(qbar + d0 + 4);
+      const float2 q2[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w), make_float2(qb.x, qb.y),
+                            make_float2(qb.z, qb.w)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        acc[e] = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&ww[e])), q2[e], acc[e]);
+    } else {
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4) {
+        const float4 q = *reinterpret_cast<const float4 *>(qbar + d0 + 4 * e4);
+        const uint32_t lo = cvt_e4m3x2_to_f16x2((uint16_t)(ww[e4] & 0xffffu));
+        const uint32_t hi = cvt_e4m3x2_to_f16x2((uint16_t)(ww[e4] >> 16));
+        acc[e4] = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&lo)), make_float2(q.x, q.y), acc[e4]);
+        acc[e4] = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&hi)), make_float2(q.z, q.w), acc[e4]);
+      }
+    }
+  }
+  return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+}
+
+// kSmoothQ: Q smoothing on (dS added to the scores); its instances carry the dS
+// stream, the others none of its state
+template <int D, int BK, bool kQK16, bool kSmoothQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -147,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_alpha = (float *)(sV + VST * C::V_BYTES);  // [NB][128]
   float *s_l = s_alpha + NB * 128;                   // [NB][2 halves][128], at an item's last tile
   float *s_mx = s_l + NB * 256;                      // [2 parities][2 halves][128]
-  float *s_qbar = s_mx + 4 * 128;                    // [2 halves][D]
-  float *s_dsc = s_qbar + 2 * D;                     // [2 buffers][2 halves][BK]
-  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 4 * BK) + 7) & ~(uintptr_t)7);
+  float *s_ds = s_mx + 4 * 128;                      // [NB][BK] dS of a tile, in t units
+  float *s_qb = s_ds + NB * BK;                      // [2 item parities][D] q_bar of the dS stream
+  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_qb + 2 * D) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
   uint64_t *q_empty = q_full + 1;
   uint64_t *k_full = q_empty + 1;    // [KST]
@@ -161,21 +203,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *r_full = p_full + NB;    // [NB] R in TMEM
   uint64_t *sr_free = r_full + NB;   // [NB] R folded into O; region free
   uint64_t *mx_full = sr_free + NB;  // [2 parities][2 halves] half maxima
-  uint64_t *qk_done = mx_full + 4;
+  uint64_t *ds_full = mx_full + 4;   // [NB] dS of the tile in s_ds
+  uint64_t *qb_full = ds_full + NB;  // [2] q_bar of the dS stream's item in s_qb
+  uint64_t *qk_done = qb_full + 2;
   uint64_t *pv_done = qk_done + 1;
   uint32_t *s_tmem = (uint32_t *)(pv_done + 1);
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
+  constexpr bool smooth_q = kSmoothQ;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], smooth_q ? 1 + kWG : 1);  // QK commit (+ the dS readers)
     }
     for (int s = 0; s < VST; ++s) {
       mbar_init(&v_full[s], 1);
@@ -186,8 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[x], 2 * kWG);
       mbar_init(&r_full[x], 1);
       mbar_init(&sr_free[x], kWG);
+      mbar_init(&ds_full[x], kWG);
     }
     for (int x = 0; x < 4; ++x) mbar_init(&mx_full[x], kWG);
+    for (int x = 0; x < 2; ++x) mbar_init(&qb_full[x], kWG);
     mbar_init(qk_done, 1);
     mbar_init(pv_done, 1);
     *s_abort = 0;
@@ -313,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
             }
             mma_commit(&s_full[b]);
-            if (!smooth_q) mma_commit(&k_empty[s]);  // with dS the softmax still reads K^
+            mma_commit(&k_empty[s]);
             if (j == it.T - 1) mma_commit(q_empty);  // Q^ may be replaced once these MMAs are done
           }
           __syncwarp();
@@ -353,7 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(&r_full[b]);
             mma_commit(&v_empty[s]);
-            if (smooth_q) mma_commit(&k_empty[gt % KST]);  // the softmax has read K^ (p_full)
           }
           __syncwarp();
         }
@@ -370,6 +415,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     int gt = 0;
+    // dS stream (Q smoothing): tile dg = item dn, tile dj of it.  Before the
+    // accumulation of tile gt the stream has produced dS up to tile gt + 1
+    // (waiting for its K^ if need be) and tile gt + 2 as well when that K^ has
+    // already landed: the wait on a K^ tile never holds up the accumulation
+    // that the QK issuer needs to free an S/R region.  Buffer dg % NB was last
+    // read by the softmax of tile dg - NB <= gt - 1, whose p_full this
+    // warpgroup has waited for; K^ stage dg % KST goes back to the producer
+    // after this read and the QK commit.  q_bar of item dn sits in
+    // s_qb[dn & 1], published through qb_full[dn & 1]: every thread arrives
+    // there after its last dS of item dn - 1, so no one still reads the
+    // buffer's previous item dn - 2.
+    static_assert(NB >= 3, "dS buffers: tiles gt + 1 and gt + 2 beside gt - 1");
+    int dn = 0, dj = 0, dg = 0, dT = 0;
+    const float *d_dk = nullptr;  // delta_K row of item dn
+    bool d_more = smooth_q && blockIdx.x < p.items, qb_wait = d_more;
+    auto ds_item = [&](int idx) {  // stage item idx of this CTA's list as item dn
+      const Item t1 = item_of(p, idx, BK);
+      if (r < D) s_qb[(dn & 1) * D + r] = p.qbar[((size_t)t1.bh * p.Tm + t1.qi) * D + r];
+      mbar_arrive(&qb_full[dn & 1]);
+      d_dk = p.dk + (size_t)t1.hkv * p.Tn;
+      dT = t1.T;
+    };
+    if (d_more) ds_item(blockIdx.x);
+    const float c2 = p.sm_log2;
     for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
       const Item it = item_of(p, blockIdx.x + n * G, BK);
       float o[D];  // this thread's row of the FP32 running output
@@ -378,6 +447,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lsum = 0.0f;
       for (int j = 0; j < it.T; ++j, ++gt) {
         const int b = gt % NB;
+        while (d_more && dg < gt + 3) {
+          // dS_j[c] = delta_K,j sum_d q_bar[d] K^_j[c, d], in t units: thread r takes key r
+          const int s = dg % KST;
+          const uint32_t ph = (dg / KST) & 1;
+          if (dg == gt + 2) {
+            if (!__all_sync(0xffffffffu, mbar_test_wait(&k_full[s], ph))) break;  // not yet: later
+          } else if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], ph, status, 42, s_abort, p.spin))) {
+            ok = false;
+            break;
+          }
+          if (qb_wait) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&qb_full[dn & 1], (dn >> 1) & 1, status, 43, s_abort, p.spin))) {
+              ok = false;
+              break;
+            }
+            qb_wait = false;
+          }
+          if (r < BK)
+            s_ds[(dg % NB) * BK + r] = qbar_dot_key<D, BK, kQK16>(sK + s * C::K_BYTES, s_qb + (dn & 1) * D, r) * d_dk[dj] * c2;
+          mbar_arrive(&ds_full[dg % NB]);
+          mbar_arrive(&k_empty[s]);
+          ++dg;
+          if (++dj == dT) {
+            dj = 0;
+            const int nx = blockIdx.x + (++dn) * G;
+            d_more = nx < p.items;
+            if (d_more) {
+              ds_item(nx);
+              qb_wait = true;
+            }
+          }
+        }
+        if (!ok) break;
         // alpha in shared memory once p_full says so, R in TMEM once r_full
         // does; the TMEM loads are warp-collective, so the warp decides together
         const bool waited = mbar_wait(&p_full[b], (gt / NB) & 1, status, 40, s_abort, p.spin) &&
@@ -442,72 +544,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int oh = hf ^ 1;
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + hf * HALF;
     const float c2 = p.sm_log2;
-    bool stop = false;  // a wait failed; leave with the warpgroup
+    bool stop = false;  // a wait failed
     int gt = 0, bb = 0, pj = 0;
-    // With dS a warp that stopped still comes to the warpgroup's next barrier,
-    // where the whole warpgroup leaves together; without dS there is none.
-    for (int n = 0; (smooth_q || !stop) && blockIdx.x + n * G < p.items; ++n) {
+    for (int n = 0; !stop && blockIdx.x + n * G < p.items; ++n) {
       const Item it = item_of(p, blockIdx.x + n * G, BK);
       const int diag = it.row0 + r + p.M - p.N;  // last key visible to this row (causal)
       const float dq = p.dq[(size_t)it.bh * p.Tm + it.qi];
-      if (smooth_q) {
-        // this warpgroup's copy of q_bar for the item; the last dS barrier of the
-        // previous item has every reader of the old values behind it
-        if (!stop && r < D) s_qbar[hf * D + r] = p.qbar[((size_t)it.bh * p.Tm + it.qi) * D + r];
-        if (named_bar_any(1 + hf, kWG, stop || *s_abort)) {
-          stop = true;
-          break;
-        }
-      }
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < it.T; ++j, ++gt, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
         const float dkj = p.dk[(size_t)it.hkv * p.Tn + j];
         const float k1 = dq * dkj * c2;  // S code -> t
-        // this warpgroup's copy of dS for all BK keys of the tile
-        float *dsc = s_dsc + ((gt & 1) * 2 + hf) * BK;
         // the TMEM loads are warp-collective: the warp decides together
-        const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin));
-        if (smooth_q) {
-          // dS_j[c] = delta_K,j * sum_d q_bar[d] K^_j[c, d]: thread r < BK takes key r
-          const int s = gt % KST;
-          const bool fail = !mbar_wait(&k_full[s], (gt / KST) & 1, status, 31, s_abort, p.spin);
-        if (!fail && r < BK) {
-          const uint8_t *kt = sK + s * C::K_BYTES;
-          float acc = 0.0f;
-#pragma unroll
-          for (int cc = 0; cc < C::QK_CHUNKS; ++cc) {
-#pragma unroll
-            for (int c16 = 0; c16 < C::QK_SW / 16; ++c16) {
-              const uint4 w = *reinterpret_cast<const uint4 *>(kt + cc * BK * C::QK_SW + swz_off<C::QK_SW>(r, c16));
-              const int d0 = (cc * C::QK_SW + c16 * 16) / C::QK_EB;
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-              if (kQK16) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
-                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e], f.x, acc);
-                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e + 1], f.y, acc);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const uint32_t h2 = cvt_e4m3x2_to_f16x2((uint16_t)(ww[e >> 1] >> ((e & 1) * 16)));
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e], f.x, acc);
-                  acc = fmaf(s_qbar[hf * D + d0 + 2 * e + 1], f.y, acc);
-                }
-              }
-            }
-          }
-          dsc[r] = acc * dkj * c2;
-        }
-          // the warpgroup leaves together: a warp that stops alone would strand
-          // the others at this barrier in the next tile
-          if (named_bar_any(1 + hf, kWG, stop || fail || !okw || *s_abort)) {
-            stop = true;
-            break;
-          }
-        } else if (stop || !okw) {
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin) &&
+                                                     (!smooth_q || mbar_wait(&ds_full[bb], pj, status, 31, s_abort, p.spin)));
+        if (!okw) {
           stop = true;
           break;
         }
@@ -530,8 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!raw) {
           if (smooth_q) {
+            const float4 *dsc = reinterpret_cast<const float4 *>(s_ds + bb * BK + hf * HALF);
+            const float2 k12 = make_float2(k1, k1);
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) x[e] = fmaf(x[e], k1, dsc[hf * HALF + e]);
+            for (int e = 0; e < HALF; e += 4) {
+              const float4 d4 = dsc[e / 4];
+              const float2 t01 = __ffma2_rn(make_float2(x[e], x[e + 1]), k12, make_float2(d4.x, d4.y));
+              const float2 t23 = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), k12, make_float2(d4.z, d4.w));
+              x[e] = t01.x;
+              x[e + 1] = t01.y;
+              x[e + 2] = t23.x;
+              x[e + 3] = t23.y;
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < HALF; ++e) x[e] *= k1;
@@ -569,8 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&mx_full[(gt & 1) * 2 + oh], (gt >> 1) & 1, status, 33, s_abort, p.spin))) {
           stop = true;
-          if (!smooth_q) break;
-          continue;  // leave with the warpgroup at the next dS barrier
+          break;
         }
         const float mt = fmaxf(mh * xs, s_mx[((gt & 1) * 2 + oh) * 128 + r] * xs);  // row max of t over the tile
         const float m_new = fmaxf(m, mt);
@@ -644,7 +703,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
-  auto kern = attn_q8_kernel<D, BK, kQK16>;
+  auto kern = (flags & SAGE_SMOOTH_Q) ? attn_q8_kernel<D, BK, kQK16, true> : attn_q8_kernel<D, BK, kQK16, false>;
   // the register split needs the launch allocation it was computed for
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;

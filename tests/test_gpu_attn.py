@@ -28,6 +28,10 @@ ATTN_SMALL = SMALL + [
     _small("causal_gqa_ragged", B=1, Hq=4, Hkv=1, N=131, M=4000, causal=True, flags=7, d=128),
     _small("long_keys", N=128, M=8192, flags=1, d=64, bk=128),
     _small("fp8_causal", mode=1, N=256, M=300, causal=True, flags=7, d=128),
+    # more work items than SMs: every persistent CTA walks several items of
+    # different lengths, so the dS stream and the rings cross item boundaries
+    _small("many_items_smooth", B=2, Hq=48, Hkv=48, N=600, M=700, causal=True, flags=7, d=64, bk=128),
+    _small("many_items_fp8_gqa_d128", mode=1, B=1, Hq=40, Hkv=8, N=520, M=520, flags=3, d=128, bk=128),
 ]
 
 FP4_ATTN_SMALL = FP4_SMALL + [
@@ -124,7 +128,7 @@ def sampled_rows(cfg, rng, extra=64):
     return np.unique(np.array(rows, dtype=np.int64))
 
 
-@pytest.mark.parametrize("name,bk", [("llm_prefill", 64), ("llm_prefill", 128), ("video", 64),
+@pytest.mark.parametrize("name,bk", [("llm_prefill", 64), ("llm_prefill", 128), ("video", 64), ("video", 128),
                                      ("chunked_gqa", 64), ("chunked_gqa", 128), ("nvfp4", 128)])
 def test_attention_full_size_sampled_rows(sage, name, bk):
     cfg = CONFIGS[name].with_(bk=bk)
