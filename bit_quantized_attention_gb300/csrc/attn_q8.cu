@@ -551,8 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int diag = it.row0 + r + p.M - p.N;  // last key visible to this row (causal)
       const float dq = p.dq[(size_t)it.bh * p.Tm + it.qi];
       float m = -INFINITY, l = 0.0f;
+      const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
+      float dk_next = dkr[0];
       for (int j = 0; j < it.T; ++j, ++gt, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
-        const float dkj = p.dk[(size_t)it.hkv * p.Tn + j];
+        const float dkj = dk_next;
+        if (j + 1 < it.T) dk_next = dkr[j + 1];  // the next tile's, its latency behind this tile
         const float k1 = dq * dkj * c2;  // S code -> t
         // the TMEM loads are warp-collective: the warp decides together
         const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin) &&
