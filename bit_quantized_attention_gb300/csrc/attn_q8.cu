@@ -555,7 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float dk_next = dkr[0];
       for (int j = 0; j < it.T; ++j, ++gt, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
         const float dkj = dk_next;
-        if (j + 1 < it.T) dk_next = dkr[j + 1];  // the next tile's, its latency behind this tile
         const float k1 = dq * dkj * c2;  // S code -> t
         // the TMEM loads are warp-collective: the warp decides together
         const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin) &&
@@ -565,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if (j + 1 < it.T) dk_next = dkr[j + 1];  // the next tile's, its latency behind this tile
         // x: this half's scores in a domain that orders like t.  Without dS and
         // with k1 > 0 that is the raw MMA output (t = x k1, the scale folded
         // into the exponent below); otherwise t itself (xs = 1), so a masked
