@@ -206,8 +206,13 @@ class OracleSample:
     def calibrated(cls, cfg, budget_s: float):
         """A sample sized to about budget_s seconds of oracle work."""
         smp = cls(cfg)
-        _, secs, n = smp.run(32)
-        want = int(max(32, budget_s / max(secs / n, 1e-6)))
+        # two probes: the cost of a row from their difference, so the fixed part
+        # of a run (thread start-up, the prorated pre-pass) does not count per row
+        _, s1, n1 = smp.run(32)
+        _, s2, n2 = smp.run(min(512, smp.sub.Hq * smp.sub.N))
+        per_row = max((s2 - s1) / max(n2 - n1, 1), s2 / max(n2, 1) / 4, 1e-6)
+        fixed = max(s1 - n1 * per_row, 0.0)
+        want = int(max(32, (budget_s - fixed) / per_row))
         per_group = smp.sub.Hq * smp.sub.N
         if want > per_group and cfg.Hkv > 1:
             smp = cls(cfg, groups=-(-want // per_group))
