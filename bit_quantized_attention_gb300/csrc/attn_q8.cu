@@ -66,7 +66,10 @@ static_assert(kSoftmaxRegs >= kLaunchRegs && kCorrRegs >= kLaunchRegs && kContro
 constexpr int NB = 3;  // S/R regions and P^ buffers
 constexpr float kLog2_448 = 8.807354922057604f;
 
-template <int D, int BK, bool kQK16>
+// kDsT: dS on the tensor core (Q smoothing with INT8 codes and 128-key tiles):
+// a 16-row tile of q_bar (fp16 hi / lo rows) per item parity in shared memory
+// and NB 16-column dS regions in TMEM
+template <int D, int BK, bool kQK16, bool kDsT = false>
 struct Cfg {
   static constexpr int HALF = BK / 2;                    // keys per softmax warpgroup
   static constexpr int QK_EB = kQK16 ? 2 : 1;           // bytes per stored Q/K code
@@ -81,7 +84,8 @@ struct Cfg {
   static constexpr int QK_KSTEPS = ROWB / 32;            // one MMA consumes 32 bytes of K
   static constexpr int PV_KSTEPS = BK / 32;
   static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + NB * BK /*dS*/ + 2 * D /*q_bar*/;
-  static constexpr int FIXED = Q_BYTES + NB * P_BYTES;
+  static constexpr int UB_BYTES = kDsT ? 16 * ROWB : 0;  // one q_bar tile (16 rows, K-major, swizzled)
+  static constexpr int FIXED = Q_BYTES + NB * P_BYTES + 2 * UB_BYTES;
   static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
   // K and V have rings of their own: a K tile is free once its QK has run
   // (and, with dS, once the accumulation warpgroup has read it); a V tile once its PV has
@@ -91,11 +95,16 @@ struct Cfg {
   static constexpr int KST = KST_FIT > 4 ? 4 : KST_FIT;
   static_assert(KST >= 2 && VST >= 2, "shared memory budget");
   static constexpr int SRW = BK > D ? BK : D;            // columns of one S / R region
-  static constexpr int TMEM_COLS = NB * SRW <= 256 ? 256 : 512;
+  static constexpr int DS_COL = NB * SRW;                // first column of the dS regions
+  static constexpr int TMEM_COLS = NB * SRW + (kDsT ? NB * 16 : 0) <= 256 ? 256 : 512;
+  static_assert(NB * SRW + (kDsT ? NB * 16 : 0) <= 512, "TMEM columns");
+  static_assert(!kDsT || (kQK16 && BK == 128 && QK_SW == 128), "dS on the tensor core: INT8 codes, 128-key tiles");
   static constexpr int SMEM_TOTAL = 1024 + FIXED + KST * K_BYTES + VST * V_BYTES + MISC;
   static constexpr uint32_t IDESC_QK =
       instr_desc(kFmtF32, kQK16 ? kFmtF16 : kFmtE4M3, kQK16 ? kFmtF16 : kFmtE4M3, BK, 128);
   static constexpr uint32_t IDESC_PV = instr_desc(kFmtF32, kFmtE4M3, kFmtE4M3, D, 128);
+  // dS^T = K^ (128 keys x d, A) x q_bar tile (16 x d, B): column 0 the hi row, 1 the lo row
+  static constexpr uint32_t IDESC_DS = instr_desc(kFmtF32, kFmtF16, kFmtF16, 16, 128);
 };
 
 struct AttnParams {
@@ -177,7 +186,10 @@ template <int D, int BK, bool kQK16, bool kSmoothQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = Cfg<D, BK, kQK16>;
+  // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles);
+  // otherwise the accumulation warpgroup takes it on CUDA cores
+  constexpr bool kDsMma = kSmoothQ && kQK16 && BK == 128;
+  using C = Cfg<D, BK, kQK16, kDsMma>;
   constexpr int KST = C::KST, VST = C::VST;
   constexpr int HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
@@ -186,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sP = sQ + C::Q_BYTES;        // [NB]
   uint8_t *sK = sP + NB * C::P_BYTES;   // [KST]
   uint8_t *sV = sK + KST * C::K_BYTES;  // [VST]
-  float *s_alpha = (float *)(sV + VST * C::V_BYTES);  // [NB][128]
+  uint8_t *sU = sV + VST * C::V_BYTES;  // [2 item parities] q_bar tiles (dS on the tensor core)
+  float *s_alpha = (float *)(sU + 2 * C::UB_BYTES);  // [NB][128]
   float *s_l = s_alpha + NB * 128;                   // [NB][2 halves][128], at an item's last tile
   float *s_mx = s_l + NB * 256;                      // [2 parities][2 halves][128]
   float *s_ds = s_mx + 4 * 128;                      // [NB][BK] dS of a tile, in t units
@@ -205,7 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mx_full = sr_free + NB;  // [2 parities][2 halves] half maxima
   uint64_t *ds_full = mx_full + 4;   // [NB] dS of the tile in s_ds
   uint64_t *qb_full = ds_full + NB;  // [2] q_bar of the dS stream's item in s_qb
-  uint64_t *qk_done = qb_full + 2;
+  uint64_t *dsr_full = qb_full + 2;  // [NB] dS^T of a tile in TMEM (tensor-core dS)
+  uint64_t *dsr_free = dsr_full + NB;  // [NB] that TMEM region read
+  uint64_t *ub_full = dsr_free + NB;   // [2] q_bar tile of an item written
+  uint64_t *ub_empty = ub_full + 2;    // [2] its last dS MMA done
+  uint64_t *qk_done = ub_empty + 2;
   uint64_t *pv_done = qk_done + 1;
   uint32_t *s_tmem = (uint32_t *)(pv_done + 1);
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
@@ -219,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_empty, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], smooth_q ? 1 + kWG : 1);  // QK commit (+ the dS readers)
+      mbar_init(&k_empty[s], (smooth_q && !kDsMma) ? 1 + kWG : 1);  // QK commit (+ the dS readers)
     }
     for (int s = 0; s < VST; ++s) {
       mbar_init(&v_full[s], 1);
@@ -231,6 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&r_full[x], 1);
       mbar_init(&sr_free[x], kWG);
       mbar_init(&ds_full[x], kWG);
+      mbar_init(&dsr_full[x], 1);
+      mbar_init(&dsr_free[x], kWG);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ub_full[x], kWG);
+      mbar_init(&ub_empty[x], 1);
     }
     for (int x = 0; x < 4; ++x) mbar_init(&mx_full[x], kWG);
     for (int x = 0; x < 2; ++x) mbar_init(&qb_full[x], kWG);
@@ -335,10 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
         const Item it = item_of(p, blockIdx.x + n * G, BK);
         if (!__all_sync(0xffffffffu, mbar_wait(q_full, n & 1, status, 23, s_abort, p.spin))) break;
+        // the item's q_bar tile (tensor-core dS)
+        if (kDsMma && !__all_sync(0xffffffffu, mbar_wait(&ub_full[n & 1], (n >> 1) & 1, status, 26, s_abort, p.spin)))
+          break;
         for (int j = 0; j < it.T; ++j, ++gt) {
           const int b = gt % NB, s = gt % KST;
           bool w = true;
           if (gt >= NB) w = mbar_wait(&sr_free[b], ((gt - NB) / NB) & 1, status, 20, s_abort, p.spin);
+          if (kDsMma && gt >= NB) w = w && mbar_wait(&dsr_free[b], ((gt - NB) / NB) & 1, status, 28, s_abort, p.spin);
           w = w && mbar_wait(&k_full[s], (gt / KST) & 1, status, 21, s_abort, p.spin);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
@@ -359,8 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
             }
             mma_commit(&s_full[b]);
+            if constexpr (kDsMma) {
+              // dS^T(tile) = K^ q_bar^T: the K^ tile as A (128 keys), the item's
+              // q_bar tile as B (16 rows: hi, lo, zeros) into dS region b
+              const uint32_t u_base = smem_u32(sU) + (n & 1) * C::UB_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
+                const int byte = kk * 32;
+                const uint32_t ak = k_base + s * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
+                const uint32_t bu = u_base + (byte / C::QK_SW) * 16 * C::QK_SW + (byte % C::QK_SW);
+                mma_f16(tmem + C::DS_COL + b * 16, smem_desc(ak, 8 * C::QK_SW, kSwizzle128),
+                        smem_desc(bu, 8 * C::QK_SW, kSwizzle128), C::IDESC_DS, kk > 0);
+              }
+              mma_commit(&dsr_full[b]);
+            }
             mma_commit(&k_empty[s]);
-            if (j == it.T - 1) mma_commit(q_empty);  // Q^ may be replaced once these MMAs are done
+            if (j == it.T - 1) {
+              mma_commit(q_empty);  // Q^ may be replaced once these MMAs are done
+              if (kDsMma) mma_commit(&ub_empty[n & 1]);  // and the item's q_bar tile
+            }
           }
           __syncwarp();
         }
@@ -432,11 +476,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool d_more = smooth_q && blockIdx.x < p.items, qb_wait = d_more;
     auto ds_item = [&](int idx) {  // stage item idx of this CTA's list as item dn
       const Item t1 = item_of(p, idx, BK);
-      if (r < D) s_qb[(dn & 1) * D + r] = p.qbar[((size_t)t1.bh * p.Tm + t1.qi) * D + r];
-      mbar_arrive(&qb_full[dn & 1]);
+      if constexpr (!kDsMma) {
+        if (r < D) s_qb[(dn & 1) * D + r] = p.qbar[((size_t)t1.bh * p.Tm + t1.qi) * D + r];
+        mbar_arrive(&qb_full[dn & 1]);
+      }
       d_dk = p.dk + (size_t)t1.hkv * p.Tn;
       dT = t1.T;
     };
+    // Tensor-core dS: the q_bar tile of item u (fp16 rows: hi = q_bar rounded
+    // toward zero, lo = the rest rounded to nearest; |q_bar| < 2^16 by the
+    // pre-pass range check, so hi + lo carries 22 bits) goes into buffer u & 1
+    // once the item u - 2 that used it has had its last dS MMA (ub_empty), and
+    // is published to the QK issuer through ub_full (every thread arrives after
+    // its writes and a proxy fence).  Rows 2..15 stay zero.  un counts the
+    // items written so far.
+    int un = 0;
+    auto prep_ub = [&](int u, bool block) -> int {  // 1 written, 0 not yet, -1 wait failed
+      if (u >= 2) {
+        const uint32_t ph = ((u - 2) >> 1) & 1;
+        const bool ready = block ? mbar_wait(&ub_empty[u & 1], ph, status, 44, s_abort, p.spin)
+                                 : mbar_test_wait(&ub_empty[u & 1], ph);
+        if (!__all_sync(0xffffffffu, ready)) return block ? -1 : 0;
+      }
+      const Item t = item_of(p, blockIdx.x + u * G, BK);
+      if (r < D) {
+        const float qv = p.qbar[((size_t)t.bh * p.Tm + t.qi) * D + r];
+        const __half hi = __float2half_rz(qv);
+        const __half lo = __float2half_rn(qv - __half2float(hi));
+        uint8_t *ub = sU + (u & 1) * C::UB_BYTES;
+        const int byte = 2 * r, cc = byte / C::QK_SW, bb = byte % C::QK_SW;
+        *reinterpret_cast<__half *>(ub + cc * 16 * C::QK_SW + swz_off<C::QK_SW>(0, bb / 16) + (bb & 15)) = hi;
+        *reinterpret_cast<__half *>(ub + cc * 16 * C::QK_SW + swz_off<C::QK_SW>(1, bb / 16) + (bb & 15)) = lo;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ub_full[u & 1]);
+      return 1;
+    };
+    if constexpr (kDsMma) {
+      // zero both q_bar tiles once (rows 0 and 1 are rewritten per item)
+      for (int i = r; i < 2 * C::UB_BYTES / 16; i += kWG) reinterpret_cast<uint4 *>(sU)[i] = make_uint4(0, 0, 0, 0);
+      named_bar_sync(3, kWG);
+    }
     if (d_more) ds_item(blockIdx.x);
     const float c2 = p.sm_log2;
     for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
@@ -447,7 +527,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lsum = 0.0f;
       for (int j = 0; j < it.T; ++j, ++gt) {
         const int b = gt % NB;
-        while (d_more && dg < gt + 3) {
+        while (kDsMma && d_more && dg < gt + 3) {
+          // dS_j[c] = delta_K,j (K^_j q_bar^T)[c], in t units, from the tensor core: thread r takes key r
+          bool prep_ok = true;
+          while (un <= dn && prep_ok) prep_ok = prep_ub(un++, true) > 0;
+          if (!prep_ok) {
+            ok = false;
+            break;
+          }
+          if (un == dn + 1 && blockIdx.x + un * G < p.items && prep_ub(un, false) > 0) ++un;
+          const int b2 = dg % NB;
+          const uint32_t ph = (dg / NB) & 1;
+          if (dg == gt + 2) {
+            if (!__all_sync(0xffffffffu, mbar_test_wait(&dsr_full[b2], ph))) break;  // not yet: later
+          } else if (!__all_sync(0xffffffffu, mbar_wait(&dsr_full[b2], ph, status, 42, s_abort, p.spin))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t dh, dl;
+          tmem_ld2(tmem + lane_off + C::DS_COL + b2 * 16, dh, dl);
+          tmem_wait_ld();
+          s_ds[b2 * BK + r] = (__uint_as_float(dh) + __uint_as_float(dl)) * d_dk[dj] * c2;
+          tc_fence_before();
+          mbar_arrive(&dsr_free[b2]);
+          mbar_arrive(&ds_full[b2]);
+          ++dg;
+          if (++dj == dT) {
+            dj = 0;
+            const int nx = blockIdx.x + (++dn) * G;
+            d_more = nx < p.items;
+            if (d_more) ds_item(nx);
+          }
+        }
+        while (!kDsMma && d_more && dg < gt + 3) {
           // dS_j[c] = delta_K,j sum_d q_bar[d] K^_j[c, d], in t units: thread r takes key r
           const int s = dg % KST;
           const uint32_t ph = (dg / KST) & 1;
@@ -706,12 +819,15 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
-  auto kern = (flags & SAGE_SMOOTH_Q) ? attn_q8_kernel<D, BK, kQK16, true> : attn_q8_kernel<D, BK, kQK16, false>;
+  const bool sq = (flags & SAGE_SMOOTH_Q) != 0;
+  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true> : attn_q8_kernel<D, BK, kQK16, false>;
+  // the Q-smoothing instance with INT8 codes and 128-key tiles holds the q_bar tiles too
+  const int smem = sq ? Cfg<D, BK, kQK16, kQK16 && BK == 128>::SMEM_TOTAL : C::SMEM_TOTAL;
   // the register split needs the launch allocation it was computed for
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
   if (fa.numRegs != kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SAGE_ERR_CUDA;
   // one persistent CTA per SM (fewer when there are fewer items)
   static int sms = 0;
@@ -722,7 +838,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
       return SAGE_ERR_CUDA;
   }
   const int grid = p.items < sms ? p.items : sms;
-  kern<<<(unsigned)grid, kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  kern<<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
