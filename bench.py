@@ -391,12 +391,19 @@ def run_gpu(args, cfg):
 
 
 def kernel_hash() -> str:
+    """Hash of the CUDA/C++ sources' code: comments dropped and whitespace runs
+    collapsed, so an edit to the documentation does not void a measurement
+    while any change to the code does."""
     import hashlib
+    import re
     h = hashlib.sha1()
     for f in sorted(os.listdir(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc"))):
         if not f.endswith((".cu", ".cuh", ".h")):
             continue
-        h.update(open(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc", f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(f.encode() + b"\0" + " ".join(text.split()).encode() + b"\0")
     return h.hexdigest()[:12]
 
 

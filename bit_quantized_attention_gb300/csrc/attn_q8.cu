@@ -32,15 +32,19 @@
 //               before its exponentials.
 //   warps 8-11  two-level accumulation O = alpha O + R with the thread's row
 //               of O in registers, then the epilogue; with Q smoothing also
-//               dS of the tile two ahead (one key per thread, from the K^ tile
-//               in shared memory), off the softmax's per-tile chain
+//               dS one or two tiles ahead, off the softmax's per-tile chain:
+//               read from TMEM (one key per thread) where the tensor core
+//               computed it, else from the K^ tile in shared memory
 //   warp 12     TMA producer: Q^ once, K^_j and V^T_j into a ring of stages
 //   warp 13     QK issuer: S(j) = Q^ K^_j^T (kind::f16 on INT8 codes held as
 //               exact fp16 integers -- sm_103a has no INT8 tensor path -- or
-//               kind::f8f6f4 on E4M3 codes)
+//               kind::f8f6f4 on E4M3 codes); with Q smoothing on INT8 codes
+//               and 128-key tiles also dS^T(j) = K^_j U^T, U the item's q_bar
+//               as fp16 hi / lo rows (kind::f16, M = 128 keys, N = 16)
 //   warp 14     PV issuer: R(j) = P^(j) V^_j (kind::f8f6f4)
 // TMEM: three S/R regions (R of tile j overwrites S of tile j once the softmax
-// has read it), so QK runs up to three tiles ahead of the accumulation.
+// has read it), so QK runs up to three tiles ahead of the accumulation; with
+// the tensor-core dS, three 16-column dS regions after them.
 // Waits are bounded: on timeout the kernel records SAGE_ERR_TIMEOUT and the
 // site, drains its own TMA loads and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
