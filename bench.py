@@ -153,6 +153,23 @@ class ClockSampler:
                 "power_w_max": max(r["power"] for r in use), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank
+    sets the job's time); the values themselves with one rank."""
+    values = [float(v) for v in values]
+    if dist is None:
+        return values
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_tops(ops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return ops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -320,12 +337,9 @@ def run_gpu(args, cfg):
     total_ms = t_start.elapsed_time(t_end)
     attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     code = sage.sage_read_status(ws)
-    if pg is not None:
-        t = torch.tensor([total_ms, attn_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms, attn_ms = float(t[0]), float(t[1])
+    total_ms, attn_ms = max_over_ranks([total_ms, attn_ms], pg, dev)
     ms_per_step = total_ms / args.steps
-    value = cfg.ops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tops(cfg.ops, world, ms_per_step)
 
     # ---- e2e through the C ABI on host buffers (pinned), copies inside the timed region
     q_pin, k_pin, v_pin = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
@@ -347,11 +361,8 @@ def run_gpu(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t[0])
-    e2e_val = cfg.ops * world / (e2e_ms * 1e-3) / 1e12
+    (e2e_ms,) = max_over_ranks([e2e_ms], pg, dev)
+    e2e_val = job_tops(cfg.ops, world, e2e_ms)
     h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
     d2h = qh.numel() * 2
 
