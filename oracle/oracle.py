@@ -19,6 +19,7 @@ LIB = os.path.join(HERE, "liborc.so")
 
 MODE_Q8_PV8, MODE_QF8_PV8, MODE_NVFP4 = 0, 1, 2
 SMOOTH_K, SMOOTH_Q, SMOOTH_V = 1, 2, 4
+P_DIRECT = 8  # NVFP4 ablation: phi on P~ directly (no level-1 scale)
 EXACT_QK, EXACT_PV = 0x100, 0x200
 
 _lock = threading.Lock()

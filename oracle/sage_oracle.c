@@ -505,9 +505,10 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
       } else {
         /* two-level P~ (SageAttention3 summary §3.4): s_P1 = rowmax(P~)/(448*6)
          * with rowmax(P~_ij) = exp(rowmax S_ij - m_ij); P2 = P~ / s_P1;
-         * s_P2, P2^ = phi(P2) over 1x16 blocks; R = (P2^ s_P2)(V^ s_V). */
+         * s_P2, P2^ = phi(P2) over 1x16 blocks; R = (P2^ s_P2)(V^ s_V).
+         * ORC_P_DIRECT: s_P1 = 1, phi on P~ itself. */
         int u;
-        sP1 = (mt == -INFINITY) ? 0.0 : exp(mt - m_new) / (448.0 * 6.0);
+        sP1 = (mt == -INFINITY) ? 0.0 : (flags & ORC_P_DIRECT) ? 1.0 : exp(mt - m_new) / (448.0 * 6.0);
         for (u = 0; u < bk; u += 16) {
           double p2[16], amax = 0.0, s2;
           uint8_t s2c;

@@ -48,6 +48,10 @@ extern "C" {
 #define ORC_SMOOTH_K 1
 #define ORC_SMOOTH_Q 2
 #define ORC_SMOOTH_V 4
+/* ablation of the NVFP4 mode (SageAttention3 summary §3.4, two-level P): phi
+ * applied to P~ itself, no level-1 scale (s_P1 = 1); no effect in the FP8 modes,
+ * whose P~ quantization is already direct */
+#define ORC_P_DIRECT 8
 /* oracle-only switches used by the pins: replace a quantizer by identity */
 #define ORC_EXACT_QK 0x100 /* S from the unrounded smoothed Q, K in fp64 */
 #define ORC_EXACT_PV 0x200 /* R from unquantized P~ and unquantized V' in fp64 */

@@ -182,6 +182,83 @@ def test_constant_scores_exact_p_path(orc, mode, causal):
     assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- direct P~ (NVFP4 ablation)
+@pytest.mark.parametrize("causal", [False, True])
+def test_direct_p_constant_scores_closed_form(orc, causal):
+    """Constant scores make P~ = 1 for every visible key.  Quantized directly,
+    each 16-key block gets s = e4m3(1/6) and code e2m1(1/s), so every P~ becomes
+    e2m1(1/s) * s (6 * 0.171875 = 1.03125), while l sums the unquantized 1s: the
+    output is that factor times the mean of the visible V rows (V exactly
+    representable), where the two-level path returns the mean itself."""
+    rng = np.random.default_rng(71)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 2, 48, 96, 32, 16, 32
+    qf = rng.standard_normal((B, Hq, N, d))
+    kf = np.broadcast_to(rng.standard_normal((B, Hkv, 1, d)), (B, Hkv, M, d)).copy()
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    vf = rng.choice(mags, size=(B, Hkv, M, d)) * rng.choice([-1, 1], size=(B, Hkv, M, d))
+    vf = vf.reshape(B, Hkv, M // 16, 16, d)
+    vf[:, :, :, 2, :] = 6.0
+    vf = (vf * (2.0 ** rng.integers(-4, 2, size=(B, Hkv, M // 16, 1, d)))).reshape(B, Hkv, M, d)
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    s1 = orc.e4m3_decode(orc.e4m3_encode(np.array([1.0 / 6.0])))[0]
+    factor = orc.e2m1_decode(orc.e2m1_encode(np.array([1.0 / s1])))[0] * s1
+    assert factor == 1.03125
+    shape = (B, Hq, Hkv, N, M, d)
+    got, _ = run_oracle(orc, shape, 2, orc.SMOOTH_K | orc.P_DIRECT, bq, bk, causal, 0.1, q, k, v)
+    two, _ = run_oracle(orc, shape, 2, orc.SMOOTH_K, bq, bk, causal, 0.1, q, k, v)
+    ref = textbook(qf, kf, vf, causal, 0.1)
+    assert np.allclose(two, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(got, factor * ref, rtol=1e-12, atol=1e-12)
+
+
+def test_direct_p_no_effect_in_fp8_modes(orc):
+    """The FP8 modes quantize P~ directly already (static 1/448): the switch
+    leaves them unchanged."""
+    B, Hq, Hkv, N, M, d = 1, 2, 1, 64, 96, 64
+    q, k, v = rand_qkv(B, Hq, Hkv, N, M, d, seed=5, koff=3.0)
+    for mode in (0, 1):
+        a, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, orc.SMOOTH_K, 128, 64, True, 0.125, q, k, v)
+        b, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), mode, orc.SMOOTH_K | orc.P_DIRECT, 128, 64, True, 0.125,
+                          q, k, v)
+        assert np.array_equal(a, b)
+
+
+def test_direct_p_small_block_scale_underflows(orc):
+    """Why the pages scale P~ in two levels (SageAttention3 summary §3.4): P~
+    lies in [0, 1], so a 16-key block whose largest P~ is small gets a direct
+    E4M3 scale max/6 below E4M3's smallest subnormal (2^-9) and rounds to zero:
+    the block vanishes from the numerator while l, which sums the unquantized
+    P~, still counts it.  One query against two key blocks (exact Q/K):
+    block A at S = 0 (P~ = 1, quantized to 6 * e4m3(1/6) = 1.03125 each) and
+    block B at S = -6.9375 (P~ = e^-6.9375, about 9.7e-4, scale about 1.6e-4).
+    Directly quantized, the output is 1.03125 * sum_A V / (16 + 16 e^-6.9375)
+    with V exactly representable; the two-level form keeps block B."""
+    B, Hq, Hkv, N, M, d = 1, 1, 1, 1, 32, 16
+    qf = np.zeros((B, Hq, N, d))
+    qf[..., 0] = 1.0
+    kf = np.zeros((B, Hkv, M, d))
+    kf[0, 0, 16:, 0] = -55.5                          # S = -55.5 / 8 on block B
+    rng = np.random.default_rng(5)
+    mags = np.array([0.5, 1, 1.5, 2, 3, 4, 6])
+    vf = rng.choice(mags, size=(B, Hkv, M, d)) * rng.choice([-1, 1], size=(B, Hkv, M, d))
+    vf[0, 0, 3, :] = 6.0                              # each 16-token block's max is 6 (V exact in NVFP4)
+    vf[0, 0, 19, :] = 6.0
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(k), kf) and np.array_equal(f64(v), vf)
+    sB = -55.5 / 8.0
+    small = np.array([np.exp(sB) / 6.0])
+    assert orc.e4m3_decode(orc.e4m3_encode(small))[0] == 0.0 and small[0] < 2.0 ** -9
+    shape = (B, Hq, Hkv, N, M, d)
+    direct, _ = run_oracle(orc, shape, 2, orc.EXACT_QK | orc.P_DIRECT, 128, 32, False, 1.0 / 8.0, q, k, v)
+    two, _ = run_oracle(orc, shape, 2, orc.EXACT_QK, 128, 32, False, 1.0 / 8.0, q, k, v)
+    l = 16.0 + 16.0 * np.exp(sB)
+    want = 1.03125 * vf[0, 0, :16].sum(axis=0) / l
+    assert np.allclose(direct.reshape(-1), want, rtol=1e-12, atol=1e-12)
+    exact = textbook(qf, kf, vf, False, 1.0 / 8.0).reshape(-1)
+    # the two-level form keeps block B: it lands much closer to exact attention
+    assert np.abs(two.reshape(-1) - exact).max() < 0.2 * np.abs(direct.reshape(-1) - exact).max()
+
+
 # ---------------------------------------------------------------- accuracy sanity
 # INT8 Q/K (the mode of the INT8/FP8 workloads) reaches 0.999.  The extra E4M3
 # Q/K mode carries 3 mantissa bits per operand (about 0.9987 here).  NVFP4 on
