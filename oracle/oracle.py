@@ -20,6 +20,7 @@ LIB = os.path.join(HERE, "liborc.so")
 MODE_Q8_PV8, MODE_QF8_PV8, MODE_NVFP4 = 0, 1, 2
 SMOOTH_K, SMOOTH_Q, SMOOTH_V = 1, 2, 4
 P_DIRECT = 8  # NVFP4 ablation: phi on P~ directly (no level-1 scale)
+Q_PER_TOKEN = 0x10  # one Q scale per query row (INT8 / E4M3 modes)
 EXACT_QK, EXACT_PV = 0x100, 0x200
 
 _lock = threading.Lock()
@@ -51,7 +52,7 @@ class _Quant(C.Structure):
     _fields_ = [("qc", C.c_void_p), ("dq", C.c_void_p), ("qbar", C.c_void_p),
                 ("kc", C.c_void_p), ("dk", C.c_void_p), ("kbar", C.c_void_p),
                 ("vc", C.c_void_p), ("dv", C.c_void_p), ("vm", C.c_void_p),
-                ("qs", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p)]
+                ("qs", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p), ("dqt", C.c_void_p)]
 
 
 def lib():
@@ -174,6 +175,7 @@ class Quant:
     qs: np.ndarray
     ks: np.ndarray
     vs: np.ndarray
+    dqt: np.ndarray  # per-token Q scales (Q_PER_TOKEN)
 
     def _struct(self):
         return _Quant(*[_p(getattr(self, f)) for f, _ in _Quant._fields_])
@@ -206,7 +208,7 @@ def quantize(shape, mode, flags, bq, bk, q, k, v) -> Quant:
         vc=np.zeros((B, Hkv, M, d), np.uint8), dv=np.zeros((B, Hkv, d), np.float32),
         vm=np.zeros((B, Hkv, d), np.float32),
         qs=np.zeros((B, Hq, N, G), np.uint8), ks=np.zeros((B, Hkv, M, G), np.uint8),
-        vs=np.zeros((B, Hkv, Mt16, d), np.uint8))
+        vs=np.zeros((B, Hkv, Mt16, d), np.uint8), dqt=np.zeros((B, Hq, N), np.float32))
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     assert qb.size == B * Hq * N * d and kb.size == B * Hkv * M * d and vb.size == kb.size
     st = qz._struct()

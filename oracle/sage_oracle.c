@@ -342,6 +342,21 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
                     orc_nvfp4_code(g[(int64_t)(r - r0) * d + gi * 16 + e], sc);
             }
           }
+        } else if (flags & ORC_Q_PER_TOKEN) {
+          /* one scale per row of gamma(Q_i) */
+          out->dq[hb * Tm + ib] = 0.0f;
+          for (r = r0; r < r1; ++r) {
+            float amax = 0.0f, sc;
+            for (c = 0; c < d; ++c)
+              if (fabsf(g[(int64_t)(r - r0) * d + c]) > amax) amax = fabsf(g[(int64_t)(r - r0) * d + c]);
+            sc = (mode == ORC_Q8_PV8) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
+            out->dqt[hb * N + r] = sc;
+            for (c = 0; c < d; ++c) {
+              float x = g[(int64_t)(r - r0) * d + c];
+              out->qc[(hb * N + r) * d + c] = (mode == ORC_Q8_PV8) ? (uint8_t)(int8_t)orc_int8_code(x, sc)
+                                                                   : orc_fp8_code(x, sc);
+            }
+          }
         } else {
           float amax = 0.0f, sc;
           for (r = r0; r < r1; ++r)
@@ -381,15 +396,16 @@ static void deq_q_row(const orc_shape *s, int mode, int flags, int bq, const uin
   const int d = s->d, N = s->N;
   const int64_t Tm = cdiv(N, bq), ib = r / bq;
   const float *qbar = qz->qbar + (hb * Tm + ib) * d;
+  const double sq = (flags & ORC_Q_PER_TOKEN) ? (double)qz->dqt[hb * N + r] : (double)qz->dq[hb * Tm + ib];
   int c;
   for (c = 0; c < d; ++c) {
     const int64_t e = (hb * N + r) * d + c;
     if (flags & ORC_EXACT_QK)
       out[c] = orc_bf16_decode(q[e]) - (double)qbar[c];
     else if (mode == ORC_Q8_PV8)
-      out[c] = (double)qz->dq[hb * Tm + ib] * (double)(int8_t)qz->qc[e];
+      out[c] = sq * (double)(int8_t)qz->qc[e];
     else if (mode == ORC_QF8_PV8)
-      out[c] = (double)qz->dq[hb * Tm + ib] * orc_e4m3_decode(qz->qc[e]);
+      out[c] = sq * orc_e4m3_decode(qz->qc[e]);
     else
       out[c] = orc_e4m3_decode(qz->qs[(hb * N + r) * (d / 16) + c / 16]) * orc_e2m1_decode(qz->qc[e]);
   }

@@ -52,6 +52,10 @@ extern "C" {
  * applied to P~ itself, no level-1 scale (s_P1 = 1); no effect in the FP8 modes,
  * whose P~ quantization is already direct */
 #define ORC_P_DIRECT 8
+/* one Q scale per query row (modes 0, 1) instead of one per bq-row block: the
+ * per-token granularity the SageAttention summaries ablate (each row of S has
+ * its own dequantization scale); q_bar stays per block */
+#define ORC_Q_PER_TOKEN 0x10
 /* oracle-only switches used by the pins: replace a quantizer by identity */
 #define ORC_EXACT_QK 0x100 /* S from the unrounded smoothed Q, K in fp64 */
 #define ORC_EXACT_PV 0x200 /* R from unquantized P~ and unquantized V' in fp64 */
@@ -78,6 +82,7 @@ typedef struct {
  *   qs  [B,Hq,N,d/16]          E4M3 block scales (mode 2)
  *   ks  [B,Hkv,M,d/16]         E4M3 block scales (mode 2)
  *   vs  [B,Hkv,ceil(M/16),d]   E4M3 block scales along tokens (mode 2)
+ *   dqt [B,Hq,N]     per-token Q scale (modes 0, 1 with ORC_Q_PER_TOKEN; dq unused then)
  * Tm = ceil(N/bq), Tn = ceil(M/bk).  Pointers a mode does not use may be NULL. */
 typedef struct {
   uint8_t *qc;
@@ -87,6 +92,7 @@ typedef struct {
   uint8_t *vc;
   float *dv, *vm;
   uint8_t *qs, *ks, *vs;
+  float *dqt;
 } orc_quant;
 
 /* ---- codecs (round to nearest, ties to even; saturate to the largest

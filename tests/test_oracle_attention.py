@@ -152,6 +152,64 @@ def test_exact_qk_codes_reproduce_textbook(orc, mode, causal):
     assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
 
 
+# ---------------------------------------------------------------- per-token Q scales
+def _rows_exact(rng, shape, mode, orc):
+    """each row: codes times its own power of two, the row's absmax at 127 (INT8)
+    or 448 (E4M3) times it, so fl(absmax / 127 or 448) is the power itself"""
+    B, H, L, d = shape
+    if mode == 0:
+        c = rng.integers(-127, 128, size=shape).astype(np.float64)
+        c[..., 0] = 127 * rng.choice([-1, 1], size=(B, H, L))
+    else:
+        mags = orc.e4m3_decode(np.arange(127))
+        c = rng.choice(mags, size=shape) * rng.choice([-1, 1], size=shape)
+        c[..., 0] = 448.0
+    e = rng.integers(-12, -2, size=(B, H, L, 1))
+    return c, 2.0 ** e
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_per_token_q_scales_are_the_row_scales(orc, mode):
+    """With Q_PER_TOKEN each row gets fl(absmax/127) (INT8) or fl(absmax/448)
+    (E4M3) of its own and codes with it: rows built as codes times a power of two
+    come back exactly.  Per block, the rows with the smaller powers share the
+    block's largest scale and lose bits: their codes differ."""
+    rng = np.random.default_rng(41 + mode)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 1, 40, 32, 32, 16, 16
+    c, s = _rows_exact(rng, (B, Hq, N, d), mode, orc)
+    q = bf16_tensor(c * s)
+    k = bf16_tensor(rng.standard_normal((B, Hkv, M, d)))
+    v = bf16_tensor(rng.standard_normal((B, Hkv, M, d)))
+    assert np.array_equal(f64(q), c * s)
+    shape = (B, Hq, Hkv, N, M, d)
+    tok = orc.quantize(shape, mode, orc.Q_PER_TOKEN, bq, bk, q, k, v)
+    assert np.array_equal(tok.dqt.astype(np.float64), s[..., 0])
+    codes = tok.qc.view(np.int8).astype(np.float64) if mode == 0 else orc.e4m3_decode(tok.qc)
+    assert np.array_equal(codes, c)
+    blk = orc.quantize(shape, mode, 0, bq, bk, q, k, v)
+    bcodes = blk.qc.view(np.int8).astype(np.float64) if mode == 0 else orc.e4m3_decode(blk.qc)
+    assert not np.array_equal(bcodes, c)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_per_token_q_exact_codes_reproduce_textbook(orc, causal):
+    """Per-token Q codes that are exact, exact K codes per block and unquantized
+    P~V: the oracle's attention is textbook attention on the bf16 inputs (each
+    row of S dequantized with its own Q scale)."""
+    rng = np.random.default_rng(61)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 1, 40, 80, 32, 16, 16
+    c, s = _rows_exact(rng, (B, Hq, N, d), 0, orc)
+    qf = c * s
+    kf = _int8_exact(rng, (B, Hkv, M, d), bk)
+    vf = rng.standard_normal((B, Hkv, M, d))
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    got, qz = run_oracle(orc, (B, Hq, Hkv, N, M, d), 0, orc.Q_PER_TOKEN | orc.EXACT_PV, bq, bk, causal, 0.02,
+                         q, k, v)
+    assert np.array_equal(qz.dqt.astype(np.float64), s[..., 0])
+    ref = textbook(qf, kf, f64(v), causal, 0.02)
+    assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
 # ---------------------------------------------------------------- exact P~ path
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("causal", [False, True])
