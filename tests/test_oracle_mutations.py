@@ -1,0 +1,74 @@
+"""The oracle's pins catch plausible mistakes in it.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped or
+flipped term, a wrong index, a wrong constant, the other tie rule), builds the
+copy, and runs the oracle's own tests against it in a subprocess: at least one
+of them must fail.  The unmutated copy must pass.  Only the copy is touched."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TESTS = [os.path.join(ROOT, "tests", "test_oracle_codecs.py"), os.path.join(ROOT, "tests", "test_oracle_attention.py")]
+
+# (name, text in sage_oracle.c, replacement); each text occurs exactly once
+MUTATIONS = [
+    ("dS dropped", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = (s0) * sm_scale;"),
+    ("dS sign", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = (s0 - ds) * sm_scale;"),
+    ("GQA map", "const int64_t hk = (int64_t)b * Hkv + h / (Hq / Hkv); /* kv head of this query head */",
+     "const int64_t hk = (int64_t)b * Hkv + h % Hkv; /* kv head of this query head */"),
+    ("causal offset", "return c <= r + (M - N);", "return c <= r;"),
+    ("l not rescaled", "l = alpha * l + rs;", "l = l + rs;"),
+    ("INT8 divisor", "float orc_int8_scale(float absmax) { return absmax / 127.0f; }",
+     "float orc_int8_scale(float absmax) { return absmax / 128.0f; }"),
+    ("INT8 clamp", "if (r > 127.0f) r = 127.0f;", "if (r > 126.0f) r = 126.0f;"),
+    ("P~ scale 448", "orc_e4m3_encode(pv[c] * 448.0)", "orc_e4m3_encode(pv[c] * 256.0)"),
+    ("output 448", "o = o / 448.0 * (double)qz->dv[hk * d + e];", "o = o / 256.0 * (double)qz->dv[hk * d + e];"),
+    ("delta_V dropped", "o = o / 448.0 * (double)qz->dv[hk * d + e];", "o = o / 448.0;"),
+    ("V_m dropped", "vrow[e] = o + (double)qz->vm[hk * d + e];", "vrow[e] = o;"),
+    ("s_P1 constant", "exp(mt - m_new) / (448.0 * 6.0)", "exp(mt - m_new) / (448.0 * 4.0)"),
+    ("s_P2 divisor", "s2c = orc_e4m3_encode(amax / 6.0);", "s2c = orc_e4m3_encode(amax / 4.0);"),
+    ("ties away from zero", "r = nearbyint(ldexp(a, -ulp_exp));", "r = round(ldexp(a, -ulp_exp));"),
+    ("mean divisor", "*mean = (n > 0) ? (float)(((double)acc * 0x1p-24) / (double)n) : 0.0f;",
+     "*mean = (n > 0) ? (float)(((double)acc * 0x1p-24) / (double)(n + 1)) : 0.0f;"),
+]
+
+
+def _copy_oracle(dst, mutation=None):
+    pkg = os.path.join(dst, "oracle")
+    os.makedirs(pkg)
+    for f in ("__init__.py", "oracle.py", "sage_oracle.c", "sage_oracle.h"):
+        shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(pkg, f))
+    if mutation is not None:
+        src = os.path.join(pkg, "sage_oracle.c")
+        text = open(src).read()
+        old, new = mutation
+        assert text.count(old) == 1, old
+        open(src, "w").write(text.replace(old, new))
+    # build the copy here, so that the subprocess only loads it
+    out = subprocess.run([sys.executable, "-c", "import oracle; oracle.build(force=True)"], cwd=dst,
+                         capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr[-2000:]
+
+
+def _run_pins(dst):
+    env = dict(os.environ, PYTHONPATH=dst + os.pathsep + ROOT)
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *TESTS],
+                          cwd=dst, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_unmutated_copy_passes(tmp_path):
+    _copy_oracle(str(tmp_path))
+    r = _run_pins(str(tmp_path))
+    assert r.returncode == 0, r.stdout[-3000:]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(tmp_path, name, old, new):
+    _copy_oracle(str(tmp_path), (old, new))
+    r = _run_pins(str(tmp_path))
+    # 1: some test failed (not an import, collection or usage error)
+    assert r.returncode == 1 and " failed" in r.stdout, (name, r.returncode, r.stdout[-3000:])
