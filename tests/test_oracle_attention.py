@@ -152,6 +152,37 @@ def test_exact_qk_codes_reproduce_textbook(orc, mode, causal):
     assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
 
 
+# ---------------------------------------------------------------- Q smoothing through the codes
+@pytest.mark.parametrize("causal", [False, True])
+def test_q_smoothing_exact_codes_reproduce_textbook(orc, causal):
+    """Q rows = a per-block base (the block's exact mean) plus +-pairs of INT8
+    codes times 2^-4: q_bar is the base exactly, gamma(Q) quantizes exactly
+    (delta_Q = 2^-4), and with exact K codes and unquantized P~V the smoothed
+    path S = (deq gamma(Q) + q_bar) deq(K)^T is textbook attention on the bf16
+    inputs (SageAttention2 summary §3.4, smoothing Q with the dS correction)."""
+    rng = np.random.default_rng(81)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 1, 32, 48, 32, 16, 16
+    c = np.zeros((B, Hq, N, d))
+    for t0 in range(0, N, bq):                         # every block: rows r and r + bq/2 cancel
+        half = rng.integers(-126, 127, size=(B, Hq, bq // 2, d)).astype(np.float64)
+        half[:, :, 0, 0] = 127.0                       # the block's absmax: delta_Q = 2^-4
+        c[:, :, t0:t0 + bq // 2] = half
+        c[:, :, t0 + bq // 2:t0 + bq] = -half
+    base = rng.integers(-64, 65, size=(B, Hq, N // bq, 1, d)).astype(np.float64)
+    base = np.broadcast_to(base, (B, Hq, N // bq, bq, d)).reshape(B, Hq, N, d)
+    qf = (base + c) * 2.0 ** -4
+    kf = _int8_exact(rng, (B, Hkv, M, d), bk)
+    vf = rng.standard_normal((B, Hkv, M, d))
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(q), qf) and np.array_equal(f64(k), kf)
+    got, qz = run_oracle(orc, (B, Hq, Hkv, N, M, d), 0, orc.SMOOTH_Q | orc.EXACT_PV, bq, bk, causal, 0.02,
+                         q, k, v)
+    assert np.array_equal(qz.qbar.astype(np.float64), (base * 2.0 ** -4)[:, :, ::bq, :])
+    assert np.array_equal(qz.qc.view(np.int8).astype(np.float64), c)
+    ref = textbook(qf, kf, f64(v), causal, 0.02)
+    assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
 # ---------------------------------------------------------------- per-token Q scales
 def _rows_exact(rng, shape, mode, orc):
     """each row: codes times its own power of two, the row's absmax at 127 (INT8)

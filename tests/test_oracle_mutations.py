@@ -34,6 +34,18 @@ MUTATIONS = [
     ("ties away from zero", "r = nearbyint(ldexp(a, -ulp_exp));", "r = round(ldexp(a, -ulp_exp));"),
     ("mean divisor", "*mean = (n > 0) ? (float)(((double)acc * 0x1p-24) / (double)n) : 0.0f;",
      "*mean = (n > 0) ? (float)(((double)acc * 0x1p-24) / (double)(n + 1)) : 0.0f;"),
+    ("K mean not subtracted (INT8/FP8)", "float x = bf16f(K[(int64_t)t * d + c]) - kbar[c];",
+     "float x = bf16f(K[(int64_t)t * d + c]);"),
+    ("Q mean not subtracted", "g[(int64_t)(r - r0) * d + c] = bf16f(Q[(int64_t)r * d + c]) - qbar[c];",
+     "g[(int64_t)(r - r0) * d + c] = bf16f(Q[(int64_t)r * d + c]);"),
+    ("NVFP4 scale divisor", "return orc_e4m3_encode((double)(absmax / 6.0f));",
+     "return orc_e4m3_encode((double)(absmax / 4.0f));"),
+    ("per-token Q dequantized per block",
+     "const double sq = (flags & ORC_Q_PER_TOKEN) ? (double)qz->dqt[hb * N + r] : (double)qz->dq[hb * Tm + ib];",
+     "const double sq = (double)qz->dq[hb * Tm + ib];"),
+    # (a power-of-two level-1 scale commutes with the E4M3 / E2M1 roundings away from
+    # the subnormal range, so the planted constant is not one)
+    ("direct P~ keeps a level-1 scale", "(flags & ORC_P_DIRECT) ? 1.0 :", "(flags & ORC_P_DIRECT) ? (1.0 / 3.0) :"),
 ]
 
 
