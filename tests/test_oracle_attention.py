@@ -152,6 +152,36 @@ def test_exact_qk_codes_reproduce_textbook(orc, mode, causal):
     assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
 
 
+# ---------------------------------------------------------------- running max as the P~ reference
+def test_p_quantized_against_the_running_max(orc):
+    """m_ij = max(m_i,j-1, rowmax S_ij) and P~_ij = exp(S_ij - m_ij)
+    (SageAttention2 summary §3.4): a tile whose own maximum lies below the
+    running one quantizes P~ relative to the running maximum.  One query; tile 0
+    holds the row maximum (S = 8 at key 0, S = -64 elsewhere), tile 1 sits at
+    S = 4.875: its P~ = e^-3.125 becomes e4m3(448 e^-3.125) / 448 = 20 / 448.
+    Exact S, V exactly representable in FP8 per channel, l over unquantized P~."""
+    B, Hq, Hkv, N, M, d, bk = 1, 1, 1, 1, 32, 16, 16
+    qf = np.zeros((B, Hq, N, d))
+    qf[..., 0] = 1.0
+    kf = np.zeros((B, Hkv, M, d))
+    kf[0, 0, 0, 0] = 8.0
+    kf[0, 0, 1:16, 0] = -64.0
+    kf[0, 0, 16:, 0] = 4.875
+    rng = np.random.default_rng(9)
+    mags = orc.e4m3_decode(np.arange(127))
+    vf = rng.choice(mags, size=(B, Hkv, M, d)) * rng.choice([-1, 1], size=(B, Hkv, M, d))
+    vf[0, 0, 7, :] = 448.0                           # per-channel absmax 448: delta_V = 1, V^ = V
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(k), kf) and np.array_equal(f64(v), vf)
+    got, _ = run_oracle(orc, (B, Hq, Hkv, N, M, d), 0, orc.EXACT_QK, 128, bk, False, 1.0, q, k, v)
+    p1 = np.exp(4.875 - 8.0)
+    ph1 = orc.e4m3_decode(orc.e4m3_encode(np.array([448.0 * p1])))[0] / 448.0
+    assert ph1 == 20.0 / 448.0
+    l = 1.0 + 16.0 * p1
+    want = (vf[0, 0, 0] + ph1 * vf[0, 0, 16:].sum(axis=0)) / l
+    assert np.allclose(got.reshape(-1), want, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- Q smoothing through the codes
 @pytest.mark.parametrize("causal", [False, True])
 def test_q_smoothing_exact_codes_reproduce_textbook(orc, causal):

@@ -45,6 +45,10 @@ MUTATIONS = [
      "const double sq = (double)qz->dq[hb * Tm + ib];"),
     # (a power-of-two level-1 scale commutes with the E4M3 / E2M1 roundings away from
     # the subnormal range, so the planted constant is not one)
+    ("running max forgets the previous tiles", "m_new = (mt > m) ? mt : m;", "m_new = mt;"),
+    ("alpha sign", "alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);",
+     "alpha = (m == -INFINITY) ? 0.0 : exp(m_new - m);"),
+    ("sm_scale before dS", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = s0 * sm_scale + ds;"),
     ("direct P~ keeps a level-1 scale", "(flags & ORC_P_DIRECT) ? 1.0 :", "(flags & ORC_P_DIRECT) ? (1.0 / 3.0) :"),
 ]
 
