@@ -76,15 +76,22 @@ def _run_pins(dst):
                           cwd=dst, env=env, capture_output=True, text=True, timeout=600)
 
 
-def test_unmutated_copy_passes(tmp_path):
-    _copy_oracle(str(tmp_path))
-    r = _run_pins(str(tmp_path))
-    assert r.returncode == 0, r.stdout[-3000:]
+def _check(tmp, name, mutation):
+    d = os.path.join(tmp, "m%02d" % name)
+    os.makedirs(d)
+    _copy_oracle(d, mutation)
+    r = _run_pins(d)
+    return r
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_fails_a_pin(tmp_path, name, old, new):
-    _copy_oracle(str(tmp_path), (old, new))
-    r = _run_pins(str(tmp_path))
+def test_unmutated_copy_passes_and_every_planted_mistake_fails_a_pin(tmp_path):
+    """All copies built and run in parallel (one subprocess each)."""
+    from concurrent.futures import ThreadPoolExecutor
+    jobs = [None] + [(old, new) for _, old, new in MUTATIONS]
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
+        results = list(ex.map(lambda a: _check(str(tmp_path), a[0], a[1]), enumerate(jobs)))
+    clean = results[0]
+    assert clean.returncode == 0, clean.stdout[-3000:]
     # 1: some test failed (not an import, collection or usage error)
-    assert r.returncode == 1 and " failed" in r.stdout, (name, r.returncode, r.stdout[-3000:])
+    missed = [m[0] for m, r in zip(MUTATIONS, results[1:]) if not (r.returncode == 1 and " failed" in r.stdout)]
+    assert not missed, missed
