@@ -152,6 +152,37 @@ def test_exact_qk_codes_reproduce_textbook(orc, mode, causal):
     assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
 
 
+# ---------------------------------------------------------------- V smoothing through the codes
+@pytest.mark.parametrize("causal", [False, True])
+def test_v_smoothing_exact_codes_reproduce_textbook(orc, causal):
+    """V = (base + deviations) 2^e per channel, the deviations in cancelling
+    token pairs from {0, +-256, +-320, +-384, +-448} (exact in E4M3) and the base
+    a multiple of 64 (so every value is exact in bf16): V_m is the base exactly,
+    delta_V = 2^e, the codes of V' = V - V_m are the deviations.  With constant
+    scores (P~ = 1, P^ = 448 exactly) the output O / l * delta_V / 448 + V_m is
+    the mean of the visible V rows: textbook attention ("Optional Smoothing of
+    V", SageAttention2 summary §3.4)."""
+    rng = np.random.default_rng(91)
+    B, Hq, Hkv, N, M, d, bq, bk = 1, 2, 2, 48, 96, 32, 16, 32
+    qf = rng.standard_normal((B, Hq, N, d))
+    kf = np.broadcast_to(rng.standard_normal((B, Hkv, 1, d)), (B, Hkv, M, d)).copy()
+    half = rng.choice([0.0, 256.0, 320.0, 384.0, -256.0, -320.0, -384.0], size=(B, Hkv, M // 2, d))
+    half[:, :, 3, :] = 448.0
+    dev = np.concatenate([half, -half], axis=2)        # token t and t + M/2 cancel
+    base = rng.choice([-448.0, -320.0, -64.0, 0.0, 64.0, 192.0, 448.0], size=(B, Hkv, 1, d))
+    e = 2.0 ** rng.integers(-6, 0, size=(B, Hkv, 1, d))
+    vf = (base + dev) * e
+    q, k, v = bf16_tensor(qf), bf16_tensor(kf), bf16_tensor(vf)
+    assert np.array_equal(f64(v), vf)
+    got, qz = run_oracle(orc, (B, Hq, Hkv, N, M, d), 0, orc.SMOOTH_K | orc.SMOOTH_V, bq, bk, causal, 0.1,
+                         q, k, v)
+    assert np.array_equal(qz.vm.astype(np.float64), (base * e)[:, :, 0, :])
+    assert np.array_equal(qz.dv.astype(np.float64), e[:, :, 0, :])
+    assert np.array_equal(orc.e4m3_decode(qz.vc), dev)
+    ref = textbook(qf, kf, vf, causal, 0.1)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- running max as the P~ reference
 def test_p_quantized_against_the_running_max(orc):
     """m_ij = max(m_i,j-1, rowmax S_ij) and P~_ij = exp(S_ij - m_ij)

@@ -49,6 +49,20 @@ MUTATIONS = [
     ("alpha sign", "alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);",
      "alpha = (m == -INFINITY) ? 0.0 : exp(m_new - m);"),
     ("sm_scale before dS", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = s0 * sm_scale + ds;"),
+    ("V mean not subtracted before quantizing",
+     "g[(int64_t)t * d + c] = bf16f(V[(int64_t)t * d + c]) - vm[c];",
+     "g[(int64_t)t * d + c] = bf16f(V[(int64_t)t * d + c]);"),
+    ("delta_V doubled", "dv[c] = orc_fp8_scale(amax);", "dv[c] = orc_fp8_scale(amax * 2.0f);"),
+    ("pad keys visible", "if (c >= M) return 0;", "if (c > M) return 0;"),
+    ("INT8 rounds half away from zero", "r = rintf(t);", "r = roundf(t);"),
+    ("INT8 truncates", "r = rintf(t);", "r = truncf(t);"),
+    ("E4M3 code without the scale", "return orc_e4m3_encode((double)(x / scale));",
+     "return orc_e4m3_encode((double)(x));"),
+    ("NVFP4 V scale not stored", "out->vs[(hb * Mt16 + tb) * d + c] = sc;", "out->vs[(hb * Mt16 + tb) * d + c] = 0x38;"),
+    ("NVFP4 Q scale not stored", "out->qs[(hb * N + r) * G16 + gi] = sc;", "out->qs[(hb * N + r) * G16 + gi] = 0x38;"),
+    ("NVFP4 K code from the next element",
+     "out->kc[(hb * M + t) * d + gi * 16 + e] = orc_nvfp4_code(gg[e], sc);",
+     "out->kc[(hb * M + t) * d + gi * 16 + e] = orc_nvfp4_code(gg[(e + 1) & 15], sc);"),
     ("direct P~ keeps a level-1 scale", "(flags & ORC_P_DIRECT) ? 1.0 :", "(flags & ORC_P_DIRECT) ? (1.0 / 3.0) :"),
 ]
 
