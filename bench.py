@@ -390,7 +390,7 @@ def run_gpu(args, cfg):
         "clocks": clocks,
         "device_status": list(code),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the CPU baseline: rank 0 at N = 1 only
         smp, nrows = OracleSample.calibrated(cfg, args.ref_budget)
         tops, secs, _ = smp.run(nrows)
         out["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": smp.threads, "kind": "oracle",
