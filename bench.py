@@ -68,17 +68,23 @@ def peak_source(mode: int, src: str, bf16: float) -> str:
 
 
 ATTN_KERNEL = {0: "attn_q8_kernel", 1: "attn_q8_kernel", 2: "attn_fp4_kernel"}
+# the files each attention kernel is compiled from (its DRAM traffic depends on
+# nothing else in the library)
+ATTN_SOURCES = {0: ("attn_q8.cu", "sm103.cuh", "layout.h", "launch.h"),
+                1: ("attn_q8.cu", "sm103.cuh", "layout.h", "launch.h"),
+                2: ("attn_fp4.cu", "sm103.cuh", "layout.h", "launch.h")}
 
 
-def read_traffic(key: str):
+def read_traffic(key: str, mode: int = 0):
     """DRAM bytes per attention launch recorded from an ncu capture, or None when
-    the kernel sources changed since (lines: key kernel_hash bytes)."""
+    the kernel's sources changed since (lines: key kernel_hash bytes)."""
     path = os.path.join(ROOT, "profiles", "attn_traffic.txt")
     if not os.path.exists(path):
         return None
     for line in open(path):
         parts = line.split()
-        if len(parts) == 3 and not line.startswith("#") and parts[0] == key and parts[1] == kernel_hash():
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == key and \
+                parts[1] == kernel_hash(ATTN_SOURCES[mode]):
             return float(parts[2])
     return None
 
@@ -371,7 +377,7 @@ def run_gpu(args, cfg):
     # algorithmic work of one launch: 4 d flops per visible (query, key) pair
     algo_flops = 4.0 * cfg.d * cfg.B * cfg.Hq * cfg.visible_pairs
     achieved = algo_flops / (attn_ms * 1e-3) / 1e12
-    traffic = read_traffic(cfg.name + "_bk%d" % cfg.bk)
+    traffic = read_traffic(cfg.name + "_bk%d" % cfg.bk, cfg.mode)
     out = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -401,14 +407,15 @@ def run_gpu(args, cfg):
         pg.destroy_process_group()
 
 
-def kernel_hash() -> str:
-    """Hash of the CUDA/C++ sources' code: comments dropped and whitespace runs
-    collapsed, so an edit to the documentation does not void a measurement
-    while any change to the code does."""
+def kernel_hash(files=None) -> str:
+    """Hash of CUDA/C++ sources' code (the given csrc files, else all of them):
+    comments dropped and whitespace runs collapsed, so an edit to the
+    documentation does not void a measurement while any change to the code does."""
     import hashlib
     import re
     h = hashlib.sha1()
-    for f in sorted(os.listdir(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc"))):
+    csrc = os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc")
+    for f in sorted(files if files is not None else os.listdir(csrc)):
         if not f.endswith((".cu", ".cuh", ".h")):
             continue
         text = open(os.path.join(ROOT, "bit_quantized_attention_gb300", "csrc", f), encoding="utf-8").read()

@@ -87,6 +87,17 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
   return launch_quantize_q8(*shape, quant_mode, flags, bq, bk, q, k, v, workspace, L, (cudaStream_t)stream);
 }
 
+// The attention call's own conditions (beyond the layout's): flags, sm_scale,
+// the causal alignment, and the NVFP4 kernel's 128-key tiles.
+static sage_status check_attn_args(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags,
+                                   int bk) {
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
+  if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
+  if (quant_mode == SAGE_NVFP4 && bk != 128) return SAGE_ERR_UNSUPPORTED;
+  return SAGE_OK;
+}
+
 sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
                           int bk, const void *workspace, size_t workspace_bytes, void *o, sage_stream_t stream) {
   sage_ws_layout L;
@@ -95,8 +106,8 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
   if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
   if (!workspace || !o || !aligned16(o) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
-  if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
-  if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
+  st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
+  if (st != SAGE_OK) return st;
   if (quant_mode == SAGE_NVFP4)
     return launch_attn_fp4(*shape, causal, sm_scale, flags, bk, workspace, L, o, (cudaStream_t)stream);
   return launch_attn_q8(*shape, causal, sm_scale, quant_mode, flags, bk, workspace, L, o, (cudaStream_t)stream);
@@ -134,6 +145,9 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
                            void *dev_buf, size_t dev_bytes, sage_stream_t stream) {
   sage_ws_layout L;
   sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  // every argument condition of the two calls below, before the first copy
+  st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
   if (st != SAGE_OK) return st;
   if (!q_host || !k_host || !v_host || !o_host || !dev_buf) return SAGE_ERR_INVALID_ARG;
   if (((uintptr_t)dev_buf & 1023)) return SAGE_ERR_INVALID_ARG;

@@ -97,6 +97,34 @@ def test_pointer_workspace_and_flag_checks(sage):
     assert a(C.byref(s2), 1, 0.125, 0, 1, 128, 64, ok, need2, ok, None) == 2          # causal with N > M
 
 
+def test_host_call_checks_everything_before_its_first_copy(sage):
+    """sage_attn_host validates all of its own and its two calls' arguments
+    before it enqueues anything (a copy attempted here, without a GPU, would
+    surface as SAGE_ERR_CUDA instead of the codes below)."""
+    s = sage.Shape(1, 2, 2, 256, 256, 64)
+    need = sage.lib.sage_host_buffer_bytes(C.byref(s), 0, 128, 64)
+    assert need > sage.sage_workspace_bytes(s, 0, 128, 64)
+    h = C.c_void_p(1 << 20)                  # host pointers, never dereferenced
+    dbuf = C.c_void_p(1 << 30)               # 1024-aligned, never dereferenced
+    f = sage.lib.sage_attn_host
+
+    def call(shape=s, causal=0, scale=0.125, mode=0, flags=1, bq=128, bk=64, q=h, k=h, v=h, o=h, buf=dbuf,
+             n=need):
+        return f(C.byref(shape), causal, scale, mode, flags, bq, bk, q, k, v, o, buf, n, None)
+    assert call(q=None) == 1 and call(o=None) == 1 and call(buf=None) == 1
+    assert call(buf=C.c_void_p((1 << 30) + 512)) == 1                    # device buffer alignment
+    assert call(n=need - 1) == 3                                          # too small
+    assert call(flags=64) == 1                                            # unknown flag
+    assert call(scale=0.0) == 1 and call(scale=float("nan")) == 1
+    s2 = sage.Shape(1, 2, 2, 512, 256, 64)
+    need2 = sage.lib.sage_host_buffer_bytes(C.byref(s2), 0, 128, 64)
+    assert call(shape=s2, causal=1, n=need2) == 2                         # causal with N > M
+    need4 = sage.lib.sage_host_buffer_bytes(C.byref(s), 2, 128, 64)
+    assert need4 > 0 and call(mode=2, bk=64, n=need4) == 2                # NVFP4 attention takes 128-key tiles
+    assert call(bq=64) == 2 and call(mode=7) == 1                         # layout conditions
+    assert sage.lib.sage_host_buffer_bytes(C.byref(sage.Shape(1, 3, 2, 256, 256, 64)), 0, 128, 64) == 0
+
+
 def test_status_strings(sage):
     for code in range(7):
         assert sage.sage_status_str(code)

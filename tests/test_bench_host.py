@@ -51,15 +51,24 @@ def test_kernel_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_hash() != h0
 
 
-def test_traffic_record_needs_the_current_sources(tmp_path, monkeypatch):
-    root = _fake_tree(tmp_path, "int g;\n")
+def test_traffic_record_needs_the_kernels_current_sources(tmp_path, monkeypatch):
+    d = tmp_path / "bit_quantized_attention_gb300" / "csrc"
+    d.mkdir(parents=True)
+    for f in ("attn_q8.cu", "sm103.cuh", "layout.h", "launch.h", "api.cu", "attn_fp4.cu"):
+        (d / f).write_text("int %s_x;\n" % f.replace(".", "_"))
+    root = str(tmp_path)
     monkeypatch.setattr(bench, "ROOT", root)
     os.makedirs(os.path.join(root, "profiles"))
     with open(os.path.join(root, "profiles", "attn_traffic.txt"), "w") as f:
-        f.write("# comment\nwl_bk128 %s 123\nwl_bk64 000000000000 456\n" % bench.kernel_hash())
-    assert bench.read_traffic("wl_bk128") == 123.0
-    assert bench.read_traffic("wl_bk64") is None
-    assert bench.read_traffic("other") is None
+        f.write("# comment\nwl_bk128 %s 123\nwl_bk64 000000000000 456\n" % bench.kernel_hash(bench.ATTN_SOURCES[0]))
+    assert bench.read_traffic("wl_bk128", 0) == 123.0
+    assert bench.read_traffic("wl_bk64", 0) is None
+    assert bench.read_traffic("other", 0) is None
+    assert bench.read_traffic("wl_bk128", 2) is None          # the NVFP4 kernel's files differ
+    (d / "api.cu").write_text("int changed;\n")             # not a file the kernel is built from
+    assert bench.read_traffic("wl_bk128", 0) == 123.0
+    (d / "attn_q8.cu").write_text("int changed;\n")
+    assert bench.read_traffic("wl_bk128", 0) is None
 
 
 def test_job_tops_is_all_ranks_over_the_slowest():
