@@ -63,22 +63,33 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 extern "C" {
 
+// The workspace layout, and the limits of the launches built on it: every
+// grid and work-item count the kernels hold in an int stays below 2^31.
+static sage_status request_layout(const sage_shape *shape, int quant_mode, int bq, int bk, sage_ws_layout *L) {
+  sage_status st = compute_layout(shape, quant_mode, bq, bk, L);
+  if (st != SAGE_OK) return st;
+  const int64_t bhq = (int64_t)shape->B * shape->Hq, bhk = (int64_t)shape->B * shape->Hkv;
+  const int64_t items = bhq * L->Tm + bhk * ((int64_t)L->Tn + L->M_pad / 128);
+  if (items >= ((int64_t)1 << 31)) return SAGE_ERR_UNSUPPORTED;
+  return SAGE_OK;
+}
+
 size_t sage_workspace_bytes(const sage_shape *shape, int quant_mode, int bq, int bk) {
   sage_ws_layout L;
-  if (compute_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  if (request_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
   return L.total;
 }
 
 sage_status sage_workspace_layout(const sage_shape *shape, int quant_mode, int bq, int bk, sage_ws_layout *out) {
   if (!out) return SAGE_ERR_INVALID_ARG;
-  return compute_layout(shape, quant_mode, bq, bk, out);
+  return request_layout(shape, quant_mode, bq, bk, out);
 }
 
 sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags, int bq, int bk, const void *q,
                               const void *k, const void *v, void *workspace, size_t workspace_bytes,
                               sage_stream_t stream) {
   sage_ws_layout L;
-  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
   if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
@@ -101,7 +112,7 @@ static sage_status check_attn_args(const sage_shape *shape, int causal, float sm
 sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
                           int bk, const void *workspace, size_t workspace_bytes, void *o, sage_stream_t stream) {
   sage_ws_layout L;
-  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
   if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
   if (!workspace || !o || !aligned16(o) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
@@ -117,7 +128,7 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
                                              const void *q, const void *k, const void *v, void *workspace,
                                              size_t workspace_bytes, sage_stream_t stream) {
   sage_ws_layout L;
-  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
   if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
@@ -136,7 +147,7 @@ static size_t io_bytes(const sage_shape *s) {
 
 size_t sage_host_buffer_bytes(const sage_shape *shape, int quant_mode, int bq, int bk) {
   sage_ws_layout L;
-  if (compute_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  if (request_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
   return L.total + io_bytes(shape);
 }
 
@@ -144,7 +155,7 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
                            int bk, const void *q_host, const void *k_host, const void *v_host, void *o_host,
                            void *dev_buf, size_t dev_bytes, sage_stream_t stream) {
   sage_ws_layout L;
-  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
   // every argument condition of the two calls below, before the first copy
   st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
@@ -174,7 +185,7 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
 sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,
                              int *code, int *site) {
   sage_ws_layout L;
-  sage_status st = compute_layout(shape, quant_mode, bq, bk, &L);
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
   if (!workspace || !code || !site) return SAGE_ERR_INVALID_ARG;
   int buf[4] = {0, 0, 0, 0};

@@ -66,6 +66,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
     ((1, 2, 2, 256, 0, 64), 0, 128, 64, 1),       # empty keys
     ((1, 2, 2, 256, 256, 64), 7, 128, 64, 1),     # unknown mode
     ((1, 2, 2, 1 << 24, 256, 64), 0, 128, 64, 2),  # beyond the exact-mean token limit
+    ((1024, 1024, 1024, 1 << 23, 256, 64), 0, 128, 64, 2),  # 2^36 query blocks: past the kernels' int counts
 ])
 def test_invalid_requests_rejected(sage, shp, mode, bq, bk, code):
     s = sage.Shape(*shp)
