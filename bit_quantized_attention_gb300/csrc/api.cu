@@ -64,13 +64,17 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 extern "C" {
 
 // The workspace layout, and the limits of the launches built on it: every
-// grid and work-item count the kernels hold in an int stays below 2^31.
+// grid and work-item count the kernels hold in an int, and every row
+// coordinate of the Q^ / K^ / V^T tensor maps (32-bit in a TMA copy), stays
+// below 2^31.
 static sage_status request_layout(const sage_shape *shape, int quant_mode, int bq, int bk, sage_ws_layout *L) {
   sage_status st = compute_layout(shape, quant_mode, bq, bk, L);
   if (st != SAGE_OK) return st;
+  const int64_t lim = (int64_t)1 << 31;
   const int64_t bhq = (int64_t)shape->B * shape->Hq, bhk = (int64_t)shape->B * shape->Hkv;
   const int64_t items = bhq * L->Tm + bhk * ((int64_t)L->Tn + L->M_pad / 128);
-  if (items >= ((int64_t)1 << 31)) return SAGE_ERR_UNSUPPORTED;
+  if (items >= lim || bhq * L->N_pad >= lim || bhk * L->M_pad >= lim || bhk * shape->d >= lim)
+    return SAGE_ERR_UNSUPPORTED;
   return SAGE_OK;
 }
 

@@ -67,6 +67,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
     ((1, 2, 2, 256, 256, 64), 7, 128, 64, 1),     # unknown mode
     ((1, 2, 2, 1 << 24, 256, 64), 0, 128, 64, 2),  # beyond the exact-mean token limit
     ((1024, 1024, 1024, 1 << 23, 256, 64), 0, 128, 64, 2),  # 2^36 query blocks: past the kernels' int counts
+    ((1, 512, 512, 256, 1 << 23, 64), 0, 128, 64, 2),  # 2^32 K rows: past a TMA row coordinate
 ])
 def test_invalid_requests_rejected(sage, shp, mode, bq, bk, code):
     s = sage.Shape(*shp)
