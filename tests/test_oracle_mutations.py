@@ -63,6 +63,20 @@ MUTATIONS = [
     ("NVFP4 K code from the next element",
      "out->kc[(hb * M + t) * d + gi * 16 + e] = orc_nvfp4_code(gg[e], sc);",
      "out->kc[(hb * M + t) * d + gi * 16 + e] = orc_nvfp4_code(gg[(e + 1) & 15], sc);"),
+    ("P2 not divided by s_P1", "p2[c] = (sP1 == 0.0) ? 0.0 : pv[u + c] / sP1;", "p2[c] = pv[u + c];"),
+    ("P^ not multiplied back by s_P2", "ph = orc_e2m1_decode(orc_e2m1_encode(p2[c] / s2)) * s2;",
+     "ph = orc_e2m1_decode(orc_e2m1_encode(p2[c] / s2));"),
+    ("E2M1 code of the unscaled P2", "ph = orc_e2m1_decode(orc_e2m1_encode(p2[c] / s2)) * s2;",
+     "ph = orc_e2m1_decode(orc_e2m1_encode(p2[c])) * s2;"),
+    ("NVFP4 V block max from one token",
+     "            for (t = t0; t < t1; ++t)\n              if (fabsf(g[(int64_t)t * d + c]) > amax) amax = "
+     "fabsf(g[(int64_t)t * d + c]);\n            sc = orc_nvfp4_scale(amax);\n            out->vs[",
+     "            for (t = t0; t < t0 + 1; ++t)\n              if (fabsf(g[(int64_t)t * d + c]) > amax) amax = "
+     "fabsf(g[(int64_t)t * d + c]);\n            sc = orc_nvfp4_scale(amax);\n            out->vs["),
+    ("NVFP4 V scale index", "orc_e4m3_decode(qz->vs[(hk * Mt16 + t / 16) * d + e]);",
+     "orc_e4m3_decode(qz->vs[(hk * Mt16 + t / 32) * d + e]);"),
+    ("l summed over quantized P^", "for (c = 0; c < bk; ++c) rs += pv[c];",
+     "for (c = 0; c < bk; ++c) rs += orc_e4m3_decode(orc_e4m3_encode(pv[c] * 448.0)) / 448.0;"),
     ("direct P~ keeps a level-1 scale", "(flags & ORC_P_DIRECT) ? 1.0 :", "(flags & ORC_P_DIRECT) ? (1.0 / 3.0) :"),
 ]
 
