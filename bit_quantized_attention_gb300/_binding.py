@@ -34,6 +34,9 @@ class SageError(RuntimeError):
 class Shape(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("B", "Hq", "Hkv", "N", "M", "d")]
 
+    def __iter__(self):
+        return iter((self.B, self.Hq, self.Hkv, self.N, self.M, self.d))
+
 
 class WsLayout(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
@@ -85,9 +88,31 @@ def _ptr(t: torch.Tensor) -> C.c_void_p:
     return C.c_void_p(t.data_ptr())
 
 
+def _bf16_4d(t: torch.Tensor, name: str):
+    if not (t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+        raise ValueError("%s must be a contiguous 4-D bf16 tensor" % name)
+
+
 def _bf16_cuda(t: torch.Tensor, name: str):
-    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
-        raise ValueError("%s must be a contiguous 4-D bf16 CUDA tensor" % name)
+    _bf16_4d(t, name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _qkv_shape(q, k, v) -> "Shape":
+    """The shape the three inputs agree on (v must have k's shape: the library
+    reads v with k's dimensions)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _bf16_4d(t, n)
+    shape = shape_of(q, k)
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("v must have k's shape [B, Hkv, M, d]")
+    return shape
+
+
+def _same_request(ws: "Workspace", shape: "Shape", mode: int, bq: int, bk: int):
+    if (tuple(ws.shape) != tuple(shape) or ws.mode != mode or ws.bq != bq or ws.bk != bk):
+        raise ValueError("the workspace was made for another shape, mode or tiling")
 
 
 def shape_of(q: torch.Tensor, k: torch.Tensor) -> Shape:
@@ -96,6 +121,7 @@ def shape_of(q: torch.Tensor, k: torch.Tensor) -> Shape:
     if B != Bk or d != dk:
         raise ValueError("q and k disagree on batch or head dim")
     return Shape(B, Hq, Hkv, N, M, d)
+
 
 
 def sage_workspace_layout(shape: Shape, mode: int, bq: int, bk: int) -> WsLayout:
@@ -133,9 +159,11 @@ def new_workspace(shape: Shape, mode: int, flags: int, bq: int = 128, bk: int = 
 
 def sage_quantize_qkv(q, k, v, mode: int, flags: int, bq: int = 128, bk: int = 64, workspace=None,
                       stream=None) -> Workspace:
+    shape = _qkv_shape(q, k, v)
+    if workspace is not None:
+        _same_request(workspace, shape, mode, bq, bk)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _bf16_cuda(t, n)
-    shape = shape_of(q, k)
     ws = workspace or new_workspace(shape, mode, flags, bq, bk, q.device)
     ws.flags = flags
     _check(lib.sage_quantize_qkv(C.byref(shape), mode, flags, bq, bk, _ptr(q), _ptr(k), _ptr(v), _ptr(ws.buf),
@@ -147,9 +175,11 @@ def sage_quantize_qkv_static_scratch(q, k, v, mode: int, flags: int, bq: int = 1
                                      workspace=None, stream=None) -> Workspace:
     """The pre-pass with its reduction scratch inside the library (no scratch
     region is needed from the caller; see include/sage.h for the limit)."""
+    shape = _qkv_shape(q, k, v)
+    if workspace is not None:
+        _same_request(workspace, shape, mode, bq, bk)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _bf16_cuda(t, n)
-    shape = shape_of(q, k)
     ws = workspace or new_workspace(shape, mode, flags, bq, bk, q.device)
     ws.flags = flags
     _check(lib.sage_quantize_qkv_static_scratch(C.byref(shape), mode, flags, bq, bk, _ptr(q), _ptr(k), _ptr(v),
@@ -162,6 +192,10 @@ def sage_attn_fwd(ws: Workspace, causal: bool, sm_scale: float, out=None, stream
     s = ws.shape
     if out is None:
         out = torch.empty((s.B, s.Hq, s.N, s.d), dtype=torch.bfloat16, device=ws.buf.device)
+    else:
+        _bf16_4d(out, "out")
+        if tuple(out.shape) != (s.B, s.Hq, s.N, s.d) or out.device != ws.buf.device:
+            raise ValueError("out must be [B, Hq, N, d] on the workspace's device")
     _check(lib.sage_attn_fwd(C.byref(s), int(bool(causal)), float(sm_scale), ws.mode, ws.flags, ws.bq, ws.bk,
                              _ptr(ws.buf), ws.buf.numel(), _ptr(out), _stream(stream)), "sage_attn_fwd")
     return out
@@ -182,8 +216,13 @@ def sage_attn_host(shape: Shape, causal: bool, sm_scale: float, mode: int, flags
                    q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor, o_host: torch.Tensor,
                    dev_buf: torch.Tensor, stream=None):
     """End-to-end call on host tensors (pinned for asynchronous copies)."""
-    if (dev_buf.data_ptr() % 1024) != 0:
-        raise ValueError("dev_buf must be 1024-byte aligned")
+    qs, ks = (shape.B, shape.Hq, shape.N, shape.d), (shape.B, shape.Hkv, shape.M, shape.d)
+    for t, n, want in ((q_host, "q_host", qs), (k_host, "k_host", ks), (v_host, "v_host", ks), (o_host, "o_host", qs)):
+        _bf16_4d(t, n)
+        if t.is_cuda or tuple(t.shape) != want:
+            raise ValueError("%s must be a host tensor of shape %s" % (n, want))
+    if not dev_buf.is_cuda or (dev_buf.data_ptr() % 1024) != 0:
+        raise ValueError("dev_buf must be a 1024-byte aligned CUDA buffer")
     _check(lib.sage_attn_host(C.byref(shape), int(bool(causal)), float(sm_scale), mode, flags, bq, bk,
                               _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(dev_buf),
                               dev_buf.numel(), _stream(stream)), "sage_attn_host")
