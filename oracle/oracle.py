@@ -18,6 +18,7 @@ SRC = os.path.join(HERE, "sage_oracle.c")
 LIB = os.path.join(HERE, "liborc.so")
 
 MODE_Q8_PV8, MODE_QF8_PV8, MODE_NVFP4 = 0, 1, 2
+MODE_SAGEBWD_I8 = 3  # SageBwd forward: INT8 per-block Q, K, V; INT8 per-token P~
 SMOOTH_K, SMOOTH_Q, SMOOTH_V = 1, 2, 4
 P_DIRECT = 8  # NVFP4 ablation: phi on P~ directly (no level-1 scale)
 Q_PER_TOKEN = 0x10  # one Q scale per query row (INT8 / E4M3 modes)
@@ -52,7 +53,8 @@ class _Quant(C.Structure):
     _fields_ = [("qc", C.c_void_p), ("dq", C.c_void_p), ("qbar", C.c_void_p),
                 ("kc", C.c_void_p), ("dk", C.c_void_p), ("kbar", C.c_void_p),
                 ("vc", C.c_void_p), ("dv", C.c_void_p), ("vm", C.c_void_p),
-                ("qs", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p), ("dqt", C.c_void_p)]
+                ("qs", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p), ("dqt", C.c_void_p),
+                ("dvb", C.c_void_p)]
 
 
 def lib():
@@ -81,6 +83,8 @@ def lib():
             L.orc_attn_rows.argtypes = [C.POINTER(_Shape), i32, i32, i32, i32, i32, dbl, vp, vp, vp,
                                         C.POINTER(_Quant), vp, i64, vp]
             L.orc_attn_rows.restype = i32
+            L.orc_attn_rows_lse.argtypes = L.orc_attn_rows.argtypes + [vp]
+            L.orc_attn_rows_lse.restype = i32
             L.orc_attn_exact_rows.argtypes = [C.POINTER(_Shape), i32, dbl, vp, vp, vp, vp, i64, vp]
             L.orc_attn_exact_rows.restype = i32
             _lib = L
@@ -176,6 +180,7 @@ class Quant:
     ks: np.ndarray
     vs: np.ndarray
     dqt: np.ndarray  # per-token Q scales (Q_PER_TOKEN)
+    dvb: np.ndarray  # per-block V scales (MODE_SAGEBWD_I8)
 
     def _struct(self):
         return _Quant(*[_p(getattr(self, f)) for f, _ in _Quant._fields_])
@@ -208,7 +213,8 @@ def quantize(shape, mode, flags, bq, bk, q, k, v) -> Quant:
         vc=np.zeros((B, Hkv, M, d), np.uint8), dv=np.zeros((B, Hkv, d), np.float32),
         vm=np.zeros((B, Hkv, d), np.float32),
         qs=np.zeros((B, Hq, N, G), np.uint8), ks=np.zeros((B, Hkv, M, G), np.uint8),
-        vs=np.zeros((B, Hkv, Mt16, d), np.uint8), dqt=np.zeros((B, Hq, N), np.float32))
+        vs=np.zeros((B, Hkv, Mt16, d), np.uint8), dqt=np.zeros((B, Hq, N), np.float32),
+        dvb=np.zeros((B, Hkv, Tn), np.float32))
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     assert qb.size == B * Hq * N * d and kb.size == B * Hkv * M * d and vb.size == kb.size
     st = qz._struct()
@@ -232,6 +238,22 @@ def attn_rows(shape, mode, flags, bq, bk, causal, sm_scale, q, k, v, qz: Quant, 
     if rc:
         raise OracleError("orc_attn_rows rc=%d" % rc)
     return out
+
+
+def attn_rows_lse(shape, mode, flags, bq, bk, causal, sm_scale, q, k, v, qz: Quant, rows):
+    """(out, lse): the fp64 output rows and each row's m + ln(l) after the last key tile."""
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    d = shape[5]
+    out = np.zeros((rows.size, d), np.float64)
+    lse = np.zeros(rows.size, np.float64)
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    st = qz._struct()
+    rc = lib().orc_attn_rows_lse(C.byref(_shape(*shape)), mode, flags, bq, bk, int(bool(causal)),
+                                 float(sm_scale), _p(qb), _p(kb), _p(vb), C.byref(st), _p(rows),
+                                 rows.size, _p(out), _p(lse))
+    if rc:
+        raise OracleError("orc_attn_rows_lse rc=%d" % rc)
+    return out, lse
 
 
 def attn_exact_rows(shape, causal, sm_scale, q, k, v, rows) -> np.ndarray:

@@ -184,11 +184,15 @@ uint8_t orc_nvfp4_code(float x, uint8_t scale_code) {
 
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+/* Q and K take the INT8 per-block quantizer in mode 0 and in the SageBwd
+ * forward (mode 3), the E4M3 one in mode 1 */
+static int int8_qk(int mode) { return mode == ORC_Q8_PV8 || mode == ORC_SAGEBWD_I8; }
+
 static int check_shape(const orc_shape *s, int mode, int bq, int bk) {
   if (!s || s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->N <= 0 || s->M <= 0 || s->d <= 0)
     return ORC_ERR_ARG;
   if (s->Hq % s->Hkv != 0 || bq <= 0 || bk <= 0) return ORC_ERR_ARG;
-  if (mode < 0 || mode > 2) return ORC_ERR_ARG;
+  if (mode < 0 || mode > 3) return ORC_ERR_ARG;
   if (mode == ORC_NVFP4 && (s->d % 16 != 0 || bk % 16 != 0)) return ORC_ERR_ARG;
   if ((int64_t)s->M > ((int64_t)1 << 23) || (int64_t)s->N > ((int64_t)1 << 23)) return ORC_ERR_ARG;
   return ORC_OK;
@@ -257,12 +261,12 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
               g[(int64_t)(t - t0) * d + c] = x;
               if (fabsf(x) > amax) amax = fabsf(x);
             }
-          sc = (mode == ORC_Q8_PV8) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
+          sc = int8_qk(mode) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
           out->dk[hb * Tn + j] = sc;
           for (t = t0; t < t1; ++t)
             for (c = 0; c < d; ++c) {
               float x = g[(int64_t)(t - t0) * d + c];
-              out->kc[(hb * M + t) * d + c] = (mode == ORC_Q8_PV8)
+              out->kc[(hb * M + t) * d + c] = int8_qk(mode)
                                                   ? (uint8_t)(int8_t)orc_int8_code(x, sc)
                                                   : orc_fp8_code(x, sc);
             }
@@ -293,6 +297,22 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
             for (t = t0; t < t1; ++t)
               out->vc[(hb * M + t) * d + c] = orc_nvfp4_code(g[(int64_t)t * d + c], sc);
           }
+      } else if (mode == ORC_SAGEBWD_I8) {
+        /* SageBwd: per-block INT8 of V' over each bk-token block and all d
+         * channels, s_V = max|V'_j| / 127 (the same quantizer as Q and K) */
+        int64_t j;
+        for (j = 0; j < Tn; ++j) {
+          const int t0 = (int)(j * bk), t1 = (int)((j + 1) * bk < M ? (j + 1) * bk : M);
+          float amax = 0.0f, sc;
+          for (t = t0; t < t1; ++t)
+            for (c = 0; c < d; ++c)
+              if (fabsf(g[(int64_t)t * d + c]) > amax) amax = fabsf(g[(int64_t)t * d + c]);
+          sc = orc_int8_scale(amax);
+          out->dvb[hb * Tn + j] = sc;
+          for (t = t0; t < t1; ++t)
+            for (c = 0; c < d; ++c)
+              out->vc[(hb * M + t) * d + c] = (uint8_t)(int8_t)orc_int8_code(g[(int64_t)t * d + c], sc);
+        }
       } else {
         float *dv = out->dv + hb * d;
         for (c = 0; c < d; ++c) {
@@ -349,11 +369,11 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
             float amax = 0.0f, sc;
             for (c = 0; c < d; ++c)
               if (fabsf(g[(int64_t)(r - r0) * d + c]) > amax) amax = fabsf(g[(int64_t)(r - r0) * d + c]);
-            sc = (mode == ORC_Q8_PV8) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
+            sc = int8_qk(mode) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
             out->dqt[hb * N + r] = sc;
             for (c = 0; c < d; ++c) {
               float x = g[(int64_t)(r - r0) * d + c];
-              out->qc[(hb * N + r) * d + c] = (mode == ORC_Q8_PV8) ? (uint8_t)(int8_t)orc_int8_code(x, sc)
+              out->qc[(hb * N + r) * d + c] = int8_qk(mode) ? (uint8_t)(int8_t)orc_int8_code(x, sc)
                                                                    : orc_fp8_code(x, sc);
             }
           }
@@ -362,12 +382,12 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
           for (r = r0; r < r1; ++r)
             for (c = 0; c < d; ++c)
               if (fabsf(g[(int64_t)(r - r0) * d + c]) > amax) amax = fabsf(g[(int64_t)(r - r0) * d + c]);
-          sc = (mode == ORC_Q8_PV8) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
+          sc = int8_qk(mode) ? orc_int8_scale(amax) : orc_fp8_scale(amax);
           out->dq[hb * Tm + ib] = sc;
           for (r = r0; r < r1; ++r)
             for (c = 0; c < d; ++c) {
               float x = g[(int64_t)(r - r0) * d + c];
-              out->qc[(hb * N + r) * d + c] = (mode == ORC_Q8_PV8)
+              out->qc[(hb * N + r) * d + c] = int8_qk(mode)
                                                   ? (uint8_t)(int8_t)orc_int8_code(x, sc)
                                                   : orc_fp8_code(x, sc);
             }
@@ -402,7 +422,7 @@ static void deq_q_row(const orc_shape *s, int mode, int flags, int bq, const uin
     const int64_t e = (hb * N + r) * d + c;
     if (flags & ORC_EXACT_QK)
       out[c] = orc_bf16_decode(q[e]) - (double)qbar[c];
-    else if (mode == ORC_Q8_PV8)
+    else if (int8_qk(mode))
       out[c] = sq * (double)(int8_t)qz->qc[e];
     else if (mode == ORC_QF8_PV8)
       out[c] = sq * orc_e4m3_decode(qz->qc[e]);
@@ -421,7 +441,7 @@ static void deq_k_row(const orc_shape *s, int mode, int flags, int bk, const uin
     const int64_t e = (hb * M + t) * d + c;
     if (flags & ORC_EXACT_QK)
       out[c] = orc_bf16_decode(k[e]) - (double)qz->kbar[hb * d + c];
-    else if (mode == ORC_Q8_PV8)
+    else if (int8_qk(mode))
       out[c] = (double)qz->dk[hb * Tn + t / bk] * (double)(int8_t)qz->kc[e];
     else if (mode == ORC_QF8_PV8)
       out[c] = (double)qz->dk[hb * Tn + t / bk] * orc_e4m3_decode(qz->kc[e]);
@@ -430,9 +450,10 @@ static void deq_k_row(const orc_shape *s, int mode, int flags, int bk, const uin
   }
 }
 
-int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int causal,
-                  double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out) {
+int orc_attn_rows_lse(const orc_shape *s, int mode, int flags, int bq, int bk, int causal,
+                      double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out,
+                      double *lse) {
   const int Hq = s->Hq, Hkv = s->Hkv, N = s->N, M = s->M, d = s->d;
   const int64_t Tn = cdiv(M, bk), Mt16 = cdiv(M, 16);
   double *qrow, *krow, *sv, *pv, *R, *O, *vrow;
@@ -467,7 +488,7 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
 
     for (j = 0; j < Tn; ++j) {
       const int kb = (int)(j * bk);
-      double mt = -INFINITY, m_new, alpha, sP1 = 0.0;
+      double mt = -INFINITY, m_new, alpha, sP1 = 0.0, sP = 0.0;
 
       /* S_ij = deq(Q^_i) deq(K^_j)^T + dS_ij, dS_ij = q_bar_i deq(K^_j)^T,
        * then times sm_scale (SageAttention2 summary §3.4 "Smoothing Q"). */
@@ -510,6 +531,21 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
           for (e = 0; e < d; ++e)
             R[e] += pv[c] * (orc_bf16_decode(v[(hk * M + t) * d + e]) - (double)qz->vm[hk * d + e]);
         }
+      } else if (mode == ORC_SAGEBWD_I8) {
+        /* SageBwd per-token P~ (SageAttention3 summary, "SageBwd Forward
+         * Pass"): s_P = exp(rowmax S_ij - m_ij) / 127, the row's largest P~ of
+         * this tile over 127; P^ = round(P~ / s_P), ties to even; R = P^ V^ in
+         * integers, dequantized by s_P s_V,j in the accumulation below */
+        sP = (mt == -INFINITY) ? 0.0 : exp(mt - m_new) / 127.0;
+        for (c = 0; c < bk; ++c) {
+          const int t = kb + c;
+          double ph;
+          if (sP == 0.0 || pv[c] == 0.0) continue;
+          ph = nearbyint(pv[c] / sP);
+          if (ph > 127.0) ph = 127.0;
+          if (ph == 0.0) continue;
+          for (e = 0; e < d; ++e) R[e] += ph * (double)(int8_t)qz->vc[(hk * M + t) * d + e];
+        }
       } else if (mode != ORC_NVFP4) {
         /* P^ = e4m3(P~ * 448) (static scale 1/448), R = P^ V^ */
         for (c = 0; c < bk; ++c) {
@@ -550,9 +586,13 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
       }
 
       /* two-level accumulation: O_ij = diag(e^(m_i,j-1 - m_ij)) O_i,j-1 + R_ij
-       * (FP4 mode: + s_P1 R_ij) */
-      for (e = 0; e < d; ++e)
-        O[e] = alpha * O[e] + ((mode == ORC_NVFP4 && !(flags & ORC_EXACT_PV)) ? sP1 * R[e] : R[e]);
+       * (FP4 mode: + s_P1 R_ij; SageBwd: + s_P s_V,j R_ij) */
+      {
+        double rsc = 1.0;
+        if (!(flags & ORC_EXACT_PV) && mode == ORC_NVFP4) rsc = sP1;
+        if (!(flags & ORC_EXACT_PV) && mode == ORC_SAGEBWD_I8) rsc = sP * (double)qz->dvb[hk * Tn + j];
+        for (e = 0; e < d; ++e) O[e] = alpha * O[e] + rsc * R[e];
+      }
       m = m_new;
     }
 
@@ -560,10 +600,12 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
      * scales are inside the product), plus V_m when V was smoothed. */
     for (e = 0; e < d; ++e) {
       double o = O[e] / l;
-      if (!(flags & ORC_EXACT_PV) && mode != ORC_NVFP4) o = o / 448.0 * (double)qz->dv[hk * d + e];
+      if (!(flags & ORC_EXACT_PV) && (mode == ORC_Q8_PV8 || mode == ORC_QF8_PV8))
+        o = o / 448.0 * (double)qz->dv[hk * d + e];
       vrow[e] = o + (double)qz->vm[hk * d + e];
       out[ri * d + e] = vrow[e];
     }
+    if (lse) lse[ri] = m + log(l);
   }
   free(qrow);
   free(krow);
@@ -573,6 +615,13 @@ int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int c
   free(R);
   free(O);
   return ORC_OK;
+}
+
+int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int causal,
+                  double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out) {
+  return orc_attn_rows_lse(s, mode, flags, bq, bk, causal, sm_scale, q, k, v, qz, rows, nrows, out,
+                           NULL);
 }
 
 int orc_attn_exact_rows(const orc_shape *s, int causal, double sm_scale, const uint16_t *q,

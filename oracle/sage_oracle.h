@@ -12,6 +12,9 @@
  *     pages' order: for each query block i and key tile j = 0..Tn-1,
  *     S = deq(Q^) deq(K^)^T [+ dS], online max / sum, P~ quantization,
  *     tile partial R = P^ V^, running O = alpha O + R, then O / l scaled;
+ *   - the SageBwd forward of the same loop (INT8 per-block Q, K, V; INT8 P~
+ *     with a per-row scale for each key tile) and, for every mode, each row's
+ *     log-sum-exp m + ln(l), the statistic a backward pass recomputes P from;
  *   - plain fp64 softmax(Q K^T sm_scale) V on the bf16 inputs.
  *
  * Sources (web pages this method is described on):
@@ -19,7 +22,8 @@
  *   §3.4: smoothing Q / K, dS, FP8 P~ with static 1/448, per-channel FP8 V,
  *   two-level accumulation, V smoothing, "The Complete Algorithm".
  *   SageAttention3 summary (arXiv 2505.11594), §3.4: NVFP4 quantizer phi,
- *   two-level quantization for P, FP4 attention algorithm.
+ *   two-level quantization for P, FP4 attention algorithm; "SageBwd Forward
+ *   Pass": per-block INT8 Q, K, V and per-token INT8 P.
  *   "Quantization for Attention, in depth" (aicassindra): datapath and the
  *   INT8 per-block quantizer.
  *
@@ -43,6 +47,11 @@ extern "C" {
 #define ORC_Q8_PV8 0   /* INT8 per-block Q/K, FP8 P~ and per-channel FP8 V */
 #define ORC_QF8_PV8 1  /* FP8 E4M3 per-block Q/K, FP8 P~ / V */
 #define ORC_NVFP4 2    /* E2M1 1x16 blocks, E4M3 scales, two-level P~ */
+/* SageBwd forward (SageAttention3 summary, "SageBwd Forward Pass"): INT8
+ * per-block Q and K as in mode 0, INT8 per-block V (one scale per bk-token
+ * block over all d channels), INT8 P~ with one scale per row and key tile,
+ * s_P = exp(rowmax S_ij - m_ij) / 127 */
+#define ORC_SAGEBWD_I8 3
 
 /* flags */
 #define ORC_SMOOTH_K 1
@@ -83,6 +92,7 @@ typedef struct {
  *   ks  [B,Hkv,M,d/16]         E4M3 block scales (mode 2)
  *   vs  [B,Hkv,ceil(M/16),d]   E4M3 block scales along tokens (mode 2)
  *   dqt [B,Hq,N]     per-token Q scale (modes 0, 1 with ORC_Q_PER_TOKEN; dq unused then)
+ *   dvb [B,Hkv,Tn]   per-block V scale (mode 3; V codes are int8 values then)
  * Tm = ceil(N/bq), Tn = ceil(M/bk).  Pointers a mode does not use may be NULL. */
 typedef struct {
   uint8_t *qc;
@@ -93,6 +103,7 @@ typedef struct {
   float *dv, *vm;
   uint8_t *qs, *ks, *vs;
   float *dqt;
+  float *dvb;
 } orc_quant;
 
 /* ---- codecs (round to nearest, ties to even; saturate to the largest
@@ -133,6 +144,14 @@ int orc_quantize(const orc_shape *s, int mode, int flags, int bq, int bk, const 
 int orc_attn_rows(const orc_shape *s, int mode, int flags, int bq, int bk, int causal,
                   double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out);
+
+/* As orc_attn_rows, and lse[i] = m + ln(l) of row i at the end of the key
+ * loop (the softmax statistics a backward pass recomputes P from; natural log,
+ * in the units of the scaled scores S * sm_scale).  lse may be NULL. */
+int orc_attn_rows_lse(const orc_shape *s, int mode, int flags, int bq, int bk, int causal,
+                      double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out,
+                      double *lse);
 
 /* Plain softmax(Q K^T sm_scale) V in fp64 on the bf16 inputs, same masks. */
 int orc_attn_exact_rows(const orc_shape *s, int causal, double sm_scale, const uint16_t *q,

@@ -12,7 +12,8 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-TESTS = [os.path.join(ROOT, "tests", "test_oracle_codecs.py"), os.path.join(ROOT, "tests", "test_oracle_attention.py")]
+TESTS = [os.path.join(ROOT, "tests", f) for f in
+         ("test_oracle_codecs.py", "test_oracle_attention.py", "test_oracle_sagebwd.py")]
 
 # (name, text in sage_oracle.c, replacement); each text occurs exactly once
 MUTATIONS = [
@@ -78,6 +79,27 @@ MUTATIONS = [
     ("l summed over quantized P^", "for (c = 0; c < bk; ++c) rs += pv[c];",
      "for (c = 0; c < bk; ++c) rs += orc_e4m3_decode(orc_e4m3_encode(pv[c] * 448.0)) / 448.0;"),
     ("direct P~ keeps a level-1 scale", "(flags & ORC_P_DIRECT) ? 1.0 :", "(flags & ORC_P_DIRECT) ? (1.0 / 3.0) :"),
+    # SageBwd forward (per-block INT8 V, per-token INT8 P~) and the softmax statistics
+    ("SageBwd s_P divisor", "sP = (mt == -INFINITY) ? 0.0 : exp(mt - m_new) / 127.0;",
+     "sP = (mt == -INFINITY) ? 0.0 : exp(mt - m_new) / 128.0;"),
+    ("SageBwd s_P from the running max, not the tile's", "sP = (mt == -INFINITY) ? 0.0 : exp(mt - m_new) / 127.0;",
+     "sP = (mt == -INFINITY) ? 0.0 : exp(m_new - m_new) / 127.0;"),
+    ("SageBwd P^ truncated", "ph = nearbyint(pv[c] / sP);", "ph = floor(pv[c] / sP);"),
+    ("SageBwd s_P not multiplied back", "rsc = sP * (double)qz->dvb[hk * Tn + j];", "rsc = (double)qz->dvb[hk * Tn + j];"),
+    ("SageBwd s_V of the first block", "rsc = sP * (double)qz->dvb[hk * Tn + j];", "rsc = sP * (double)qz->dvb[hk * Tn];"),
+    ("SageBwd V block max over one channel",
+     "            for (c = 0; c < d; ++c)\n              if (fabsf(g[(int64_t)t * d + c]) > amax) amax = "
+     "fabsf(g[(int64_t)t * d + c]);\n          sc = orc_int8_scale(amax);\n          out->dvb",
+     "            for (c = 0; c < 1; ++c)\n              if (fabsf(g[(int64_t)t * d + c]) > amax) amax = "
+     "fabsf(g[(int64_t)t * d + c]);\n          sc = orc_int8_scale(amax);\n          out->dvb"),
+    ("SageBwd V codes from the E4M3 quantizer",
+     "out->vc[(hb * M + t) * d + c] = (uint8_t)(int8_t)orc_int8_code(g[(int64_t)t * d + c], sc);",
+     "out->vc[(hb * M + t) * d + c] = orc_fp8_code(g[(int64_t)t * d + c], sc);"),
+    ("SageBwd Q and K on the E4M3 quantizer", "return mode == ORC_Q8_PV8 || mode == ORC_SAGEBWD_I8;",
+     "return mode == ORC_Q8_PV8;"),
+    ("SageBwd output keeps the 448 / delta_V epilogue", "(mode == ORC_Q8_PV8 || mode == ORC_QF8_PV8))",
+     "mode != ORC_NVFP4)"),
+    ("lse without the log", "if (lse) lse[ri] = m + log(l);", "if (lse) lse[ri] = m + l;"),
 ]
 
 
