@@ -293,3 +293,55 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+
+
+# ---------------------------------------------------------------- varlen (packed sequences)
+def _packed_bits(x) -> np.ndarray:
+    """bf16 [total, H, d] tensor or uint16 array -> contiguous uint16 [total, H, d]."""
+    b = _bits(x)
+    assert b.ndim == 3
+    return b
+
+
+def _seq_lens(cu, name):
+    cu = np.asarray(cu, dtype=np.int64)
+    if cu.ndim != 1 or cu.size < 2 or cu[0] != 0 or np.any(np.diff(cu) < 0):
+        raise OracleError("%s must start at 0 and not decrease" % name)
+    return cu
+
+
+def attn_varlen(mode, flags, bq, bk, causal, sm_scale, q, k, v, cu_seqlens_q, cu_seqlens_k):
+    """Quantized attention over packed sequences (the varlen interface of the
+    SageAttention production guide, "Handling Varying Sequence Lengths with
+    VarLen Kernels"): q [total_q, Hq, d], k and v [total_k, Hkv, d], sequence s
+    holding rows cu_seqlens_q[s]:cu_seqlens_q[s+1] and keys
+    cu_seqlens_k[s]:cu_seqlens_k[s+1].  Each sequence is its own attention
+    problem: its own means, its own query and key blocks starting at its first
+    token, its own bottom-right causal mask.  Returns (out [total_q, Hq, d] fp64,
+    lse [total_q, Hq], one Quant per sequence or None for a sequence with no
+    query).  A sequence with queries but no keys is an argument error."""
+    qb, kb, vb = _packed_bits(q), _packed_bits(k), _packed_bits(v)
+    cq, ck = _seq_lens(cu_seqlens_q, "cu_seqlens_q"), _seq_lens(cu_seqlens_k, "cu_seqlens_k")
+    Hq, d, Hkv = qb.shape[1], qb.shape[2], kb.shape[1]
+    if cq.size != ck.size or cq[-1] != qb.shape[0] or ck[-1] != kb.shape[0] or vb.shape != kb.shape:
+        raise OracleError("cu_seqlens and packed tensors disagree")
+    out = np.zeros((qb.shape[0], Hq, d), np.float64)
+    lse = np.zeros((qb.shape[0], Hq), np.float64)
+    quants = []
+    for s in range(cq.size - 1):
+        Lq, Lk = int(cq[s + 1] - cq[s]), int(ck[s + 1] - ck[s])
+        if Lq == 0:
+            quants.append(None)
+            continue
+        if Lk == 0:
+            raise OracleError("sequence %d has queries but no keys" % s)
+        shape = (1, Hq, Hkv, Lq, Lk, d)
+        qs = np.ascontiguousarray(qb[cq[s]:cq[s + 1]].transpose(1, 0, 2))
+        ks = np.ascontiguousarray(kb[ck[s]:ck[s + 1]].transpose(1, 0, 2))
+        vs = np.ascontiguousarray(vb[ck[s]:ck[s + 1]].transpose(1, 0, 2))
+        qz = quantize(shape, mode, flags & 0xFF, bq, bk, qs, ks, vs)
+        o, l = attn_rows_lse(shape, mode, flags, bq, bk, causal, sm_scale, qs, ks, vs, qz, all_rows(shape))
+        out[cq[s]:cq[s + 1]] = o.reshape(Hq, Lq, d).transpose(1, 0, 2)
+        lse[cq[s]:cq[s + 1]] = l.reshape(Hq, Lq).T
+        quants.append(qz)
+    return out, lse, quants

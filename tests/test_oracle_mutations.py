@@ -13,9 +13,10 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TESTS = [os.path.join(ROOT, "tests", f) for f in
-         ("test_oracle_codecs.py", "test_oracle_attention.py", "test_oracle_sagebwd.py")]
+         ("test_oracle_codecs.py", "test_oracle_attention.py", "test_oracle_sagebwd.py", "test_oracle_varlen.py")]
 
-# (name, text in sage_oracle.c, replacement); each text occurs exactly once
+# (name, text in sage_oracle.c, replacement); each text occurs exactly once.  The
+# packed-sequence composition lives in oracle.py: those entries name that file.
 MUTATIONS = [
     ("dS dropped", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = (s0) * sm_scale;"),
     ("dS sign", "sv[c] = (s0 + ds) * sm_scale;", "sv[c] = (s0 - ds) * sm_scale;"),
@@ -100,6 +101,12 @@ MUTATIONS = [
     ("SageBwd output keeps the 448 / delta_V epilogue", "(mode == ORC_Q8_PV8 || mode == ORC_QF8_PV8))",
      "mode != ORC_NVFP4)"),
     ("lse without the log", "if (lse) lse[ri] = m + log(l);", "if (lse) lse[ri] = m + l;"),
+    ("varlen keys sliced at the query offsets", "ks = np.ascontiguousarray(kb[ck[s]:ck[s + 1]]",
+     "ks = np.ascontiguousarray(kb[cq[s]:cq[s] + Lk]", "oracle.py"),
+    ("varlen output rows not transposed back", "o.reshape(Hq, Lq, d).transpose(1, 0, 2)",
+     "o.reshape(Lq, Hq, d)", "oracle.py"),
+    ("varlen causal offset of the packed matrix", "o, l = attn_rows_lse(shape, mode, flags, bq, bk, causal,",
+     "o, l = attn_rows_lse(shape, mode, flags, bq, bk, causal and Lq == Lk,", "oracle.py"),
 ]
 
 
@@ -109,9 +116,9 @@ def _copy_oracle(dst, mutation=None):
     for f in ("__init__.py", "oracle.py", "sage_oracle.c", "sage_oracle.h"):
         shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(pkg, f))
     if mutation is not None:
-        src = os.path.join(pkg, "sage_oracle.c")
+        old, new = mutation[:2]
+        src = os.path.join(pkg, mutation[2] if len(mutation) > 2 else "sage_oracle.c")
         text = open(src).read()
-        old, new = mutation
         assert text.count(old) == 1, old
         open(src, "w").write(text.replace(old, new))
     # build the copy here, so that the subprocess only loads it
@@ -137,7 +144,7 @@ def _check(tmp, name, mutation):
 def test_unmutated_copy_passes_and_every_planted_mistake_fails_a_pin(tmp_path):
     """All copies built and run in parallel (one subprocess each)."""
     from concurrent.futures import ThreadPoolExecutor
-    jobs = [None] + [(old, new) for _, old, new in MUTATIONS]
+    jobs = [None] + [m[1:] for m in MUTATIONS]
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         results = list(ex.map(lambda a: _check(str(tmp_path), a[0], a[1]), enumerate(jobs)))
     clean = results[0]
