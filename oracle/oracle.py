@@ -23,6 +23,7 @@ SMOOTH_K, SMOOTH_Q, SMOOTH_V = 1, 2, 4
 P_DIRECT = 8  # NVFP4 ablation: phi on P~ directly (no level-1 scale)
 Q_PER_TOKEN = 0x10  # one Q scale per query row (INT8 / E4M3 modes)
 EXACT_QK, EXACT_PV = 0x100, 0x200
+EXACT_BWD = 0x400  # backward: P, dO, dS unquantized
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,9 @@ def lib():
             L.orc_attn_rows.restype = i32
             L.orc_attn_rows_lse.argtypes = L.orc_attn_rows.argtypes + [vp]
             L.orc_attn_rows_lse.restype = i32
+            L.orc_sagebwd_backward.argtypes = [C.POINTER(_Shape), i32, i32, i32, i32, dbl, vp, vp,
+                                               C.POINTER(_Quant), vp, vp, vp, vp, vp, vp, vp]
+            L.orc_sagebwd_backward.restype = i32
             L.orc_attn_exact_rows.argtypes = [C.POINTER(_Shape), i32, dbl, vp, vp, vp, vp, i64, vp]
             L.orc_attn_exact_rows.restype = i32
             _lib = L
@@ -254,6 +258,26 @@ def attn_rows_lse(shape, mode, flags, bq, bk, causal, sm_scale, q, k, v, qz: Qua
     if rc:
         raise OracleError("orc_attn_rows_lse rc=%d" % rc)
     return out, lse
+
+
+def sagebwd_backward(shape, flags, bq, bk, causal, sm_scale, q, k, v, qz: Quant, o, dout, lse):
+    """(dq, dk, dv) fp64 of the SageBwd backward; o fp64 [B,Hq,N,d] and lse fp64
+    [B,Hq,N] from the forward, dout bf16 [B,Hq,N,d]; see sage_oracle.h."""
+    B, Hq, Hkv, N, M, d = shape
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    assert o.size == B * Hq * N * d and lse.size == B * Hq * N and db.size == o.size
+    dq = np.zeros((B, Hq, N, d), np.float64)
+    dk = np.zeros((B, Hkv, M, d), np.float64)
+    dv = np.zeros((B, Hkv, M, d), np.float64)
+    st = qz._struct()
+    rc = lib().orc_sagebwd_backward(C.byref(_shape(*shape)), flags, bq, bk, int(bool(causal)),
+                                    float(sm_scale), _p(qb), _p(kb), C.byref(st), _p(vb), _p(o), _p(db),
+                                    _p(lse), _p(dq), _p(dk), _p(dv))
+    if rc:
+        raise OracleError("orc_sagebwd_backward rc=%d" % rc)
+    return dq, dk, dv
 
 
 def attn_exact_rows(shape, causal, sm_scale, q, k, v, rows) -> np.ndarray:

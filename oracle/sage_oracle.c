@@ -665,3 +665,178 @@ int orc_attn_exact_rows(const orc_shape *s, int causal, double sm_scale, const u
   free(sc);
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* SageBwd backward                                                     */
+/* ------------------------------------------------------------------ */
+
+/* INT8 per-block code of a value in fp64 against an fp64 scale (P and dS are
+ * formed inside the backward, not in a binary32 pre-pass): round half to
+ * even, clamp to +-127, 0 when the block is all zero. */
+static double int8_code64(double x, double scale) {
+  double r;
+  if (scale == 0.0) return 0.0;
+  r = nearbyint(x / scale);
+  if (r > 127.0) r = 127.0;
+  if (r < -127.0) r = -127.0;
+  return r;
+}
+
+int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int causal, double sm_scale,
+                         const uint16_t *q, const uint16_t *k, const orc_quant *qz, const uint16_t *v,
+                         const double *o, const uint16_t *dout, const double *lse, double *dq,
+                         double *dk, double *dv) {
+  const int B = s->B, Hq = s->Hq, Hkv = s->Hkv, N = s->N, M = s->M, d = s->d;
+  const int64_t Tm = cdiv(N, bq), Tn = cdiv(M, bk);
+  const int exact = (flags & ORC_EXACT_BWD) != 0;
+  int8_t *doc = NULL;   /* dO codes of one head [N][d] */
+  float *dos = NULL;    /* dO block scales of one head [Tm] */
+  double *Dr = NULL;    /* D_r = rowsum(dO o O) of one head [N] */
+  double *P = NULL, *dS = NULL, *Qd = NULL, *Kd = NULL;
+  int64_t n;
+  int b, h, rc = check_shape(s, ORC_SAGEBWD_I8, bq, bk);
+  if (rc) return rc;
+  if (causal && N > M) return ORC_ERR_ARG;
+
+  doc = (int8_t *)malloc((size_t)N * d);
+  dos = (float *)malloc(sizeof(float) * (size_t)Tm);
+  Dr = (double *)malloc(sizeof(double) * (size_t)N);
+  P = (double *)malloc(sizeof(double) * (size_t)bq * bk);
+  dS = (double *)malloc(sizeof(double) * (size_t)bq * bk);
+  Qd = (double *)malloc(sizeof(double) * (size_t)bq * d); /* deq(Q^_i) rows */
+  Kd = (double *)malloc(sizeof(double) * (size_t)bk * d); /* deq(K^_j) rows */
+  if (!doc || !dos || !Dr || !P || !dS || !Qd || !Kd) {
+    rc = ORC_ERR_ARG;
+    goto done;
+  }
+  n = (int64_t)B * Hq * N * d;
+  for (int64_t i = 0; i < n; ++i)
+    if (!in_range(bf16f(dout[i]))) {
+      rc = ORC_ERR_RANGE;
+      goto done;
+    }
+  memset(dq, 0, sizeof(double) * (size_t)n);
+  n = (int64_t)B * Hkv * M * d;
+  memset(dk, 0, sizeof(double) * (size_t)n);
+  memset(dv, 0, sizeof(double) * (size_t)n);
+
+  for (b = 0; b < B; ++b)
+    for (h = 0; h < Hq; ++h) {
+      const int64_t bh = (int64_t)b * Hq + h;
+      const int64_t hk = (int64_t)b * Hkv + h / (Hq / Hkv);
+      const uint16_t *dO = dout + bh * N * d;
+      const float *kbar = qz->kbar + hk * d;
+      int64_t i, j;
+      int r, c, e;
+
+      /* dO^: per-block INT8 over each bq-row block, binary32, as Q in the
+       * forward (a pre-pass quantizer) */
+      for (i = 0; i < Tm; ++i) {
+        const int r0 = (int)(i * bq), r1 = (int)((i + 1) * bq < N ? (i + 1) * bq : N);
+        float amax = 0.0f;
+        for (r = r0; r < r1; ++r)
+          for (e = 0; e < d; ++e)
+            if (fabsf(bf16f(dO[(int64_t)r * d + e])) > amax) amax = fabsf(bf16f(dO[(int64_t)r * d + e]));
+        dos[i] = orc_int8_scale(amax);
+        for (r = r0; r < r1; ++r)
+          for (e = 0; e < d; ++e)
+            doc[(int64_t)r * d + e] = (int8_t)orc_int8_code(bf16f(dO[(int64_t)r * d + e]), dos[i]);
+      }
+      /* D_r = sum_e dO[r,e] O[r,e] */
+      for (r = 0; r < N; ++r) {
+        double acc = 0.0;
+        for (e = 0; e < d; ++e) acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * o[(bh * N + r) * d + e];
+        Dr[r] = acc;
+      }
+
+      for (j = 0; j < Tn; ++j) {
+        const int t0 = (int)(j * bk), nk = (int)((j + 1) * bk < M ? bk : M - j * bk);
+        for (c = 0; c < nk; ++c) deq_k_row(s, ORC_SAGEBWD_I8, flags, bk, k, qz, hk, t0 + c, Kd + (int64_t)c * d);
+
+        for (i = 0; i < Tm; ++i) {
+          const int r0 = (int)(i * bq), nq = (int)((i + 1) * bq < N ? bq : N - i * bq);
+          const float *qbar = qz->qbar + (bh * Tm + i) * d;
+          double pmax = 0.0, smax = 0.0, sP, sdS;
+
+          for (r = 0; r < nq; ++r) deq_q_row(s, ORC_SAGEBWD_I8, flags, bq, q, qz, bh, r0 + r, Qd + (int64_t)r * d);
+
+          /* S_ij recomputed as in the forward, P_ij = exp(S - lse) */
+          for (r = 0; r < nq; ++r)
+            for (c = 0; c < bk; ++c) {
+              double pv = 0.0;
+              if (c < nk && visible(causal, r0 + r, t0 + c, N, M)) {
+                double s0 = 0.0, ds = 0.0;
+                for (e = 0; e < d; ++e) s0 += Qd[(int64_t)r * d + e] * Kd[(int64_t)c * d + e];
+                if (flags & ORC_SMOOTH_Q)
+                  for (e = 0; e < d; ++e) ds += (double)qbar[e] * Kd[(int64_t)c * d + e];
+                pv = exp((s0 + ds) * sm_scale - lse[bh * N + r0 + r]);
+              }
+              P[r * bk + c] = pv;
+              if (pv > pmax) pmax = pv;
+            }
+
+          /* dV_j += P^T dO, P^ per tile, dO^ per block */
+          sP = pmax / 127.0;
+          for (c = 0; c < nk; ++c)
+            for (r = 0; r < nq; ++r) {
+              const double pq = exact ? P[r * bk + c] : int8_code64(P[r * bk + c], sP) * sP;
+              if (pq == 0.0) continue;
+              for (e = 0; e < d; ++e) {
+                const double g = exact ? orc_bf16_decode(dO[(int64_t)(r0 + r) * d + e])
+                                       : (double)doc[(int64_t)(r0 + r) * d + e] * (double)dos[i];
+                dv[(hk * M + t0 + c) * d + e] += pq * g;
+              }
+            }
+
+          /* dP = dO V^T unquantized; dS = P o (dP - D) */
+          for (r = 0; r < nq; ++r)
+            for (c = 0; c < bk; ++c) {
+              double dp = 0.0, x;
+              if (P[r * bk + c] == 0.0) {
+                dS[r * bk + c] = 0.0;
+                continue;
+              }
+              for (e = 0; e < d; ++e)
+                dp += orc_bf16_decode(dO[(int64_t)(r0 + r) * d + e]) *
+                      orc_bf16_decode(v[(hk * M + t0 + c) * d + e]);
+              x = P[r * bk + c] * (dp - Dr[r0 + r]);
+              dS[r * bk + c] = x;
+              if (fabs(x) > smax) smax = fabs(x);
+            }
+
+          /* dQ_i += (dS^ K^) s_dS + rowsum(dS) k_bar^T and
+           * dK_j += (dS^T Q^) s_dS + colsum(dS) q_bar_i^T: the INT8 products
+           * take the smoothed operands, the smoothing corrections the
+           * unquantized dS (in higher precision); k_bar and q_bar are 0 when K
+           * or Q was not smoothed */
+          sdS = smax / 127.0;
+          for (r = 0; r < nq; ++r)
+            for (c = 0; c < nk; ++c) {
+              const double gx = dS[r * bk + c];
+              const double g = exact ? gx : int8_code64(gx, sdS) * sdS;
+              if (gx == 0.0) continue;
+              for (e = 0; e < d; ++e) {
+                dq[(bh * N + r0 + r) * d + e] += g * Kd[(int64_t)c * d + e] + gx * (double)kbar[e];
+                dk[(hk * M + t0 + c) * d + e] += g * Qd[(int64_t)r * d + e] + gx * (double)qbar[e];
+              }
+            }
+        }
+      }
+    }
+
+  /* the scores were S * sm_scale: dQ and dK carry that factor */
+  n = (int64_t)B * Hq * N * d;
+  for (int64_t i = 0; i < n; ++i) dq[i] *= sm_scale;
+  n = (int64_t)B * Hkv * M * d;
+  for (int64_t i = 0; i < n; ++i) dk[i] *= sm_scale;
+
+done:
+  free(doc);
+  free(dos);
+  free(Dr);
+  free(P);
+  free(dS);
+  free(Qd);
+  free(Kd);
+  return rc;
+}

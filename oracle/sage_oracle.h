@@ -68,6 +68,7 @@ extern "C" {
 /* oracle-only switches used by the pins: replace a quantizer by identity */
 #define ORC_EXACT_QK 0x100 /* S from the unrounded smoothed Q, K in fp64 */
 #define ORC_EXACT_PV 0x200 /* R from unquantized P~ and unquantized V' in fp64 */
+#define ORC_EXACT_BWD 0x400 /* backward: P, dO and dS unquantized in fp64 */
 
 /* error codes */
 #define ORC_OK 0
@@ -152,6 +153,31 @@ int orc_attn_rows_lse(const orc_shape *s, int mode, int flags, int bq, int bk, i
                       double sm_scale, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const orc_quant *qz, const int64_t *rows, int64_t nrows, double *out,
                       double *lse);
+
+/* SageBwd backward (SageAttention3 summary, "SageBwd Backward Pass and the
+ * Critical dOV^T Decision", eq. 8 and Algorithm 3), key blocks j outer, query
+ * blocks i inner:
+ *   S_ij recomputed from the forward's Q^, K^ (and dS when Q was smoothed),
+ *   P_ij = exp(S_ij sm_scale - lse_i);
+ *   dV_j += (P^_ij^T dO^_i) s_P s_dO    P per bq x bk tile, dO per bq-row block,
+ *                                        both INT8 per-block (max / 127);
+ *   dP_ij = dO_i V_j^T                   unquantized (bf16 operands, fp64 here);
+ *   dS_ij = P_ij o (dP_ij - D_i), D_i = rowsum(dO_i o O_i), INT8 per tile;
+ *   dQ_i += (dS^_ij K^_j) s_dS s_K,j + rowsum(dS_ij) k_bar^T
+ *   dK_j += (dS^_ij^T Q^_i) s_dS s_Q,i [+ colsum(dS_ij) q_bar_i^T when Q was
+ *                                        smoothed] -- the smoothing corrections
+ *                                        from the unquantized dS;
+ *   dQ, dK times sm_scale at the end.
+ * qz is the forward's quantization (mode ORC_SAGEBWD_I8 or ORC_Q8_PV8, whose Q
+ * and K codes are the same); o [B,Hq,N,d] the forward output and lse [B,Hq,N]
+ * its statistics; dout bf16 [B,Hq,N,d].  Outputs fp64: dq [B,Hq,N,d],
+ * dk and dv [B,Hkv,M,d] (query heads of a kv head summed).  Flags: the
+ * forward's smoothing flags, ORC_EXACT_QK (unquantized smoothed Q and K) and
+ * ORC_EXACT_BWD. */
+int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int causal, double sm_scale,
+                         const uint16_t *q, const uint16_t *k, const orc_quant *qz, const uint16_t *v,
+                         const double *o, const uint16_t *dout, const double *lse, double *dq,
+                         double *dk, double *dv);
 
 /* Plain softmax(Q K^T sm_scale) V in fp64 on the bf16 inputs, same masks. */
 int orc_attn_exact_rows(const orc_shape *s, int causal, double sm_scale, const uint16_t *q,

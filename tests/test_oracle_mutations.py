@@ -13,7 +13,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TESTS = [os.path.join(ROOT, "tests", f) for f in
-         ("test_oracle_codecs.py", "test_oracle_attention.py", "test_oracle_sagebwd.py", "test_oracle_varlen.py")]
+         ("test_oracle_codecs.py", "test_oracle_attention.py", "test_oracle_sagebwd.py", "test_oracle_varlen.py",
+          "test_oracle_sagebwd_backward.py")]
 
 # (name, text in sage_oracle.c, replacement); each text occurs exactly once.  The
 # packed-sequence composition lives in oracle.py: those entries name that file.
@@ -101,6 +102,21 @@ MUTATIONS = [
     ("SageBwd output keeps the 448 / delta_V epilogue", "(mode == ORC_Q8_PV8 || mode == ORC_QF8_PV8))",
      "mode != ORC_NVFP4)"),
     ("lse without the log", "if (lse) lse[ri] = m + log(l);", "if (lse) lse[ri] = m + l;"),
+    # SageBwd backward
+    ("backward dS without D_i", "x = P[r * bk + c] * (dp - Dr[r0 + r]);", "x = P[r * bk + c] * dp;"),
+    ("backward dS without P", "x = P[r * bk + c] * (dp - Dr[r0 + r]);", "x = (dp - Dr[r0 + r]);"),
+    ("backward D_i from dO alone", "acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * o[(bh * N + r) * d + e];",
+     "acc += orc_bf16_decode(dO[(int64_t)r * d + e]);"),
+    ("backward P not normalised by lse", "pv = exp((s0 + ds) * sm_scale - lse[bh * N + r0 + r]);",
+     "pv = exp((s0 + ds) * sm_scale);"),
+    ("backward s_P divisor", "sP = pmax / 127.0;", "sP = pmax / 128.0;"),
+    ("backward s_dS divisor", "sdS = smax / 127.0;", "sdS = smax / 128.0;"),
+    ("backward dO scale not multiplied back", "* (double)dos[i];", ";"),
+    ("backward dK without sm_scale", "for (int64_t i = 0; i < n; ++i) dk[i] *= sm_scale;", ""),
+    ("backward dQ without sm_scale", "for (int64_t i = 0; i < n; ++i) dq[i] *= sm_scale;", ""),
+    ("backward k_bar correction dropped", "+ gx * (double)kbar[e];", ";"),
+    ("backward k_bar correction from the INT8 dS", "+ gx * (double)kbar[e];", "+ g * (double)kbar[e];"),
+    ("backward q_bar correction dropped", "+ gx * (double)qbar[e];", ";"),
     ("varlen keys sliced at the query offsets", "ks = np.ascontiguousarray(kb[ck[s]:ck[s + 1]]",
      "ks = np.ascontiguousarray(kb[cq[s]:cq[s] + Lk]", "oracle.py"),
     ("varlen output rows not transposed back", "o.reshape(Hq, Lq, d).transpose(1, 0, 2)",
