@@ -279,7 +279,8 @@ def workload_config(cfg):
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "N": cfg.N, "M": cfg.M, "d": cfg.d,
             "causal": cfg.causal, "quant_mode": ["int8_qk_fp8_pv", "fp8_qk_fp8_pv", "nvfp4"][cfg.mode],
             "flags": {"smooth_k": bool(cfg.flags & 1), "smooth_q": bool(cfg.flags & 2),
-                      "smooth_v": bool(cfg.flags & 4)},
+                      "smooth_v": bool(cfg.flags & 4), "p_direct": bool(cfg.flags & 8),
+                      "q_per_token": bool(cfg.flags & 0x10)},
             "bq": cfg.bq, "bk": cfg.bk,
             "l2": "inputs larger than L2 (%.0f MB of bf16 Q/K/V per step), no flush" % (
                 2.0 * cfg.d * (cfg.B * cfg.Hq * cfg.N + 2 * cfg.B * cfg.Hkv * cfg.M) / 1e6),
@@ -437,6 +438,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     ap.add_argument("--heads", type=int, default=0, help="override Hq (Hkv scaled to keep the group size)")
+    ap.add_argument("--flags", type=lambda x: int(x, 0), default=None,
+                    help="override the workload's flags (ablations: 1 smooth K, 2 smooth Q, 4 smooth V, "
+                         "8 direct P~ in the NVFP4 mode, 0x10 per-token Q scales)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -446,6 +450,8 @@ def main():
         cfg = cfg.with_(bk=args.bk)
     if args.batch:
         cfg = cfg.with_(B=args.batch)
+    if args.flags is not None:
+        cfg = cfg.with_(flags=args.flags)
     if args.heads:
         g = cfg.Hq // cfg.Hkv
         if args.heads % g:

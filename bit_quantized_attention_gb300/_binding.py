@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(HERE, "libsage.so")
 
 SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4 = 0, 1, 2
 SAGE_SMOOTH_K, SAGE_SMOOTH_Q, SAGE_SMOOTH_V = 1, 2, 4
+SAGE_P_DIRECT, SAGE_Q_PER_TOKEN = 8, 0x10
 STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3: "SAGE_ERR_WORKSPACE",
           4: "SAGE_ERR_RANGE", 5: "SAGE_ERR_TIMEOUT", 6: "SAGE_ERR_CUDA"}
 
@@ -41,7 +42,7 @@ class Shape(C.Structure):
 class WsLayout(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
                                           "qsf", "ksf", "vsf", "stats", "status", "total")] + \
-               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")]
+               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")] + [("dqt", C.c_size_t)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

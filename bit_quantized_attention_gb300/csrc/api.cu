@@ -89,13 +89,22 @@ sage_status sage_workspace_layout(const sage_shape *shape, int quant_mode, int b
   return request_layout(shape, quant_mode, bq, bk, out);
 }
 
+// Flag bits: unknown bits are an invalid argument; per-token Q scales exist in
+// the INT8 / FP8 modes only (NVFP4 scales Q per 1x16 block already).
+static sage_status check_flags(int quant_mode, int flags) {
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V | SAGE_P_DIRECT | SAGE_Q_PER_TOKEN))
+    return SAGE_ERR_INVALID_ARG;
+  if ((flags & SAGE_Q_PER_TOKEN) && quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  return SAGE_OK;
+}
+
 sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags, int bq, int bk, const void *q,
                               const void *k, const void *v, void *workspace, size_t workspace_bytes,
                               sage_stream_t stream) {
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
@@ -106,7 +115,8 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
 // the causal alignment, and the NVFP4 kernel's 128-key tiles.
 static sage_status check_attn_args(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags,
                                    int bk) {
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  sage_status st = check_flags(quant_mode, flags);
+  if (st != SAGE_OK) return st;
   if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
   if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
   if (quant_mode == SAGE_NVFP4 && bk != 128) return SAGE_ERR_UNSUPPORTED;
@@ -118,7 +128,7 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!workspace || !o || !aligned16(o) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
   st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
@@ -134,7 +144,7 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;

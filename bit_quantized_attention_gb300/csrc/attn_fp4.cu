@@ -7,6 +7,7 @@
 //   m_ij  = max(m_i,j-1, rowmax S_ij sm_scale),   P~ = exp(S sm_scale - m_ij)
 //   l_ij  = e^(m_i,j-1 - m_ij) l + rowsum P~        (unquantized P~)
 //   s_P1  = rowmax P~_ij / (448 * 6) = exp(rowmax S_ij sm_scale - m_ij) / 2688
+//           (1 under the direct-P~ ablation, which quantizes P~ itself)
 //   P2    = P~ / s_P1;  (s_P2, P2^) = phi(P2) over 1x16 blocks of keys
 //   R_ij  = FP4MMA(P2^, s_P2, V^_j, s_V)            tile partial, this tile only
 //   O_ij  = e^(m_i,j-1 - m_ij) O_i,j-1 + s_P1 R_ij  FP32 running output
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int last_row = min(p.N, row0 + 128) - 1;
   const int T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
   const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
+  const bool direct = (p.flags & SAGE_P_DIRECT) != 0;  // phi on P~ itself (ablation)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -465,8 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m, mt);
       const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
       const bool any = mt != -INFINITY;
-      const float sp1 = any ? ex2_approx(mt - m_new) * (1.0f / 2688.0f) : 0.0f;
-      const float f = (any && mh != -INFINITY) ? ex2_approx(mht - mt) * 2688.0f : 0.0f;  // P2 = e f
+      // direct P~ (ablation): s_P1 = 1 and P2 = P~ = e exp2(m_half - m_new)
+      const float sp1 = !any ? 0.0f : direct ? 1.0f : ex2_approx(mt - m_new) * (1.0f / 2688.0f);
+      const float f = (!any || mh == -INFINITY) ? 0.0f
+                      : direct                 ? ex2_approx(mht - m_new)
+                                               : ex2_approx(mht - mt) * 2688.0f;  // P2 = e f
       uint8_t *prow = sP + bb * C::P_BYTES;
       uint32_t scw = 0;
       uint32_t pk[8];

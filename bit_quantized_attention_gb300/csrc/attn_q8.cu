@@ -5,6 +5,7 @@
 // §3.4 "The Complete Algorithm"; "Quantization for Attention, in depth",
 // "The datapath and its quantize points"):
 //   S_ij  = delta_Q delta_K,j (Q^_i K^_j^T) + dS_ij,  dS_ij = q_bar_i deq(K^_j)^T
+//           (delta_Q one per query block, or one per row with per-token Q scales)
 //   m_ij  = max(m_i,j-1, rowmax S_ij * sm_scale)
 //   P~_ij = exp(S_ij sm_scale - m_ij),  l_ij = e^(m_i,j-1 - m_ij) l + rowsum P~
 //   P^_ij = e4m3(448 P~_ij)                          (static scale 1/448)
@@ -116,6 +117,7 @@ struct AttnParams {
   int items;      // B * Hq * Tm work items (one query block of one head each)
   float sm_log2;  // sm_scale * log2(e)
   const float *dq, *qbar, *dk, *dv, *vm;
+  const float *dqt;  // per-row Q scales [B*Hq*N_pad] (SAGE_Q_PER_TOKEN)
   __nv_bfloat16 *o;
   int *status;
   long long spin;
@@ -666,7 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; !stop && blockIdx.x + n * G < p.items; ++n) {
       const Item it = item_of(p, blockIdx.x + n * G, BK);
       const int diag = it.row0 + r + p.M - p.N;  // last key visible to this row (causal)
-      const float dq = p.dq[(size_t)it.bh * p.Tm + it.qi];
+      // this row's Q scale: its own (per-token Q) or its block's
+      const float dq = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
+                                                    : p.dq[(size_t)it.bh * p.Tm + it.qi];
       float m = -INFINITY, l = 0.0f;
       const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
       float dk_next = dkr[0];
@@ -816,6 +820,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.flags = flags;
   p.sm_log2 = sm_scale * 1.4426950408889634f;
   p.dq = (const float *)(w + L.dq);
+  p.dqt = (const float *)(w + L.dqt);
   p.qbar = (const float *)(w + L.qbar);
   p.dk = (const float *)(w + L.dk);
   p.dv = (const float *)(w + L.dv);

@@ -77,6 +77,7 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   L->vsf = take(fp4 ? (size_t)(B * Hkv * cdiv(d, 128) * 128 * (M_pad / 16)) : 0);
   L->stats = take(stats_bytes(*s));
   L->status = take(16);
+  L->dqt = take((size_t)(B * Hq * N_pad * 4));
   L->total = off;
   L->N_pad = (int)N_pad;
   L->M_pad = (int)M_pad;

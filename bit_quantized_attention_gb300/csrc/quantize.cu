@@ -297,6 +297,7 @@ struct QuantArgs {
   int mode, flags;
   uint8_t *qhat, *khat, *vhat;
   float *dq, *qbar, *dk, *kbar, *dv, *vm;
+  float *dqt;  // per-row Q scales (SAGE_Q_PER_TOKEN)
   StatsView st;
   int *status;
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
@@ -384,6 +385,9 @@ __device__ __forceinline__ void encode8(const float (&f)[8], const float (&mu)[8
 // One block of `rows` rows (<= 128) of a [*, D] bf16 matrix: optional
 // per-block mean (fixed point over the valid rows) or a given mean, then the
 // per-block absmax scale and the codes.  Rows past `valid_rows` get code 0.
+// kPerRow: each row takes its own scale, max over its channels of
+// |fl(x - mu)| / 127 (or / 448), written to row_delta_out[r] (0 past
+// valid_rows), and *delta_out is 0.
 // The absmax max_r |fl(x_r - mu)| of a channel is taken from the channel's
 // extremes (rounded subtraction is monotone), which packed bf16 min / max
 // track exactly; they also carry the range check (NaN propagates).
@@ -395,10 +399,11 @@ __host__ __device__ constexpr int qk_pool_bytes() { return (kThreads / (D / 8)) 
 template <int D>
 __host__ __device__ constexpr int v_pool_bytes() { return 3 * D * 4 + D * 33 * 4; }
 
-template <int D, bool kInt8>
+template <int D, bool kInt8, bool kPerRow = false>
 __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
                             const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
-                            float *mean_out, int *status, int site, unsigned char *pool) {
+                            float *mean_out, int *status, int site, unsigned char *pool,
+                            float *row_delta_out = nullptr) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
   long long (*ssum)[D] = reinterpret_cast<long long (*)[D]>(pool);
   float *smean = reinterpret_cast<float *>(pool + RPP * D * 8);
@@ -463,10 +468,38 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
     }
     if (bad) raise_status(status, SAGE_ERR_RANGE, site);
   }
+  constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
+  if constexpr (kPerRow) {
+    // per-row scales: the VPR threads of a row are consecutive lanes of one
+    // warp (VPR divides 32), so the row maximum is a shuffle reduction; every
+    // lane runs every shuffle
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int r = rr + p * RPP;
+      float f[8];
+      unpack_bf16x8(x[p], f);
+      float am = 0.0f;
+      if (r < valid_rows) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(f[e], mu[e])));
+      }
+#pragma unroll
+      for (int o = 1; o < VPR; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float dr = __fdiv_rn(am, kInt8 ? 127.0f : 448.0f);
+      const float rc = __frcp_rn(dr);
+      if (r < rows) {
+        encode8<kInt8>(f, mu, dr, rc, r < valid_rows && dr != 0.0f, dst + ((size_t)r * D + vc * 8) * CB);
+        if (vc == 0) row_delta_out[r] = dr;
+      }
+    }
+    if (threadIdx.x == 0) *delta_out = 0.0f;
+    if (mean_out)
+      for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
+    return;
+  }
   amax = block_max(amax, red);
   const float delta = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
   const float rcp = __frcp_rn(delta);
-  constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
@@ -480,7 +513,9 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
     for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
 }
 
-template <int D, bool kInt8>
+// kPerRow: per-row Q scales (SAGE_Q_PER_TOKEN), an instance of its own so that
+// the per-block instances keep their register allocation
+template <int D, bool kInt8, bool kPerRow>
 __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArgs a) {
   constexpr int CB = kInt8 ? 2 : 1;
   constexpr int kPool = qk_pool_bytes<D>() > v_pool_bytes<D>() ? qk_pool_bytes<D>() : v_pool_bytes<D>();
@@ -493,9 +528,10 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     const int valid = max(0, min(128, a.N - r0));
     const bool smooth = (a.flags & SAGE_SMOOTH_Q) != 0;
     float *qbar = a.qbar + ((size_t)bh * a.Tm + i) * D;
-    quant_block<D, kInt8>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0, nullptr,
-                          a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i, qbar,
-                          a.status, 3, pool);
+    quant_block<D, kInt8, kPerRow>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0,
+                                   nullptr, a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB,
+                                   a.dq + (size_t)bh * a.Tm + i, qbar, a.status, 3, pool,
+                                   a.dqt + (size_t)bh * a.N_pad + r0);
     return;
   }
   cta -= a.nq;
@@ -838,6 +874,7 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.khat = (uint8_t *)(w + L.khat);
   a.vhat = (uint8_t *)(w + L.vhat);
   a.dq = (float *)(w + L.dq);
+  a.dqt = (float *)(w + L.dqt);
   a.qbar = (float *)(w + L.qbar);
   a.dk = (float *)(w + L.dk);
   a.kbar = (float *)(w + L.kbar);
@@ -849,18 +886,12 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.nk = s.B * s.Hkv * L.Tn;
   const int nv = s.B * s.Hkv * (L.M_pad / 128);
   const unsigned grid = (unsigned)(a.nq + a.nk + nv);
-  const bool i8 = (mode == SAGE_Q8_PV8);
-  if (s.d == 64) {
-    if (i8)
-      quantize_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
-  } else {
-    if (i8)
-      quantize_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
-  }
+  const bool i8 = (mode == SAGE_Q8_PV8), pr = (flags & SAGE_Q_PER_TOKEN) != 0;
+  auto kern = s.d == 64 ? (i8 ? (pr ? quantize_kernel<64, true, true> : quantize_kernel<64, true, false>)
+                              : (pr ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>))
+                        : (i8 ? (pr ? quantize_kernel<128, true, true> : quantize_kernel<128, true, false>)
+                              : (pr ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>));
+  kern<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 

@@ -67,7 +67,16 @@ enum {
 enum {
   SAGE_SMOOTH_K = 1, /* subtract mean(K) over tokens (always exact) */
   SAGE_SMOOTH_Q = 2, /* subtract the per-block mean of Q, add dS back */
-  SAGE_SMOOTH_V = 4  /* subtract mean(V) over tokens, add it back to O */
+  SAGE_SMOOTH_V = 4, /* subtract mean(V) over tokens, add it back to O */
+  /* ablation of the NVFP4 mode (SageAttention3 summary §3.4, "Two-Level
+   * Quantization for P"): phi applied to P~ itself, no level-1 scale; accepted
+   * and without effect in modes 0 and 1, whose P~ quantization is direct */
+  SAGE_P_DIRECT = 8,
+  /* one Q scale per query row instead of one per 128-row block (modes 0, 1);
+   * q_bar stays per block.  Per-thread / per-token granularity is what the
+   * SageAttention summaries trade against the MMA layout; on tcgen05 each
+   * softmax thread owns a whole row of S, so it costs the kernel one load */
+  SAGE_Q_PER_TOKEN = 0x10
 };
 
 typedef struct {
@@ -91,11 +100,13 @@ typedef struct {
  *   qsf, ksf, vsf         E4M3 block scales (mode 2), layouts in the .cu file
  *   stats                 reduction scratch of sage_quantize_qkv
  *   status                int32[4]: code, site, detail, spare
+ *   dqt    [B*Hq*N_pad]   fp32 per-row Q scale (SAGE_Q_PER_TOKEN; 0 on pad rows)
  * N_pad = N rounded up to 128, M_pad = M rounded up to 128, Tm = N_pad/bq,
  * Tn = ceil(M/bk). */
 typedef struct {
   size_t qhat, dq, qbar, khat, dk, kbar, vhat, dv, vm, qsf, ksf, vsf, stats, status, total;
   int N_pad, M_pad, Tm, Tn;
+  size_t dqt;
 } sage_ws_layout;
 
 /* Workspace size in bytes for a shape and mode; 0 if the request is invalid

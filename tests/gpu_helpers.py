@@ -39,6 +39,7 @@ def read_workspace(ws, mode: int) -> dict:
         kbar=f32("kbar", B * Hkv * d).reshape(B, Hkv, d),
         dv=f32("dv", B * Hkv * d).reshape(B, Hkv, d),
         vm=f32("vm", B * Hkv * d).reshape(B, Hkv, d),
+        dqt=f32("dqt", B * Hq * Np).reshape(B, Hq, Np)[:, :, :N],
         pad_q=_np(qraw).reshape(B, Hq, Np, d * cb)[:, :, N:],
         pad_v=vt_pad(ws, B, Hkv, d, Mp, M),
     )
@@ -140,6 +141,8 @@ def compare_codes(got: dict, ref, mode: int, flags: int):
     out["kbar"] = np.array_equal(bits(got["kbar"]), bits(ref.kbar))
     out["vm"] = np.array_equal(bits(got["vm"]), bits(ref.vm))
     out["qbar"] = np.array_equal(bits(got["qbar"]), bits(ref.qbar))
+    if flags & 0x10:  # per-token Q scales
+        out["dqt"] = np.array_equal(bits(got["dqt"]), bits(ref.dqt))
     out["qc"] = np.array_equal(qc, qc_ref)
     out["kc"] = np.array_equal(kc, kc_ref)
     out["vc"] = np.array_equal(vc, vc_ref)

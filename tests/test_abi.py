@@ -46,7 +46,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
         s = sage.Shape(*shp)
         L = sage.sage_workspace_layout(s, mode, 128, bk).as_dict()
         offs = [L[k] for k in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm", "qsf", "ksf",
-                               "vsf", "stats", "status", "total")]
+                               "vsf", "stats", "status", "dqt", "total")]
         assert all(o % 1024 == 0 for o in offs)
         assert offs == sorted(offs)
         assert L["N_pad"] % 128 == 0 and L["N_pad"] >= shp[3]
@@ -54,6 +54,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
         assert L["Tn"] == -(-shp[4] // bk)
         code_b = 2 if mode == 0 else 1
         assert L["dq"] - L["qhat"] >= shp[0] * shp[1] * L["N_pad"] * shp[5] * code_b
+        assert L["total"] - L["dqt"] >= shp[0] * shp[1] * L["N_pad"] * 4     # one Q scale per row
         assert sage.sage_workspace_bytes(s, mode, 128, bk) == L["total"]
 
 
@@ -117,6 +118,8 @@ def test_host_call_checks_everything_before_its_first_copy(sage):
     assert call(buf=C.c_void_p((1 << 30) + 512)) == 1                    # device buffer alignment
     assert call(n=need - 1) == 3                                          # too small
     assert call(flags=64) == 1                                            # unknown flag
+    assert call(mode=2, bk=128, flags=1 | 0x10, n=sage.lib.sage_host_buffer_bytes(C.byref(s), 2, 128, 128)) == 2
+    # (per-token Q scales are for the INT8 / FP8 modes)
     assert call(scale=0.0) == 1 and call(scale=float("nan")) == 1
     s2 = sage.Shape(1, 2, 2, 512, 256, 64)
     need2 = sage.lib.sage_host_buffer_bytes(C.byref(s2), 0, 128, 64)
