@@ -15,7 +15,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsage.so")
 
-SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4 = 0, 1, 2
+SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4, SAGE_SAGEBWD_I8 = 0, 1, 2, 3
 SAGE_SMOOTH_K, SAGE_SMOOTH_Q, SAGE_SMOOTH_V = 1, 2, 4
 SAGE_P_DIRECT, SAGE_Q_PER_TOKEN = 8, 0x10
 STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3: "SAGE_ERR_WORKSPACE",
@@ -42,7 +42,8 @@ class Shape(C.Structure):
 class WsLayout(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
                                           "qsf", "ksf", "vsf", "stats", "status", "total")] + \
-               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")] + [("dqt", C.c_size_t)]
+               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")] + \
+               [(n, C.c_size_t) for n in ("dqt", "dvb", "lse")]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -231,6 +232,16 @@ def sage_attn_host(shape: Shape, causal: bool, sm_scale: float, mode: int, flags
 
 def sage_status_str(code: int) -> str:
     return lib.sage_status_str(code).decode()
+
+
+def sage_lse(ws: Workspace) -> torch.Tensor:
+    """The per-row log-sum-exp the SageBwd forward (mode 3) wrote into the
+    workspace, ln sum_j exp(S_ij sm_scale), as a float32 view [B, Hq, N]."""
+    if ws.mode != SAGE_SAGEBWD_I8:
+        raise ValueError("the log-sum-exp is written by the SageBwd forward (mode 3) only")
+    s, L = ws.shape, ws.layout
+    t = ws.region("lse", s.B * s.Hq * L.N_pad * 4).view(torch.float32)
+    return t.view(s.B, s.Hq, L.N_pad)[:, :, :s.N]
 
 
 def sage_attn(q, k, v, causal: bool, sm_scale: float, mode: int = SAGE_Q8_PV8, flags: int = SAGE_SMOOTH_K,

@@ -73,22 +73,26 @@ constexpr float kLog2_448 = 8.807354922057604f;
 
 // kDsT: dS on the tensor core (Q smoothing with INT8 codes and 128-key tiles):
 // a 16-row tile of q_bar (fp16 hi / lo rows) per item parity in shared memory
-// and NB 16-column dS regions in TMEM
-template <int D, int BK, bool kQK16, bool kDsT = false>
+// and NB 16-column dS regions in TMEM.  kPV16: the SageBwd forward, P^ and V^
+// as INT8 codes held in fp16 (kind::f16 PV), with a per-row factor
+// s_P s_V,j per tile for the accumulation and the row statistics kept
+template <int D, int BK, bool kQK16, bool kDsT = false, bool kPV16 = false>
 struct Cfg {
   static constexpr int HALF = BK / 2;                    // keys per softmax warpgroup
   static constexpr int QK_EB = kQK16 ? 2 : 1;           // bytes per stored Q/K code
   static constexpr int ROWB = D * QK_EB;                 // bytes per Q/K row
   static constexpr int QK_SW = ROWB >= 128 ? 128 : 64;   // swizzle span of Q/K tiles
   static constexpr int QK_CHUNKS = ROWB / QK_SW;         // swizzle spans per row
-  static constexpr int PV_SW = BK >= 128 ? 128 : 64;     // swizzle span of P^ and V^T tiles
+  static constexpr int PV_EB = kPV16 ? 2 : 1;           // bytes per stored P^ / V^ code
+  static constexpr int PV_SW = BK * PV_EB >= 128 ? 128 : 64;  // swizzle span of P^ and V^T tiles
   static constexpr int Q_BYTES = 128 * ROWB;
   static constexpr int K_BYTES = BK * ROWB;
-  static constexpr int V_BYTES = D * BK;
-  static constexpr int P_BYTES = 128 * BK;
+  static constexpr int V_BYTES = D * BK * PV_EB;
+  static constexpr int P_BYTES = 128 * BK * PV_EB;
   static constexpr int QK_KSTEPS = ROWB / 32;            // one MMA consumes 32 bytes of K
-  static constexpr int PV_KSTEPS = BK / 32;
-  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + NB * BK /*dS*/ + 2 * D /*q_bar*/;
+  static constexpr int PV_KSTEPS = BK * PV_EB / 32;
+  static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + NB * BK /*dS*/ + 2 * D /*q_bar*/ +
+                                (kPV16 ? 2 * NB * 128 : 0) /*s_P s_V, final max*/;
   static constexpr int UB_BYTES = kDsT ? 16 * ROWB : 0;  // one q_bar tile (16 rows, K-major, swizzled)
   static constexpr int FIXED = Q_BYTES + NB * P_BYTES + 2 * UB_BYTES;
   static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
@@ -107,7 +111,9 @@ struct Cfg {
   static constexpr int SMEM_TOTAL = 1024 + FIXED + KST * K_BYTES + VST * V_BYTES + MISC;
   static constexpr uint32_t IDESC_QK =
       instr_desc(kFmtF32, kQK16 ? kFmtF16 : kFmtE4M3, kQK16 ? kFmtF16 : kFmtE4M3, BK, 128);
-  static constexpr uint32_t IDESC_PV = instr_desc(kFmtF32, kFmtE4M3, kFmtE4M3, D, 128);
+  static constexpr uint32_t IDESC_PV =
+      instr_desc(kFmtF32, kPV16 ? kFmtF16 : kFmtE4M3, kPV16 ? kFmtF16 : kFmtE4M3, D, 128);
+  static_assert(!kPV16 || (kQK16 && BK == 64), "SageBwd forward: INT8 codes, 64-key tiles");
   // dS^T = K^ (128 keys x d, A) x q_bar tile (16 x d, B): column 0 the hi row, 1 the lo row
   static constexpr uint32_t IDESC_DS = instr_desc(kFmtF32, kFmtF16, kFmtF16, 16, 128);
 };
@@ -118,6 +124,8 @@ struct AttnParams {
   float sm_log2;  // sm_scale * log2(e)
   const float *dq, *qbar, *dk, *dv, *vm;
   const float *dqt;  // per-row Q scales [B*Hq*N_pad] (SAGE_Q_PER_TOKEN)
+  const float *dvb;  // per-block V scales [B*Hkv*Tn] (SageBwd forward)
+  float *lse;        // per-row log-sum-exp [B*Hq*N_pad] (SageBwd forward)
   __nv_bfloat16 *o;
   int *status;
   long long spin;
@@ -187,15 +195,15 @@ __device__ __forceinline__ float qbar_dot_key(const uint8_t *kt, const float *qb
 }
 
 // kSmoothQ: Q smoothing on (dS added to the scores); its instances carry the dS
-// stream, the others none of its state
-template <int D, int BK, bool kQK16, bool kSmoothQ>
+// stream, the others none of its state.  kPV16: the SageBwd forward.
+template <int D, int BK, bool kQK16, bool kSmoothQ, bool kPV16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles);
   // otherwise the accumulation warpgroup takes it on CUDA cores
   constexpr bool kDsMma = kSmoothQ && kQK16 && BK == 128;
-  using C = Cfg<D, BK, kQK16, kDsMma>;
+  using C = Cfg<D, BK, kQK16, kDsMma, kPV16>;
   constexpr int KST = C::KST, VST = C::VST;
   constexpr int HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
@@ -210,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_mx = s_l + NB * 256;                      // [2 parities][2 halves][128]
   float *s_ds = s_mx + 4 * 128;                      // [NB][BK] dS of a tile, in t units
   float *s_qb = s_ds + NB * BK;                      // [2 item parities][D] q_bar of the dS stream
-  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_qb + 2 * D) + 7) & ~(uintptr_t)7);
+  float *s_w = s_qb + 2 * D;                         // [NB][128] s_P s_V,j of a tile (SageBwd)
+  float *s_mrow = s_w + (kPV16 ? NB * 128 : 0);      // [NB][128] running max at an item's last tile (SageBwd)
+  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_mrow + (kPV16 ? NB * 128 : 0)) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
   uint64_t *q_empty = q_full + 1;
   uint64_t *k_full = q_empty + 1;    // [KST]
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (v_more && gv < gk && (gv < VST || mbar_try_wait(&v_empty[gv % VST], ((gv / VST) - 1) & 1))) {
           const int s = gv % VST;
           mbar_expect_tx(&v_full[s], C::V_BYTES);
-          tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], vj * BK, vit.hkv * D);
+          tma_load_2d(sV + s * C::V_BYTES, &tm_v, &v_full[s], vj * BK * C::PV_EB, vit.hkv * D);
           ++gv;
           if (++vj == vit.T) {
             vj = 0;
@@ -445,7 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
               const uint64_t bd = smem_desc(v_base + s * C::V_BYTES + kk * 32, 8 * C::PV_SW,
                                             C::PV_SW == 128 ? kSwizzle128 : kSwizzle64);
-              mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
+              if (kPV16)
+                mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
+              else
+                mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_PV, kk > 0);
             }
             mma_commit(&r_full[b]);
             mma_commit(&v_empty[s]);
@@ -530,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float o[D];  // this thread's row of the FP32 running output
 #pragma unroll
       for (int c = 0; c < D; ++c) o[c] = 0.0f;
-      float lsum = 0.0f;
+      float lsum = 0.0f, mrow = 0.0f;
       for (int j = 0; j < it.T; ++j, ++gt) {
         const int b = gt % NB;
         while (kDsMma && d_more && dg < gt + 3) {
@@ -609,8 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float a = s_alpha[b * 128 + r];
-        if (j == it.T - 1) lsum = s_l[(b * 2 + 0) * 128 + r] + s_l[(b * 2 + 1) * 128 + r];
+        if (j == it.T - 1) {
+          lsum = s_l[(b * 2 + 0) * 128 + r] + s_l[(b * 2 + 1) * 128 + r];
+          if constexpr (kPV16) mrow = s_mrow[b * 128 + r];
+        }
         const float2 a2 = make_float2(a, a);
+        // SageBwd: R holds integer sums of code products; s_P s_V,j scales them
+        const float wv = kPV16 ? s_w[b * 128 + r] : 1.0f;
+        const float2 w2 = make_float2(wv, wv);
         const uint32_t tR = tmem + lane_off + b * C::SRW;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -619,8 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 o2 = __ffma2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2,
-                                         make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1])));
+            float2 r2 = make_float2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]));
+            if constexpr (kPV16) r2 = __fmul2_rn(r2, w2);
+            const float2 o2 = __ffma2_rn(make_float2(o[ch * 32 + e], o[ch * 32 + e + 1]), a2, r2);
             o[ch * 32 + e] = o2.x;
             o[ch * 32 + e + 1] = o2.y;
           }
@@ -629,16 +649,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sr_free[b]);
       }
       if (!ok) break;
-      // epilogue of this item: O / l * delta_V (+ V_m) in bf16
+      // epilogue of this item: O / l * delta_V (+ V_m) in bf16; SageBwd: O / l
+      // (+ V_m), the scales being inside O, and the row's log-sum-exp
+      // ln2 (m + log2 l) in the units of S sm_scale
       const int row = it.row0 + r;
+      if (kPV16 && row < p.N) p.lse[(size_t)it.bh * p.N_pad + row] = (mrow + log2f(lsum)) * 0.6931471805599453f;
       if (row < p.N) {
         const float inv_l = 1.0f / lsum;
         const float *dv = p.dv + (size_t)it.hkv * D, *vm = p.vm + (size_t)it.hkv * D;
         __nv_bfloat16 *dst = p.o + ((size_t)it.bh * p.N + row) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 8) {
-          const float4 dv0 = __ldg(reinterpret_cast<const float4 *>(dv + c));
-          const float4 dv1 = __ldg(reinterpret_cast<const float4 *>(dv + c + 4));
+          const float4 one4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+          const float4 dv0 = kPV16 ? one4 : __ldg(reinterpret_cast<const float4 *>(dv + c));
+          const float4 dv1 = kPV16 ? one4 : __ldg(reinterpret_cast<const float4 *>(dv + c + 4));
           const float4 vm0 = __ldg(reinterpret_cast<const float4 *>(vm + c));
           const float4 vm1 = __ldg(reinterpret_cast<const float4 *>(vm + c + 4));
           const float dvs[8] = {dv0.x, dv0.y, dv0.z, dv0.w, dv1.x, dv1.y, dv1.z, dv1.w};
@@ -673,9 +697,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     : p.dq[(size_t)it.bh * p.Tm + it.qi];
       float m = -INFINITY, l = 0.0f;
       const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
+      const float *dvbr = kPV16 ? p.dvb + (size_t)it.hkv * p.Tn : nullptr;  // SageBwd V block scales
       float dk_next = dkr[0];
       for (int j = 0; j < it.T; ++j, ++gt, bb = (bb + 1 == NB) ? 0 : bb + 1, pj ^= (bb == 0) ? 1 : 0) {
         const float dkj = dk_next;
+        const float dvbj = kPV16 ? dvbr[j] : 0.0f;  // used at the tile's end, its latency hidden
         const float k1 = dq * dkj * c2;  // S code -> t
         // the TMEM loads are warp-collective: the warp decides together
         const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin) &&
@@ -758,6 +784,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mt = fmaxf(mh * xs, s_mx[((gt & 1) * 2 + oh) * 128 + r] * xs);  // row max of t over the tile
         const float m_new = fmaxf(m, mt);
         const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
+        if constexpr (kPV16) {
+          uint8_t *prow = sP + bb * C::P_BYTES;
+          // SageBwd (SageAttention3 summary, "SageBwd Forward Pass"): one P~
+          // scale per row and tile, s_P = exp2(m_tile - m_new) / 127, so
+          // P^ = rint(P~ / s_P) = rint(127 exp2(t - m_tile)) = rint(e g3); the
+          // codes go out as fp16 integers, 8 keys per 16-byte chunk
+          const float g3 = (mh == -INFINITY) ? 0.0f : 127.0f * ex2_approx(mht - mt);
+          const float2 g32 = make_float2(g3, g3);
+#pragma unroll
+          for (int ch = 0; ch < HALF / 8; ++ch) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float2 p2 = __fmul2_rn(make_float2(x[ch * 8 + e], x[ch * 8 + e + 1]), g32);
+              const __half2 h = __floats2half2_rn(fminf(rintf(p2.x), 127.0f), fminf(rintf(p2.y), 127.0f));
+              pk[e / 2] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            // keys hf HALF + 8 ch .. +7 are 16-byte chunk (hf HALF / 8 + ch) of row r
+            *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, hf * (HALF / 8) + ch)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          // l sums the unquantized P~ = e exp2(m_half - m_new)
+          const float u = (mh == -INFINITY) ? 0.0f : ex2_approx(mht - m_new);
+          l = fmaf(alpha, l, u * (se2.x + se2.y));
+          if (hf == 0) s_w[bb * 128 + r] = (mt == -INFINITY) ? 0.0f : ex2_approx(mt - m_new) * (1.0f / 127.0f) * dvbj;
+          if (hf == 0 && j == it.T - 1) s_mrow[bb * 128 + r] = m_new;
+        } else {
         // P^ = e4m3(448 exp2(t - m_new)) = e4m3(e g)
         const float g = (mh == -INFINITY) ? 0.0f : ex2_approx(mht - m_new + kLog2_448);
         const float2 g2 = make_float2(g, g);
@@ -777,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         l = fmaf(alpha, l, g * (se2.x + se2.y));  // 448 times this half's sum of P~
+        }
         m = m_new;
         if (hf == 0) s_alpha[bb * 128 + r] = alpha;
         if (j == it.T - 1) s_l[(bb * 2 + hf) * 128 + r] = l;
@@ -793,10 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQkWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, int BK, bool kQK16>
+template <int D, int BK, bool kQK16, bool kPV16 = false>
 sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags, const void *ws,
                      const sage_ws_layout &L, void *o, cudaStream_t stream) {
-  using C = Cfg<D, BK, kQK16>;
+  using C = Cfg<D, BK, kQK16, false, kPV16>;
   const char *w = (const char *)ws;
   CUtensorMap tq, tk, tv;
   sage_status st;
@@ -804,7 +858,8 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   if (st != SAGE_OK) return st;
   st = make_tmap_2d(&tk, w + L.khat, C::ROWB, (uint64_t)s.B * s.Hkv * L.M_pad, C::ROWB, C::QK_SW, BK, C::QK_SW);
   if (st != SAGE_OK) return st;
-  st = make_tmap_2d(&tv, w + L.vhat, L.M_pad, (uint64_t)s.B * s.Hkv * D, L.M_pad, BK, D, C::PV_SW);
+  st = make_tmap_2d(&tv, w + L.vhat, (uint64_t)L.M_pad * C::PV_EB, (uint64_t)s.B * s.Hkv * D,
+                    (uint64_t)L.M_pad * C::PV_EB, BK * C::PV_EB, D, C::PV_SW);
   if (st != SAGE_OK) return st;
   AttnParams p;
   p.N = s.N;
@@ -821,6 +876,8 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.sm_log2 = sm_scale * 1.4426950408889634f;
   p.dq = (const float *)(w + L.dq);
   p.dqt = (const float *)(w + L.dqt);
+  p.dvb = (const float *)(w + L.dvb);
+  p.lse = (float *)(w + L.lse);
   p.qbar = (const float *)(w + L.qbar);
   p.dk = (const float *)(w + L.dk);
   p.dv = (const float *)(w + L.dv);
@@ -829,9 +886,9 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
   const bool sq = (flags & SAGE_SMOOTH_Q) != 0;
-  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true> : attn_q8_kernel<D, BK, kQK16, false>;
+  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true, kPV16> : attn_q8_kernel<D, BK, kQK16, false, kPV16>;
   // the Q-smoothing instance with INT8 codes and 128-key tiles holds the q_bar tiles too
-  const int smem = sq ? Cfg<D, BK, kQK16, kQK16 && BK == 128>::SMEM_TOTAL : C::SMEM_TOTAL;
+  const int smem = sq ? Cfg<D, BK, kQK16, kQK16 && BK == 128, kPV16>::SMEM_TOTAL : C::SMEM_TOTAL;
   // the register split needs the launch allocation it was computed for
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
@@ -855,6 +912,11 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
 
 sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
                            const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream) {
+  if (mode == SAGE_SAGEBWD_I8) {  // INT8 codes throughout, 64-key tiles (checked by the caller)
+    if (bk != 64) return SAGE_ERR_UNSUPPORTED;
+    return s.d == 64 ? launch_t<64, 64, true, true>(s, causal, sm_scale, flags, ws, L, o, stream)
+                     : launch_t<128, 64, true, true>(s, causal, sm_scale, flags, ws, L, o, stream);
+  }
   const bool i8 = (mode == SAGE_Q8_PV8);
   if (s.d == 64) {
     if (bk == 64)

@@ -34,12 +34,14 @@ inline sage_status check_request(const sage_shape *s, int mode, int bq, int bk) 
   if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->N <= 0 || s->M <= 0 || s->d <= 0)
     return SAGE_ERR_INVALID_ARG;
   if (s->Hq % s->Hkv != 0) return SAGE_ERR_INVALID_ARG;
-  if (mode < SAGE_Q8_PV8 || mode > SAGE_NVFP4) return SAGE_ERR_INVALID_ARG;
+  if (mode < SAGE_Q8_PV8 || mode > SAGE_SAGEBWD_I8) return SAGE_ERR_INVALID_ARG;
   if (bq <= 0 || bk <= 0) return SAGE_ERR_INVALID_ARG;
   if (s->N > kMaxTokens || s->M > kMaxTokens) return SAGE_ERR_UNSUPPORTED;
   if (s->d != 64 && s->d != 128) return SAGE_ERR_UNSUPPORTED;
   if (bq != 128) return SAGE_ERR_UNSUPPORTED;
   if (bk != 64 && bk != 128) return SAGE_ERR_UNSUPPORTED;
+  // SageBwd: 16-bit P^ and V^ tiles fit the shared memory with 64-key tiles
+  if (mode == SAGE_SAGEBWD_I8 && bk != 64) return SAGE_ERR_UNSUPPORTED;
   if ((int64_t)s->B * s->Hq > (1 << 20) || (int64_t)s->B * s->Hkv > (1 << 20)) return SAGE_ERR_UNSUPPORTED;
   return SAGE_OK;
 }
@@ -50,9 +52,10 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   const int64_t B = s->B, Hq = s->Hq, Hkv = s->Hkv, d = s->d;
   const int64_t N_pad = align_up((size_t)s->N, 128), M_pad = align_up((size_t)s->M, 128);
   const int64_t Tm = N_pad / bq, Tn = cdiv(s->M, bk);
-  // bytes per stored code: fp16 integer (mode 0), E4M3 byte (1), packed E2M1 (2)
-  const double code_bytes = (mode == SAGE_Q8_PV8) ? 2.0 : (mode == SAGE_QF8_PV8 ? 1.0 : 0.5);
-  const double v_bytes = (mode == SAGE_NVFP4) ? 0.5 : 1.0;
+  // bytes per stored code: fp16 integer (modes 0, 3), E4M3 byte (1), packed E2M1 (2)
+  const bool i8 = (mode == SAGE_Q8_PV8 || mode == SAGE_SAGEBWD_I8);
+  const double code_bytes = i8 ? 2.0 : (mode == SAGE_QF8_PV8 ? 1.0 : 0.5);
+  const double v_bytes = (mode == SAGE_NVFP4) ? 0.5 : (mode == SAGE_SAGEBWD_I8 ? 2.0 : 1.0);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -78,6 +81,8 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   L->stats = take(stats_bytes(*s));
   L->status = take(16);
   L->dqt = take((size_t)(B * Hq * N_pad * 4));
+  L->dvb = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hkv * Tn * 4) : 0);
+  L->lse = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * 4) : 0);
   L->total = off;
   L->N_pad = (int)N_pad;
   L->M_pad = (int)M_pad;

@@ -298,6 +298,7 @@ struct QuantArgs {
   uint8_t *qhat, *khat, *vhat;
   float *dq, *qbar, *dk, *kbar, *dv, *vm;
   float *dqt;  // per-row Q scales (SAGE_Q_PER_TOKEN)
+  float *dvb;  // per-block V scales (SageBwd forward)
   StatsView st;
   int *status;
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
@@ -514,8 +515,9 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 }
 
 // kPerRow: per-row Q scales (SAGE_Q_PER_TOKEN), an instance of its own so that
-// the per-block instances keep their register allocation
-template <int D, bool kInt8, bool kPerRow>
+// the per-block instances keep their register allocation.  kVBlk: the SageBwd
+// forward's V (per-block INT8 over 64-token blocks, fp16 integer codes).
+template <int D, bool kInt8, bool kPerRow, bool kVBlk>
 __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArgs a) {
   constexpr int CB = kInt8 ? 2 : 1;
   constexpr int kPool = qk_pool_bytes<D>() > v_pool_bytes<D>() ? qk_pool_bytes<D>() : v_pool_bytes<D>();
@@ -546,6 +548,77 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     return;
   }
   cta -= a.nk;
+  if constexpr (kVBlk) {
+    // ---- V token chunk (b, g, 128 tokens), SageBwd forward (SageAttention3
+    // summary, "SageBwd Forward Pass"): the chunk holds two 64-token blocks;
+    // per block s_V = max |fl(V - V_m)| / 127 over its tokens and all
+    // channels, codes rint(fl(V' / s_V)) as fp16 integers written transposed
+    // (token-contiguous per channel).  Work item = 4 consecutive tokens x 8
+    // channels; the 32 lanes of a warp take 32 consecutive token groups of the
+    // same channels, so lanes 0-15 hold block 0 and 16-31 block 1, and each
+    // code store of a warp is 256 contiguous bytes.  Tokens past M get code 0
+    // (the attention's masked keys read them).  The raw rows stay in
+    // registers between the maximum and the codes.
+    constexpr int VPR = D / 8;
+    constexpr int IPT = 32 * VPR / kThreads;  // work items per thread
+    static_assert(IPT >= 1 && IPT * kThreads == 32 * VPR, "whole work items per thread");
+    const int nchunk = a.M_pad / 128;
+    const int ch = cta % nchunk, hb = cta / nchunk;
+    float *vmean = reinterpret_cast<float *>(pool);
+    unsigned *bmax = reinterpret_cast<unsigned *>(vmean + D);  // block maxima (non-negative floats as bits)
+    for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
+    if (threadIdx.x < 2) bmax[threadIdx.x] = 0u;
+    __syncthreads();
+    const int t0 = ch * 128;
+    const int tg = threadIdx.x & 31, blk = tg >> 4;  // token group (the lane) and its 64-token block
+    uint4 raw[IPT][4];
+    float am = 0.0f;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      const int cg = (threadIdx.x + k * kThreads) >> 5;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 4 * tg + u;
+        raw[k][u] = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + cg] : make_uint4(0, 0, 0, 0);
+        if (t < a.M) {
+          float f[8];
+          unpack_bf16x8(raw[k][u], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(f[e], vmean[cg * 8 + e])));
+        }
+      }
+    }
+    // half-warp maxima (lanes 0-15 block 0, 16-31 block 1), then one atomic each
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if ((tg & 15) == 0) atomicMax(&bmax[blk], __float_as_uint(am));
+    __syncthreads();
+    const float delta = __fdiv_rn(__uint_as_float(bmax[blk]), 127.0f);
+    const float rcp = __frcp_rn(delta);
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      const int cg = (threadIdx.x + k * kThreads) >> 5;
+      float f[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) unpack_bf16x8(raw[k][u], f[u]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float c4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          c4[u] = (delta != 0.0f && t0 + 4 * tg + u < a.M)
+                      ? int8_code(__fsub_rn(f[u][e], vmean[cg * 8 + e]), delta, rcp) : 0.0f;
+        const __half2 h01 = __floats2half2_rn(c4[0], c4[1]), h23 = __floats2half2_rn(c4[2], c4[3]);
+        *reinterpret_cast<uint2 *>(a.vhat + (((size_t)hb * D + cg * 8 + e) * a.M_pad + t0 + 4 * tg) * 2) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+      }
+    }
+    if (threadIdx.x < 2) {
+      const int j = t0 / 64 + threadIdx.x;  // 64-token block index
+      if (j < a.Tn) a.dvb[(size_t)hb * a.Tn + j] = __fdiv_rn(__uint_as_float(bmax[threadIdx.x]), 127.0f);
+    }
+    return;
+  }
   // ---- V token chunk (b, g, 128 tokens): per-channel scales from the stats,
   // E4M3 codes written transposed (token-contiguous per channel).  Each work
   // item is 4 consecutive tokens x 8 channels: the 4 codes of a channel pack
@@ -875,6 +948,7 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.vhat = (uint8_t *)(w + L.vhat);
   a.dq = (float *)(w + L.dq);
   a.dqt = (float *)(w + L.dqt);
+  a.dvb = (float *)(w + L.dvb);
   a.qbar = (float *)(w + L.qbar);
   a.dk = (float *)(w + L.dk);
   a.kbar = (float *)(w + L.kbar);
@@ -886,11 +960,17 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.nk = s.B * s.Hkv * L.Tn;
   const int nv = s.B * s.Hkv * (L.M_pad / 128);
   const unsigned grid = (unsigned)(a.nq + a.nk + nv);
-  const bool i8 = (mode == SAGE_Q8_PV8), pr = (flags & SAGE_Q_PER_TOKEN) != 0;
-  auto kern = s.d == 64 ? (i8 ? (pr ? quantize_kernel<64, true, true> : quantize_kernel<64, true, false>)
-                              : (pr ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>))
-                        : (i8 ? (pr ? quantize_kernel<128, true, true> : quantize_kernel<128, true, false>)
-                              : (pr ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>));
+  const bool pr = (flags & SAGE_Q_PER_TOKEN) != 0;
+  void (*kern)(QuantArgs) = nullptr;
+  if (mode == SAGE_SAGEBWD_I8)
+    kern = s.d == 64 ? (pr ? quantize_kernel<64, true, true, true> : quantize_kernel<64, true, false, true>)
+                     : (pr ? quantize_kernel<128, true, true, true> : quantize_kernel<128, true, false, true>);
+  else if (mode == SAGE_Q8_PV8)
+    kern = s.d == 64 ? (pr ? quantize_kernel<64, true, true, false> : quantize_kernel<64, true, false, false>)
+                     : (pr ? quantize_kernel<128, true, true, false> : quantize_kernel<128, true, false, false>);
+  else
+    kern = s.d == 64 ? (pr ? quantize_kernel<64, false, true, false> : quantize_kernel<64, false, false, false>)
+                     : (pr ? quantize_kernel<128, false, true, false> : quantize_kernel<128, false, false, false>);
   kern<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }

@@ -60,7 +60,13 @@ typedef enum {
 enum {
   SAGE_Q8_PV8 = 0,  /* INT8 per-block Q/K, FP8 E4M3 P~ (1/448) and per-channel FP8 V */
   SAGE_QF8_PV8 = 1, /* FP8 E4M3 per-block Q/K, FP8 P~ / V as above */
-  SAGE_NVFP4 = 2    /* NVFP4 Q/K/V (E2M1, 1x16 blocks, E4M3 scales), two-level P~ */
+  SAGE_NVFP4 = 2,   /* NVFP4 Q/K/V (E2M1, 1x16 blocks, E4M3 scales), two-level P~ */
+  /* SageBwd forward (SageAttention3 summary, "SageBwd Forward Pass"): INT8
+   * per-block Q and K as in mode 0, INT8 per-block V (one scale per bk-token
+   * block), INT8 P~ with one scale per row and key tile,
+   * s_P = exp(rowmax S_ij - m_ij) / 127; bk = 64.  The attention also writes
+   * each row's log-sum-exp (region lse), which a backward pass needs */
+  SAGE_SAGEBWD_I8 = 3
 };
 
 /* flags */
@@ -101,12 +107,16 @@ typedef struct {
  *   stats                 reduction scratch of sage_quantize_qkv
  *   status                int32[4]: code, site, detail, spare
  *   dqt    [B*Hq*N_pad]   fp32 per-row Q scale (SAGE_Q_PER_TOKEN; 0 on pad rows)
+ *   dvb    [B*Hkv*Tn]     fp32 per-block V scale (mode 3, whose vhat holds the
+ *          INT8 codes as fp16 values)
+ *   lse    [B*Hq*N_pad]   fp32 log-sum-exp of each row's scaled scores,
+ *          ln sum_j exp(S_ij sm_scale) (mode 3; rows past N not written)
  * N_pad = N rounded up to 128, M_pad = M rounded up to 128, Tm = N_pad/bq,
  * Tn = ceil(M/bk). */
 typedef struct {
   size_t qhat, dq, qbar, khat, dk, kbar, vhat, dv, vm, qsf, ksf, vsf, stats, status, total;
   int N_pad, M_pad, Tm, Tn;
-  size_t dqt;
+  size_t dqt, dvb, lse;
 } sage_ws_layout;
 
 /* Workspace size in bytes for a shape and mode; 0 if the request is invalid

@@ -141,3 +141,19 @@ def test_package_has_no_fallback():
     assert "raise ImportError" in src
     for bad in ("import oracle", "from oracle", "sage_oracle"):
         assert bad not in src
+
+
+def test_sagebwd_layout(sage):
+    """Mode 3 (SageBwd forward): fp16 V codes, per-block V scales, per-row
+    log-sum-exp; 64-key tiles only."""
+    shp = (2, 8, 4, 1000, 1500, 128)
+    s = sage.Shape(*shp)
+    L = sage.sage_workspace_layout(s, 3, 128, 64).as_dict()
+    B, Hq, Hkv, N, M, d = shp
+    assert L["dv"] - L["vhat"] >= B * Hkv * d * L["M_pad"] * 2
+    assert L["lse"] - L["dvb"] >= B * Hkv * L["Tn"] * 4
+    assert L["total"] - L["lse"] >= B * Hq * L["N_pad"] * 4
+    assert all(L[k] % 1024 == 0 for k in ("dqt", "dvb", "lse", "total"))
+    assert sage.sage_workspace_bytes(s, 3, 128, 128) == 0
+    with pytest.raises(sage.SageError):
+        sage.sage_workspace_layout(s, 3, 128, 128)

@@ -78,7 +78,7 @@ def check(cfg, got_rows, q, k, v, rows, threads=None):
     if exact is not None:
         e = output_metrics(got_rows, exact)
         o = output_metrics(ref, exact)
-        bar = {0: 0.999, 1: 0.998, 2: 0.975}[cfg.mode]
+        bar = {0: 0.999, 1: 0.998, 2: 0.975, 3: 0.999}[cfg.mode]
         assert e["cos"] >= bar, (e, o)
         if cfg.mode == 2:
             assert e["cos"] >= o["cos"] - 2e-3, (e, o)
