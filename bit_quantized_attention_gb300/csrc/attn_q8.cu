@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "layout.h"
 #include "launch.h"
@@ -195,14 +196,17 @@ __device__ __forceinline__ float qbar_dot_key(const uint8_t *kt, const float *qb
 }
 
 // kSmoothQ: Q smoothing on (dS added to the scores); its instances carry the dS
-// stream, the others none of its state.  kPV16: the SageBwd forward.
-template <int D, int BK, bool kQK16, bool kSmoothQ, bool kPV16>
+// stream, the others none of its state.  kPV16: the SageBwd forward.  kPing:
+// the softmax warpgroups take whole key tiles in turn instead of halves of
+// every tile (instances without Q smoothing, INT8 / FP8 P~).
+template <int D, int BK, bool kQK16, bool kSmoothQ, bool kPV16, bool kPing = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles);
   // otherwise the accumulation warpgroup takes it on CUDA cores
   constexpr bool kDsMma = kSmoothQ && kQK16 && BK == 128;
+  static_assert(!kPing || (!kSmoothQ && !kPV16), "tiles in turn: plain scores, FP8 P~");
   using C = Cfg<D, BK, kQK16, kDsMma, kPV16>;
   constexpr int KST = C::KST, VST = C::VST;
   constexpr int HALF = C::HALF;
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < NB; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 2 * kWG);
+      mbar_init(&p_full[x], kPing ? kWG : 2 * kWG);  // one or both softmax warpgroups
       mbar_init(&r_full[x], 1);
       mbar_init(&sr_free[x], kWG);
       mbar_init(&ds_full[x], kWG);
@@ -622,7 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float a = s_alpha[b * 128 + r];
-        if (j == it.T - 1) {
+        if constexpr (kPing) {
+          lsum = fmaf(a, lsum, s_l[b * 128 + r]);  // l from each tile's row sum
+        } else if (j == it.T - 1) {
           lsum = s_l[(b * 2 + 0) * 128 + r] + s_l[(b * 2 + 1) * 128 + r];
           if constexpr (kPV16) mrow = s_mrow[b * 128 + r];
         }
@@ -677,6 +683,128 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+      }
+    }
+  } else if constexpr (kPing) {
+    reg_alloc<kSoftmaxRegs>();
+    // ------------------------------------------------------------ softmax, whole tiles in turn
+    // Warpgroup w takes the key tiles gt with gt % 2 == w: all BK keys of its
+    // 128 rows (one row per thread, its TMEM lane), streamed from TMEM in
+    // 32-column chunks twice, the row maximum first, then the exponentials and
+    // P^.  Only the running maximum passes between the warpgroups: tile gt
+    // publishes m_gt (s_mx[gt % NB], mx_full[gt % NB]) as soon as it has its own
+    // row maximum and m_gt-1, before its exponentials, so the other
+    // warpgroup's next tile waits on a few instructions of this one.  Each
+    // tile hands the accumulation warpgroup alpha and its row sum (s_l), from
+    // which that warpgroup keeps l.  Buffer reuse: s_mx[b] of tile gt is read
+    // by tile gt + 1 and next written by tile gt + NB, both of the same
+    // warpgroup (NB odd); s_alpha / s_l as in the split form.
+    static_assert(NB % 2 == 1, "the reader of a running maximum is its next writer");
+    const int r = threadIdx.x & (kWG - 1);
+    const int wg = warp >> 2;
+    const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float c2 = p.sm_log2;
+    bool stop = false;
+    int gt = 0;
+    for (int n = 0; !stop && blockIdx.x + n * G < p.items; ++n) {
+      const Item it = item_of(p, blockIdx.x + n * G, BK);
+      const int diag = it.row0 + r + p.M - p.N;  // last key visible to this row (causal)
+      const float dq = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
+                                                    : p.dq[(size_t)it.bh * p.Tm + it.qi];
+      const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
+      for (int j = 0; j < it.T; ++j, ++gt) {
+        if ((gt & 1) != wg) continue;
+        const int bb = gt % NB;
+        const float dkj = dkr[j];  // in flight during the S wait
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[bb], (gt / NB) & 1, status, 32, s_abort, p.spin))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const float k1 = dq * dkj * c2;  // S code -> t
+        // x orders like t: the raw MMA output with the scale folded into the
+        // exponent when k1 > 0, else t itself (a masked -inf never meets a 0)
+        const bool raw = k1 > 0.0f;
+        const float xs = raw ? k1 : 1.0f;
+        const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > it.row0 + p.M - p.N);
+        const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // keys at or past lim are masked
+        const uint32_t tSb = tS + bb * C::SRW;
+        // pass 1: the row maximum
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int ch = 0; ch < BK / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tSb + ch * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(v[e]);
+            if (!raw) x *= k1;
+            if (edge && ch * 32 + e >= lim) x = -INFINITY;
+            mq[e & 3] = fmaxf(mq[e & 3], x);
+          }
+        }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float mt = (mx == -INFINITY) ? -INFINITY : mx * xs;  // row max of t over the tile
+        // the running maximum: the previous tile's, from the other warpgroup
+        float m_prev = -INFINITY;
+        if (j > 0) {
+          const int pb = (gt - 1) % NB;
+          if (!__all_sync(0xffffffffu, mbar_wait(&mx_full[pb], ((gt - 1) / NB) & 1, status, 33, s_abort, p.spin))) {
+            stop = true;
+            break;
+          }
+          m_prev = s_mx[pb * 128 + r];
+        }
+        const float m_new = fmaxf(m_prev, mt);
+        s_mx[bb * 128 + r] = m_new;
+        mbar_arrive(&mx_full[bb]);
+        const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m_prev - m_new);
+        // pass 2: P^ = e4m3(448 exp2(t - m_new)) with the 448 in the exponent's
+        // bias; a row with nothing visible yet has only masked keys (-> 0)
+        const float mb = (m_new == -INFINITY) ? INFINITY : m_new - kLog2_448;
+        const float2 xs2 = make_float2(xs, xs), nb2 = make_float2(-mb, -mb);
+        uint8_t *prow = sP + bb * C::P_BYTES;
+        float2 rs2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int ch = 0; ch < BK / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tSb + ch * 32, v);
+          tmem_wait_ld();
+          float pv[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+            if (!raw) {
+              x0 *= k1;
+              x1 *= k1;
+            }
+            if (edge) {
+              x0 = (ch * 32 + e < lim) ? x0 : -INFINITY;
+              x1 = (ch * 32 + e + 1 < lim) ? x1 : -INFINITY;
+            }
+            const float2 arg = __ffma2_rn(make_float2(x0, x1), xs2, nb2);
+            pv[e] = ex2_approx(arg.x);
+            pv[e + 1] = ex2_approx(arg.y);
+            rs2 = __fadd2_rn(rs2, make_float2(pv[e], pv[e + 1]));
+          }
+          // keys 32 ch .. 32 ch + 31 are 16-byte chunks 2 ch and 2 ch + 1 of row r
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              const int i0 = h * 16 + e;
+              pk[e / 4] = (uint32_t)cvt_e4m3x2(pv[i0], pv[i0 + 1]) | ((uint32_t)cvt_e4m3x2(pv[i0 + 2], pv[i0 + 3]) << 16);
+            }
+            *reinterpret_cast<uint4 *>(prow + swz_off<C::PV_SW>(r, 2 * ch + h)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+        s_alpha[bb * 128 + r] = alpha;
+        s_l[bb * 128 + r] = rs2.x + rs2.y;  // 448 times this tile's sum of P~, against m_new
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[bb]);
       }
     }
   } else {
@@ -886,7 +1014,13 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
   const bool sq = (flags & SAGE_SMOOTH_Q) != 0;
-  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true, kPV16> : attn_q8_kernel<D, BK, kQK16, false, kPV16>;
+  // whole key tiles in turn between the softmax warpgroups (SAGE_PINGPONG=1):
+  // an alternative softmax schedule for the instances without Q smoothing
+  const char *pp = getenv("SAGE_PINGPONG");
+  const bool ping = !sq && !kPV16 && pp && pp[0] == '1';
+  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true, kPV16>
+                 : (ping ? attn_q8_kernel<D, BK, kQK16, false, kPV16, !kPV16>
+                         : attn_q8_kernel<D, BK, kQK16, false, kPV16>);
   // the Q-smoothing instance with INT8 codes and 128-key tiles holds the q_bar tiles too
   const int smem = sq ? Cfg<D, BK, kQK16, kQK16 && BK == 128, kPV16>::SMEM_TOTAL : C::SMEM_TOTAL;
   // the register split needs the launch allocation it was computed for
