@@ -198,7 +198,7 @@ __device__ __forceinline__ float qbar_dot_key(const uint8_t *kt, const float *qb
 // kSmoothQ: Q smoothing on (dS added to the scores); its instances carry the dS
 // stream, the others none of its state.  kPV16: the SageBwd forward.  kPing:
 // the softmax warpgroups take whole key tiles in turn instead of halves of
-// every tile (instances without Q smoothing, INT8 / FP8 P~).
+// every tile (INT8 / FP8 P~).
 template <int D, int BK, bool kQK16, bool kSmoothQ, bool kPV16, bool kPing = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles);
   // otherwise the accumulation warpgroup takes it on CUDA cores
   constexpr bool kDsMma = kSmoothQ && kQK16 && BK == 128;
-  static_assert(!kPing || (!kSmoothQ && !kPV16), "tiles in turn: plain scores, FP8 P~");
+  static_assert(!kPing || !kPV16, "tiles in turn: FP8 P~");
   using C = Cfg<D, BK, kQK16, kDsMma, kPV16>;
   constexpr int KST = C::KST, VST = C::VST;
   constexpr int HALF = C::HALF;
@@ -716,15 +716,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((gt & 1) != wg) continue;
         const int bb = gt % NB;
         const float dkj = dkr[j];  // in flight during the S wait
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[bb], (gt / NB) & 1, status, 32, s_abort, p.spin))) {
+        const bool okw = mbar_wait(&s_full[bb], (gt / NB) & 1, status, 32, s_abort, p.spin) &&
+                         (!kSmoothQ || mbar_wait(&ds_full[bb], (gt / NB) & 1, status, 31, s_abort, p.spin));
+        if (!__all_sync(0xffffffffu, okw)) {
           stop = true;
           break;
         }
         tc_fence_after();
         const float k1 = dq * dkj * c2;  // S code -> t
         // x orders like t: the raw MMA output with the scale folded into the
-        // exponent when k1 > 0, else t itself (a masked -inf never meets a 0)
-        const bool raw = k1 > 0.0f;
+        // exponent when k1 > 0 and there is no dS, else t itself (a masked -inf
+        // never meets a 0)
+        const bool raw = !kSmoothQ && k1 > 0.0f;
+        const float *dsc = s_ds + bb * BK;  // dS of the tile in t units (Q smoothing)
         const float xs = raw ? k1 : 1.0f;
         const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > it.row0 + p.M - p.N);
         const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // keys at or past lim are masked
@@ -739,7 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float x = __uint_as_float(v[e]);
-            if (!raw) x *= k1;
+            if constexpr (kSmoothQ)
+              x = fmaf(x, k1, dsc[ch * 32 + e]);
+            else if (!raw)
+              x *= k1;
             if (edge && ch * 32 + e >= lim) x = -INFINITY;
             mq[e & 3] = fmaxf(mq[e & 3], x);
           }
@@ -775,7 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
-            if (!raw) {
+            if constexpr (kSmoothQ) {
+              const float2 t2 = __ffma2_rn(make_float2(x0, x1), make_float2(k1, k1),
+                                           *reinterpret_cast<const float2 *>(dsc + ch * 32 + e));
+              x0 = t2.x;
+              x1 = t2.y;
+            } else if (!raw) {
               x0 *= k1;
               x1 *= k1;
             }
@@ -1015,10 +1027,10 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.spin = spin_limit_cycles();
   const bool sq = (flags & SAGE_SMOOTH_Q) != 0;
   // whole key tiles in turn between the softmax warpgroups (SAGE_PINGPONG=1):
-  // an alternative softmax schedule for the instances without Q smoothing
+  // an alternative softmax schedule (not for the SageBwd forward)
   const char *pp = getenv("SAGE_PINGPONG");
-  const bool ping = !sq && !kPV16 && pp && pp[0] == '1';
-  auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true, kPV16>
+  const bool ping = !kPV16 && pp && pp[0] == '1';
+  auto kern = sq ? (ping ? attn_q8_kernel<D, BK, kQK16, true, kPV16, !kPV16> : attn_q8_kernel<D, BK, kQK16, true, kPV16>)
                  : (ping ? attn_q8_kernel<D, BK, kQK16, false, kPV16, !kPV16>
                          : attn_q8_kernel<D, BK, kQK16, false, kPV16>);
   // the Q-smoothing instance with INT8 codes and 128-key tiles holds the q_bar tiles too
