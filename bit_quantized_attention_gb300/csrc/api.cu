@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -194,6 +195,50 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
   if (st != SAGE_OK) return st;
   if (cudaMemcpyAsync(o_host, dO, qn, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return SAGE_ERR_CUDA;
   return SAGE_OK;
+}
+
+size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,
+                                   int d, int quant_mode, int bq, int bk) {
+  VarlenPlan P;
+  if (quant_mode == SAGE_NVFP4) return 0;  // packed sequences: INT8 / FP8 / SageBwd modes
+  if (plan_varlen(nseq, cu_seqlens_q, cu_seqlens_k, Hq, Hkv, d, quant_mode, bq, bk, 0, &P) != SAGE_OK) return 0;
+  sage_ws_layout L;
+  if (request_layout(&P.shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  return P.total;
+}
+
+sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv, int d,
+                             int causal, float sm_scale, int quant_mode, int flags, int bq, int bk, const void *q,
+                             const void *k, const void *v, void *workspace, size_t workspace_bytes, void *o,
+                             sage_stream_t stream) {
+  VarlenPlan P;
+  sage_status st = plan_varlen(nseq, cu_seqlens_q, cu_seqlens_k, Hq, Hkv, d, quant_mode, bq, bk, causal, &P);
+  if (st != SAGE_OK) return st;
+  sage_ws_layout L;
+  if ((st = request_layout(&P.shape, quant_mode, bq, bk, &L)) != SAGE_OK) return st;  // the int-range checks
+  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  if ((st = check_attn_args(&P.shape, causal, sm_scale, quant_mode, flags, bk)) != SAGE_OK) return st;
+  if (!q || !k || !v || !o || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)workspace & 1023))
+    return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < P.total) return SAGE_ERR_WORKSPACE;
+  // the sequence and work item tables, one host-to-device copy (from pageable
+  // memory: the call returns once the source has been staged)
+  char *ws = (char *)workspace;
+  std::vector<char> tabs(P.total - P.seq_off, 0);
+  memcpy(tabs.data(), P.seqs.data(), sizeof(VarSeq) * P.seqs.size());
+  memcpy(tabs.data() + (P.item_off - P.seq_off), P.item_codes.data(), sizeof(int) * P.item_codes.size());
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(ws + P.seq_off, tabs.data(), tabs.size(), cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return SAGE_ERR_CUDA;
+  const VarSeq *seq = (const VarSeq *)(ws + P.seq_off);
+  st = launch_quantize_q8(P.shape, quant_mode, flags, bq, bk, q, k, v, workspace, P.L, cs, seq);
+  if (st != SAGE_OK) return st;
+  VarDev var;
+  var.item_tab = (const int *)(ws + P.item_off);
+  var.items = P.items;
+  var.seq = seq;
+  return launch_attn_q8(P.shape, causal, sm_scale, quant_mode, flags, bk, workspace, P.L, o, cs, var);
 }
 
 sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,

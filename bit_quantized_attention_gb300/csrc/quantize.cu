@@ -134,9 +134,13 @@ __global__ void init_kernel(StatsView st, int n, int *status) {
 // issued in batches of kBatch rows so several are in flight.  Min / max run
 // on packed bf16 pairs with NaN propagation (they are exact, and a NaN or an
 // out-of-range value shows in the extremes).
-template <int D, bool kSumK, bool kSumV>
+// Packed sequences (seq non-null): batch b is sequence b, its M its own key
+// count, and its rows sit at (k0 + t) * Hkv + h of the packed [total, Hkv, d]
+// inputs; CTAs past the sequence's keys have nothing to do.
+template <int D, bool kSumK, bool kSumV, bool kVar>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                                         int M, StatsView st, int *status) {
+                                                         int M, StatsView st, int *status, const VarSeq *seq,
+                                                         int Hkv) {
   constexpr int VPR = D / 8;               // 16-byte vectors per row (threads per row)
   constexpr int RPP = kThreads / VPR;      // rows per pass
   constexpr int kBatch = 4;
@@ -148,6 +152,15 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   const int hb = blockIdx.y;
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
   const int t0 = blockIdx.x * kStatTokens;
+  // row of token t: hb * M + t (batched) or (k0 + t) * Hkv + h (packed)
+  long long row_base = (long long)hb * M, row_step = 1;
+  if constexpr (kVar) {
+    const VarSeq sq = seq[hb / Hkv];
+    M = sq.M;
+    row_base = (long long)sq.k0 * Hkv + hb % Hkv;
+    row_step = Hkv;
+    if (t0 >= M) return;  // the whole CTA: nothing of this sequence here
+  }
   const int t1 = min(M, t0 + kStatTokens);
   int klo[8], khi[8], vlo[8], vhi[8];
   __nv_bfloat162 kmn[4], kmx[4], vmn[4], vmx[4];
@@ -169,7 +182,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int t = tb + i * RPP;
-      const size_t off = ((size_t)hb * M + min(t, t1 - 1)) * VPR + vc;
+      const size_t off = kVar ? (size_t)(row_base + (long long)min(t, t1 - 1) * row_step) * VPR + vc
+                              : ((size_t)hb * M + min(t, t1 - 1)) * VPR + vc;
       kb[i] = k[off];
       vb[i] = v[off];
     }
@@ -263,26 +277,37 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
 
 template <int D>
 void launch_stats(dim3 grid, int flags, const void *k, const void *v, int M, StatsView st, int *status,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const VarSeq *seq, int Hkv) {
   const bool sk = (flags & SAGE_SMOOTH_K) != 0, sv = (flags & SAGE_SMOOTH_V) != 0;
   const uint4 *k4 = (const uint4 *)k, *v4 = (const uint4 *)v;
-  if (sk && sv)
-    stats_kernel<D, true, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
-  else if (sk)
-    stats_kernel<D, true, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
-  else if (sv)
-    stats_kernel<D, false, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+  using Kern = void (*)(const uint4 *, const uint4 *, int, StatsView, int *, const VarSeq *, int);
+  Kern kern;
+  if (seq)
+    kern = sk ? (sv ? stats_kernel<D, true, true, true> : stats_kernel<D, true, false, true>)
+              : (sv ? stats_kernel<D, false, true, true> : stats_kernel<D, false, false, true>);
   else
-    stats_kernel<D, false, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+    kern = sk ? (sv ? stats_kernel<D, true, true, false> : stats_kernel<D, true, false, false>)
+              : (sv ? stats_kernel<D, false, true, false> : stats_kernel<D, false, false, false>);
+  kern<<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status, seq, Hkv);
 }
 
 // ------------------------------------------------------------------ finalize
 // One thread per (b, kv-head, channel): k_bar and V_m from the fixed-point
 // sums (when smoothed), and delta_V = max_t |fl(V - V_m)| / 448 from the channel
 // min and max (rounded subtraction is monotone).
-__global__ void finalize_kernel(StatsView st, int n, int M, int flags, float *kbar, float *vm, float *dv) {
+// Packed sequences: the mean of (b, h) is over sequence b's M (a sequence
+// with no keys has no mean and no use for one: 0).
+__global__ void finalize_kernel(StatsView st, int n, int M, int flags, float *kbar, float *vm, float *dv,
+                                const VarSeq *seq, int per_seq) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  if (seq) {
+    M = seq[i / per_seq].M;
+    if (M == 0) {
+      kbar[i] = vm[i] = dv[i] = 0.0f;
+      return;
+    }
+  }
   kbar[i] = (flags & SAGE_SMOOTH_K) ? mean_from_sum(st.ksum[i], M) : 0.0f;
   const float mu = (flags & SAGE_SMOOTH_V) ? mean_from_sum(st.vsum[i], M) : 0.0f;
   const float hi = order_val(st.vmax[i]), lo = order_val(st.vmin[i]);
@@ -299,6 +324,7 @@ struct QuantArgs {
   float *dq, *qbar, *dk, *kbar, *dv, *vm;
   float *dqt;  // per-row Q scales (SAGE_Q_PER_TOKEN)
   float *dvb;  // per-block V scales (SageBwd forward)
+  const VarSeq *seq;  // packed sequences: per-sequence lengths and first rows (null: batched)
   StatsView st;
   int *status;
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
@@ -404,7 +430,7 @@ template <int D, bool kInt8, bool kPerRow = false>
 __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
                             const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
                             float *mean_out, int *status, int site, unsigned char *pool,
-                            float *row_delta_out = nullptr) {
+                            float *row_delta_out = nullptr, int src_stride = D / 8) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
   long long (*ssum)[D] = reinterpret_cast<long long (*)[D]>(pool);
   float *smean = reinterpret_cast<float *>(pool + RPP * D * 8);
@@ -417,7 +443,7 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
-    x[p] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+    x[p] = (r < valid_rows) ? src[(size_t)r * src_stride + vc] : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
@@ -517,7 +543,8 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 // kPerRow: per-row Q scales (SAGE_Q_PER_TOKEN), an instance of its own so that
 // the per-block instances keep their register allocation.  kVBlk: the SageBwd
 // forward's V (per-block INT8 over 64-token blocks, fp16 integer codes).
-template <int D, bool kInt8, bool kPerRow, bool kVBlk>
+// kVar: packed sequences (per-sequence lengths, packed [total, H, d] inputs).
+template <int D, bool kInt8, bool kPerRow, bool kVBlk, bool kVar>
 __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArgs a) {
   constexpr int CB = kInt8 ? 2 : 1;
   constexpr int kPool = qk_pool_bytes<D>() > v_pool_bytes<D>() ? qk_pool_bytes<D>() : v_pool_bytes<D>();
@@ -527,13 +554,21 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     // ---- Q block (b, h, i)
     const int i = cta % a.Tm, bh = cta / a.Tm;
     const int r0 = i * 128;
-    const int valid = max(0, min(128, a.N - r0));
+    // rows of this block in the input: batched [B, Hq, N, d], or packed [total, Hq, d]
+    int Nb = a.N, stride = D / 8;
+    const uint4 *src = a.q + ((size_t)bh * a.N + r0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[bh / a.Hq];
+      Nb = sq.N;
+      stride = a.Hq * (D / 8);
+      src = a.q + ((size_t)(sq.q0 + r0) * a.Hq + bh % a.Hq) * (D / 8);
+    }
+    const int valid = max(0, min(128, Nb - r0));
     const bool smooth = (a.flags & SAGE_SMOOTH_Q) != 0;
     float *qbar = a.qbar + ((size_t)bh * a.Tm + i) * D;
-    quant_block<D, kInt8, kPerRow>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0,
-                                   nullptr, a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB,
-                                   a.dq + (size_t)bh * a.Tm + i, qbar, a.status, 3, pool,
-                                   a.dqt + (size_t)bh * a.N_pad + r0);
+    quant_block<D, kInt8, kPerRow>(src, valid, 128, smooth && valid > 0, nullptr,
+                                   a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i,
+                                   qbar, a.status, 3, pool, a.dqt + (size_t)bh * a.N_pad + r0, stride);
     return;
   }
   cta -= a.nq;
@@ -541,10 +576,18 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     // ---- K block (b, g, j): k_bar over all tokens from the finalize pass
     const int j = cta % a.Tn, hb = cta / a.Tn;
     const int t0 = j * a.bk;
-    const int valid = max(0, min(a.bk, a.M - t0));
-    quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, a.kbar + (size_t)hb * D,
+    int Mb = a.M, stride = D / 8;
+    const uint4 *src = a.k + ((size_t)hb * a.M + t0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      stride = a.Hkv * (D / 8);
+      src = a.k + ((size_t)(sq.k0 + t0) * a.Hkv + hb % a.Hkv) * (D / 8);
+    }
+    const int valid = max(0, min(a.bk, Mb - t0));
+    quant_block<D, kInt8>(src, valid, a.bk, false, a.kbar + (size_t)hb * D,
                           a.khat + ((size_t)hb * a.M_pad + t0) * D * CB, a.dk + (size_t)hb * a.Tn + j, nullptr,
-                          a.status, 1, pool);
+                          a.status, 1, pool, nullptr, stride);
     return;
   }
   cta -= a.nk;
@@ -564,6 +607,15 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     static_assert(IPT >= 1 && IPT * kThreads == 32 * VPR, "whole work items per thread");
     const int nchunk = a.M_pad / 128;
     const int ch = cta % nchunk, hb = cta / nchunk;
+    // this (b, kv-head)'s keys: batched rows hb * M + t, or packed (k0 + t) * Hkv + h
+    int Mb = a.M;
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
     float *vmean = reinterpret_cast<float *>(pool);
     unsigned *bmax = reinterpret_cast<unsigned *>(vmean + D);  // block maxima (non-negative floats as bits)
     for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
@@ -579,8 +631,9 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = t0 + 4 * tg + u;
-        raw[k][u] = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + cg] : make_uint4(0, 0, 0, 0);
-        if (t < a.M) {
+        const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + cg : ((size_t)hb * a.M + t) * VPR + cg;
+        raw[k][u] = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
+        if (t < Mb) {
           float f[8];
           unpack_bf16x8(raw[k][u], f);
 #pragma unroll
@@ -606,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
         float c4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          c4[u] = (delta != 0.0f && t0 + 4 * tg + u < a.M)
+          c4[u] = (delta != 0.0f && t0 + 4 * tg + u < Mb)
                       ? int8_code(__fsub_rn(f[u][e], vmean[cg * 8 + e]), delta, rcp) : 0.0f;
         const __half2 h01 = __floats2half2_rn(c4[0], c4[1]), h23 = __floats2half2_rn(c4[2], c4[3]);
         *reinterpret_cast<uint2 *>(a.vhat + (((size_t)hb * D + cg * 8 + e) * a.M_pad + t0 + 4 * tg) * 2) =
@@ -628,6 +681,14 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
   {
     const int nchunk = a.M_pad / 128;
     const int ch = cta % nchunk, hb = cta / nchunk;
+    int Mb = a.M;
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
     float *vmean = reinterpret_cast<float *>(pool), *vdelta = vmean + D, *vrcp = vdelta + D;
     uint32_t (*tile)[33] = reinterpret_cast<uint32_t (*)[33]>(vrcp + D);
     for (int c = threadIdx.x; c < D; c += kThreads) {
@@ -645,12 +706,13 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = t0 + 4 * tg + u;
-        raw[u] = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + cg] : make_uint4(0, 0, 0, 0);
+        const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + cg : ((size_t)hb * a.M + t) * VPR + cg;
+        raw[u] = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
       }
       uint32_t word[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (t0 + 4 * tg + u >= a.M) continue;
+        if (t0 + 4 * tg + u >= Mb) continue;
         float f[8];
         unpack_bf16x8(raw[u], f);
 #pragma unroll
@@ -882,19 +944,36 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 
 // Enqueue init, statistics, finalize and quantize on `stream`, with the
 // statistics scratch at `st`.
+// the quantize instance of a request: head dim, mode (INT8 / E4M3 Q and K;
+// SageBwd V), per-row Q scales, packed sequences
+template <bool kVar>
+static void (*pick_quantize(int d, int mode, bool pr))(QuantArgs) {
+  if (mode == SAGE_SAGEBWD_I8)
+    return d == 64 ? (pr ? quantize_kernel<64, true, true, true, kVar> : quantize_kernel<64, true, false, true, kVar>)
+                   : (pr ? quantize_kernel<128, true, true, true, kVar> : quantize_kernel<128, true, false, true, kVar>);
+  if (mode == SAGE_Q8_PV8)
+    return d == 64 ? (pr ? quantize_kernel<64, true, true, false, kVar> : quantize_kernel<64, true, false, false, kVar>)
+                   : (pr ? quantize_kernel<128, true, true, false, kVar> : quantize_kernel<128, true, false, false, kVar>);
+  return d == 64 ? (pr ? quantize_kernel<64, false, true, false, kVar> : quantize_kernel<64, false, false, false, kVar>)
+                 : (pr ? quantize_kernel<128, false, true, false, kVar> : quantize_kernel<128, false, false, false, kVar>);
+}
+
 static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, const void *q, const void *k,
-                              const void *v, void *ws, const sage_ws_layout &L, StatsView st, cudaStream_t stream) {
+                              const void *v, void *ws, const sage_ws_layout &L, StatsView st, cudaStream_t stream,
+                              const VarSeq *seq = nullptr) {
   char *w = (char *)ws;
   int *status = (int *)(w + L.status);
   const int n = s.B * s.Hkv * s.d;
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
   dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
+  if (mode == SAGE_NVFP4 && seq) return SAGE_ERR_UNSUPPORTED;  // packed sequences: INT8 / FP8 modes
   if (s.d == 64)
-    launch_stats<64>(sg, flags, k, v, s.M, st, status, stream);
+    launch_stats<64>(sg, flags, k, v, s.M, st, status, stream, seq, s.Hkv);
   else
-    launch_stats<128>(sg, flags, k, v, s.M, st, status, stream);
+    launch_stats<128>(sg, flags, k, v, s.M, st, status, stream, seq, s.Hkv);
   finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, s.M, flags, (float *)(w + L.kbar),
-                                                        (float *)(w + L.vm), (float *)(w + L.dv));
+                                                        (float *)(w + L.vm), (float *)(w + L.dv), seq,
+                                                        s.Hkv * s.d);
   if (mode == SAGE_NVFP4) {
     Fp4Args f;
     f.q = (const uint4 *)q;
@@ -949,6 +1028,7 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.dq = (float *)(w + L.dq);
   a.dqt = (float *)(w + L.dqt);
   a.dvb = (float *)(w + L.dvb);
+  a.seq = seq;
   a.qbar = (float *)(w + L.qbar);
   a.dk = (float *)(w + L.dk);
   a.kbar = (float *)(w + L.kbar);
@@ -961,25 +1041,16 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   const int nv = s.B * s.Hkv * (L.M_pad / 128);
   const unsigned grid = (unsigned)(a.nq + a.nk + nv);
   const bool pr = (flags & SAGE_Q_PER_TOKEN) != 0;
-  void (*kern)(QuantArgs) = nullptr;
-  if (mode == SAGE_SAGEBWD_I8)
-    kern = s.d == 64 ? (pr ? quantize_kernel<64, true, true, true> : quantize_kernel<64, true, false, true>)
-                     : (pr ? quantize_kernel<128, true, true, true> : quantize_kernel<128, true, false, true>);
-  else if (mode == SAGE_Q8_PV8)
-    kern = s.d == 64 ? (pr ? quantize_kernel<64, true, true, false> : quantize_kernel<64, true, false, false>)
-                     : (pr ? quantize_kernel<128, true, true, false> : quantize_kernel<128, true, false, false>);
-  else
-    kern = s.d == 64 ? (pr ? quantize_kernel<64, false, true, false> : quantize_kernel<64, false, false, false>)
-                     : (pr ? quantize_kernel<128, false, true, false> : quantize_kernel<128, false, false, false>);
+  void (*kern)(QuantArgs) = seq ? pick_quantize<true>(s.d, mode, pr) : pick_quantize<false>(s.d, mode, pr);
   kern<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
 sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
                                const void *k, const void *v, void *ws, const sage_ws_layout &L,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const VarSeq *seq) {
   (void)bq;
-  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, stats_view(ws, L, s), stream);
+  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, stats_view(ws, L, s), stream, seq);
 }
 
 }  // namespace sage

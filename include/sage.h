@@ -177,6 +177,32 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
                            const void *v_host, void *o_host, void *dev_buf, size_t dev_bytes,
                            sage_stream_t stream);
 
+/* Packed sequences (the SageAttention production guide, "Handling Varying
+ * Sequence Lengths with VarLen Kernels": sageattn_varlen).  q is bf16
+ * [total_q, Hq, d], k and v bf16 [total_k, Hkv, d], o bf16 [total_q, Hq, d],
+ * all contiguous; sequence s holds query rows cu_seqlens_q[s] ..
+ * cu_seqlens_q[s+1] - 1 and key rows cu_seqlens_k[s] .. cu_seqlens_k[s+1] - 1.
+ * cu_seqlens_q and cu_seqlens_k are HOST int32 arrays of nseq + 1 entries,
+ * starting at 0 and non-decreasing; a sequence with queries needs keys, and a
+ * causal mask (bottom-right aligned within each sequence) needs at least as many
+ * keys as queries.  Each sequence is its own attention problem: its own means,
+ * scales and query / key blocks, starting at its first token.  Modes 0, 1 and 3
+ * (NVFP4: SAGE_ERR_UNSUPPORTED).
+ * The workspace holds the batched layout of B = nseq, N = the longest query
+ * run, M = the longest key run (so sage_workspace_layout of that shape
+ * locates the codes), then the sequence and work-item tables; compute and
+ * traffic follow the sequences' own lengths.  sage_attn_varlen runs the
+ * pre-pass and the attention on `stream`; its tables reach the device by one
+ * copy from pageable host memory, so the call returns only after the runtime
+ * has staged them (not capturable into a CUDA graph).
+ * sage_varlen_workspace_bytes returns 0 for an invalid or unsupported request. */
+size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,
+                                   int d, int quant_mode, int bq, int bk);
+sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv, int d,
+                             int causal, float sm_scale, int quant_mode, int flags, int bq, int bk, const void *q,
+                             const void *k, const void *v, void *workspace, size_t workspace_bytes, void *o,
+                             sage_stream_t stream);
+
 /* Copy the device status word back (blocking on that copy only): *code is a
  * sage_status (SAGE_OK, SAGE_ERR_RANGE or SAGE_ERR_TIMEOUT), *site says where
  * it was raised.  The status word is cleared by every sage_quantize_qkv. */
