@@ -374,13 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
     const float xs = smooth_q ? 1.0f : c2;  // x -> t
+    bool stop = false;  // a wait failed late in this warp's previous tile
     for (int j = wg; j < T; j += 2) {
       const int bb = j % NB;
       float *dsc = s_dsc + (((j >> 1) & 1) * 2 + wg) * BK;
       const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], (j / NB) & 1, status, 32, s_abort, p.spin));
       if (smooth_q) {
         const int s = j % ST;
-        const bool fail = !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
+        const bool fail = stop || !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
         if (!fail) {
           const int key = r;
           const uint8_t *kt = sK + s * C::K_BYTES;
@@ -412,8 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           dsc[key] = acc * c2;
         }
-        if (named_bar_any(kBarDs0 + wg, kWG, fail || !okw || *s_abort)) break;
-      } else if (!okw) {
+        // the warpgroup leaves together: a warp that stopped alone would strand
+        // the others at this barrier in its next tile
+        if (named_bar_any(kBarDs0 + wg, kWG, stop || fail || !okw || *s_abort)) break;
+      } else if (stop || !okw) {
         break;
       }
       tc_fence_after();
@@ -449,8 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_prev = -INFINITY;
       if (j > 0) {
         const int pb = (j - 1) % NB;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mx_full[pb], ((j - 1) / NB) & 1, status, 33, s_abort, p.spin)))
-          break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&mx_full[pb], ((j - 1) / NB) & 1, status, 33, s_abort, p.spin))) {
+          stop = true;
+          if (!smooth_q) break;
+          continue;  // leave with the warpgroup at the next dS barrier
+        }
         m_prev = s_mx[pb * 128 + r];
       }
       const float m_new = fmaxf(m_prev, mt);
