@@ -200,7 +200,6 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
 size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,
                                    int d, int quant_mode, int bq, int bk) {
   VarlenPlan P;
-  if (quant_mode == SAGE_NVFP4) return 0;  // packed sequences: INT8 / FP8 / SageBwd modes
   if (plan_varlen(nseq, cu_seqlens_q, cu_seqlens_k, Hq, Hkv, d, quant_mode, bq, bk, 0, &P) != SAGE_OK) return 0;
   sage_ws_layout L;
   if (request_layout(&P.shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
@@ -216,7 +215,6 @@ sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_se
   if (st != SAGE_OK) return st;
   sage_ws_layout L;
   if ((st = request_layout(&P.shape, quant_mode, bq, bk, &L)) != SAGE_OK) return st;  // the int-range checks
-  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
   if ((st = check_attn_args(&P.shape, causal, sm_scale, quant_mode, flags, bk)) != SAGE_OK) return st;
   if (!q || !k || !v || !o || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)workspace & 1023))
@@ -238,6 +236,8 @@ sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_se
   var.item_tab = (const int *)(ws + P.item_off);
   var.items = P.items;
   var.seq = seq;
+  if (quant_mode == SAGE_NVFP4)
+    return launch_attn_fp4(P.shape, causal, sm_scale, flags, bk, workspace, P.L, o, cs, var);
   return launch_attn_q8(P.shape, causal, sm_scale, quant_mode, flags, bk, workspace, P.L, o, cs, var);
 }
 

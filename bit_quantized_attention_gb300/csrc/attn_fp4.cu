@@ -107,9 +107,13 @@ struct Fp4Params {
   __nv_bfloat16 *o;
   int *status;
   long long spin;
+  // packed sequences (kVar): block b of the grid takes work item item_tab[b]
+  // (code bh * Tm + qi); seq holds each sequence's lengths and first rows
+  const int *item_tab;
+  const VarSeq *seq;
 };
 
-template <int D, bool kPing>
+template <int D, bool kPing, bool kVar>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fp4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Fp4Params p) {
@@ -149,13 +153,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.Tm;
-  const int qi = p.Tm - 1 - blockIdx.x % p.Tm;  // longest causal rows first
+  // this block's query block: longest causal rows first (batched: by block
+  // index; packed sequences: the table's order); Nq, Mk its sequence's counts
+  int bh, qi, Nq = p.N, Mk = p.M, q0 = 0;
+  if constexpr (kVar) {
+    const int code = p.item_tab[blockIdx.x];
+    bh = code / p.Tm;
+    qi = code % p.Tm;
+    const VarSeq sq = p.seq[bh / p.Hq];
+    Nq = sq.N;
+    Mk = sq.M;
+    q0 = sq.q0;
+  } else {
+    bh = blockIdx.x / p.Tm;
+    qi = p.Tm - 1 - blockIdx.x % p.Tm;
+  }
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int hkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int row0 = qi * 128;
-  const int last_row = min(p.N, row0 + 128) - 1;
-  const int T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
+  const int last_row = min(Nq, row0 + 128) - 1;
+  const int Tn = kVar ? (Mk + BK - 1) / BK : p.Tn;
+  const int T = p.causal ? min(Tn, (last_row + Mk - Nq) / BK + 1) : Tn;
   const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
   const bool direct = (p.flags & SAGE_P_DIRECT) != 0;  // phi on P~ itself (ablation)
 
@@ -340,9 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O / l + V_m in bf16
     if (ok && T >= 1) {
       const int row = row0 + r;
-      if (row < p.N) {
+      if (row < Nq) {
         const float inv_l = 1.0f / (kPing ? lsum : s_l[r] + s_l[128 + r]);
-        __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + row) * D;
+        // the output row: batched [B, Hq, N, d], or packed [total_q, Hq, d]
+        __nv_bfloat16 *dst = kVar ? p.o + ((size_t)(q0 + row) * p.Hq + h) * D : p.o + ((size_t)bh * p.N + row) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 8) {
           uint32_t w[4];
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x & (kWG - 1);
     const int wg = warp >> 2;
     const uint32_t tS0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
+    const int diag = row0 + r + Mk - Nq;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
     const float xs = smooth_q ? 1.0f : c2;  // x -> t
     bool stop = false;  // a wait failed late in this warp's previous tile
@@ -420,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // tile keys >= lim are invisible
-      const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N);
+      const int lim = (p.causal ? min(Mk, diag + 1) : Mk) - j * BK;  // tile keys >= lim are invisible
+      const bool edge = (j * BK + BK > Mk) || (p.causal && j * BK + BK - 1 > row0 + Mk - Nq);
       const uint32_t tSb = tS0 + bb * C::SRW;
       // pass 1: 16-key block maxima in x (raw S, or t with dS)
       float bm[BK / 16];
@@ -531,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x & (kWG - 1);
     const int hf = warp >> 2;  // which half of the key tile
     const uint32_t tS0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
+    const int diag = row0 + r + Mk - Nq;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
     float m = -INFINITY, l = 0.0f;
     bool stop = false;  // a wait failed late in the previous tile
@@ -590,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // m_tile then enters as one factor, P2 = 2688 exp2(t - m_tile) =
       // e * 2688 exp2(m_half - m_tile), so neither half waits on the other
       // before its exponentials.
-      const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // tile keys >= lim are invisible
-      const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N);
+      const int lim = (p.causal ? min(Mk, diag + 1) : Mk) - j * BK;  // tile keys >= lim are invisible
+      const bool edge = (j * BK + BK > Mk) || (p.causal && j * BK + BK - 1 > row0 + Mk - Nq);
       const int oh = hf ^ 1;
       float x[HALF];
       float bm[HALF / 16];
@@ -698,9 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQkWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool kPing>
+template <int D, bool kPing, bool kVar>
 sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags, const void *ws,
-                     const sage_ws_layout &L, void *o, cudaStream_t stream) {
+                     const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var) {
   using C = Fp4Cfg<D, kPing>;
   const char *w = (const char *)ws;
   CUtensorMap tq, tk, tv;
@@ -731,29 +750,36 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
-  auto kern = attn_fp4_kernel<D, kPing>;
+  p.item_tab = var.item_tab;
+  p.seq = var.seq;
+  auto kern = attn_fp4_kernel<D, kPing, kVar>;
   // the register split assumes the block launches with kLaunchRegs per thread
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
   if (fa.numRegs != kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL) != cudaSuccess)
     return SAGE_ERR_CUDA;
-  kern<<<(unsigned)(s.B * s.Hq * L.Tm), kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  const int blocks = kVar ? var.items : s.B * s.Hq * L.Tm;
+  if (blocks <= 0) return SAGE_OK;
+  kern<<<(unsigned)blocks, kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
 }  // namespace
 
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
-                            const sage_ws_layout &L, void *o, cudaStream_t stream) {
+                            const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var) {
   if (bk != BK) return SAGE_ERR_UNSUPPORTED;
+  if (var.item_tab)  // packed sequences: the split schedule
+    return s.d == 64 ? launch_t<64, false, true>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                     : launch_t<128, false, true>(s, causal, sm_scale, flags, ws, L, o, stream, var);
   // whole key tiles in turn between the softmax warpgroups (SAGE_PINGPONG=1)
   const char *pp = getenv("SAGE_PINGPONG");
   if (pp && pp[0] == '1')
-    return s.d == 64 ? launch_t<64, true>(s, causal, sm_scale, flags, ws, L, o, stream)
-                     : launch_t<128, true>(s, causal, sm_scale, flags, ws, L, o, stream);
-  return s.d == 64 ? launch_t<64, false>(s, causal, sm_scale, flags, ws, L, o, stream)
-                   : launch_t<128, false>(s, causal, sm_scale, flags, ws, L, o, stream);
+    return s.d == 64 ? launch_t<64, true, false>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                     : launch_t<128, true, false>(s, causal, sm_scale, flags, ws, L, o, stream, var);
+  return s.d == 64 ? launch_t<64, false, false>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                   : launch_t<128, false, false>(s, causal, sm_scale, flags, ws, L, o, stream, var);
 }
 
 }  // namespace sage

@@ -42,7 +42,7 @@ sage_status launch_attn_q8_var(const sage_shape &s, int causal, float sm_scale, 
 
 // Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
-                            const sage_ws_layout &L, void *o, cudaStream_t stream);
+                            const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var = VarDev());
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (api.cu).
 // A 2-D byte tensor [rows][cols] with row pitch `pitch` bytes, box {box_cols, box_rows}.

@@ -777,7 +777,7 @@ __device__ __forceinline__ size_t atom_off(int r, int blk) { return (size_t)(r &
 template <int D>
 __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, bool own_mean,
                               const float *__restrict__ given_mean, uint8_t *codes, uint8_t *atoms,
-                              float *mean_out, int *status, int site) {
+                              float *mean_out, int *status, int site, int src_stride = D / 8) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
   __shared__ long long ssum[RPP][D];
   __shared__ float smean[D];
@@ -787,7 +787,7 @@ __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, boo
 #pragma unroll
   for (int pp = 0; pp < PASSES; ++pp) {
     const int r = rr + pp * RPP;
-    x[pp] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+    x[pp] = (r < valid_rows) ? src[(size_t)r * src_stride + vc] : make_uint4(0, 0, 0, 0);
   }
   if (own_mean) {
     long long sacc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -851,6 +851,8 @@ __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, boo
 struct Fp4Args {
   const uint4 *q, *k, *v;
   int N, M, N_pad, M_pad, Tm, flags;
+  int Hq, Hkv;
+  const VarSeq *seq;  // packed sequences (kVar instances)
   uint8_t *qhat, *khat, *vhat, *qsf, *ksf, *vsf;
   const float *kbar, *vm;
   float *qbar;
@@ -858,18 +860,27 @@ struct Fp4Args {
   int nq, nk;
 };
 
-template <int D>
+// kVar: packed sequences (each sequence's own lengths, packed [total, H, d] inputs)
+template <int D, bool kVar>
 __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
   int cta = blockIdx.x;
   if (cta < a.nq) {
     // ---- Q block (b, h, i) of 128 rows, optional per-block mean
     const int i = cta % a.Tm, bh = cta / a.Tm;
     const int r0 = i * 128;
-    const int valid = max(0, min(128, a.N - r0));
-    fp4_row_block<D>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, (a.flags & SAGE_SMOOTH_Q) && valid > 0,
-                     nullptr, a.qhat + ((size_t)bh * a.N_pad + r0) * (D / 2),
+    int Nb = a.N, stride = D / 8;
+    const uint4 *src = a.q + ((size_t)bh * a.N + r0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[bh / a.Hq];
+      Nb = sq.N;
+      stride = a.Hq * (D / 8);
+      src = a.q + ((size_t)(sq.q0 + r0) * a.Hq + bh % a.Hq) * (D / 8);
+    }
+    const int valid = max(0, min(128, Nb - r0));
+    fp4_row_block<D>(src, valid, (a.flags & SAGE_SMOOTH_Q) && valid > 0, nullptr,
+                     a.qhat + ((size_t)bh * a.N_pad + r0) * (D / 2),
                      a.qsf + ((size_t)bh * a.Tm + i) * (D / 64) * 512, a.qbar + ((size_t)bh * a.Tm + i) * D,
-                     a.status, 3);
+                     a.status, 3, stride);
     return;
   }
   cta -= a.nq;
@@ -878,10 +889,17 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
     // ---- K block (b, g, 128 rows) with k_bar over all tokens
     const int ch = cta % nchunk, hb = cta / nchunk;
     const int t0 = ch * 128;
-    const int valid = max(0, min(128, a.M - t0));
-    fp4_row_block<D>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, false, a.kbar + (size_t)hb * D,
-                     a.khat + ((size_t)hb * a.M_pad + t0) * (D / 2),
-                     a.ksf + ((size_t)hb * nchunk + ch) * (D / 64) * 512, nullptr, a.status, 1);
+    int Mb = a.M, stride = D / 8;
+    const uint4 *src = a.k + ((size_t)hb * a.M + t0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      stride = a.Hkv * (D / 8);
+      src = a.k + ((size_t)(sq.k0 + t0) * a.Hkv + hb % a.Hkv) * (D / 8);
+    }
+    const int valid = max(0, min(128, Mb - t0));
+    fp4_row_block<D>(src, valid, false, a.kbar + (size_t)hb * D, a.khat + ((size_t)hb * a.M_pad + t0) * (D / 2),
+                     a.ksf + ((size_t)hb * nchunk + ch) * (D / 64) * 512, nullptr, a.status, 1, stride);
     return;
   }
   cta -= a.nk;
@@ -892,13 +910,22 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
     const int t0 = ch * 128;
     constexpr int VPR = D / 8, RPP = kThreads / VPR;
     constexpr int CA = (D + 127) / 128;  // channel atoms
+    int Mb = a.M;  // this (b, kv-head)'s keys; rows hb * M + t, or (k0 + t) * Hkv + h packed
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
     __shared__ __nv_bfloat16 tile[128][D + 2];
     __shared__ float vmean[D];
     for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
     const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
     for (int r = rr; r < 128; r += RPP) {
       const int t = t0 + r;
-      const uint4 u = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + vc] : make_uint4(0, 0, 0, 0);
+      const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + vc : ((size_t)hb * a.M + t) * VPR + vc;
+      const uint4 u = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -911,10 +938,10 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const int t = t0 + tb * 16 + u;
-        g[u] = (t < a.M) ? __fsub_rn(__bfloat162float(tile[tb * 16 + u][c]), vmean[c]) : 0.0f;
+        g[u] = (t < Mb) ? __fsub_rn(__bfloat162float(tile[tb * 16 + u][c]), vmean[c]) : 0.0f;
         amax = fmaxf(amax, fabsf(g[u]));
       }
-      const bool any = t0 + tb * 16 < a.M;
+      const bool any = t0 + tb * 16 < Mb;
       const uint32_t sc = any ? nvfp4_scale(amax) : 0;
       const float d = e4m3_value(sc);
       uint32_t w0 = 0, w1 = 0;
@@ -923,12 +950,12 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 #pragma unroll
         for (int u = 0; u < 8; u += 2) {
           const int t = t0 + tb * 16 + u;
-          w0 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * u);
+          w0 |= (t < Mb ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * u);
         }
 #pragma unroll
         for (int u = 8; u < 16; u += 2) {
           const int t = t0 + tb * 16 + u;
-          w1 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * (u - 8));
+          w1 |= (t < Mb ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * (u - 8));
         }
       }
       // a token past M inside a pair contributes a zero nibble (its value is 0 anyway)
@@ -966,7 +993,6 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   const int n = s.B * s.Hkv * s.d;
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
   dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
-  if (mode == SAGE_NVFP4 && seq) return SAGE_ERR_UNSUPPORTED;  // packed sequences: INT8 / FP8 modes
   if (s.d == 64)
     launch_stats<64>(sg, flags, k, v, s.M, st, status, stream, seq, s.Hkv);
   else
@@ -985,6 +1011,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
     f.M_pad = L.M_pad;
     f.Tm = L.Tm;
     f.flags = flags;
+    f.Hq = s.Hq;
+    f.Hkv = s.Hkv;
+    f.seq = seq;
     f.qhat = (uint8_t *)(w + L.qhat);
     f.khat = (uint8_t *)(w + L.khat);
     f.vhat = (uint8_t *)(w + L.vhat);
@@ -1000,10 +1029,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
     const unsigned g4 = (unsigned)(f.nq + 2 * f.nk);  // Q blocks, K blocks, V chunks
     // the V-scale atoms of d = 64 use half their rows: clear them first
     if (s.d % 128 != 0 && cudaMemsetAsync(f.vsf, 0, L.stats - L.vsf, stream) != cudaSuccess) return SAGE_ERR_CUDA;
-    if (s.d == 64)
-      quantize_fp4_kernel<64><<<g4, kThreads, 0, stream>>>(f);
-    else
-      quantize_fp4_kernel<128><<<g4, kThreads, 0, stream>>>(f);
+    auto fk = seq ? (s.d == 64 ? quantize_fp4_kernel<64, true> : quantize_fp4_kernel<128, true>)
+                  : (s.d == 64 ? quantize_fp4_kernel<64, false> : quantize_fp4_kernel<128, false>);
+    fk<<<g4, kThreads, 0, stream>>>(f);
     return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
   }
   QuantArgs a;

@@ -186,8 +186,8 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
  * starting at 0 and non-decreasing; a sequence with queries needs keys, and a
  * causal mask (bottom-right aligned within each sequence) needs at least as many
  * keys as queries.  Each sequence is its own attention problem: its own means,
- * scales and query / key blocks, starting at its first token.  Modes 0, 1 and 3
- * (NVFP4: SAGE_ERR_UNSUPPORTED).
+ * scales and query / key blocks, starting at its first token.  Every mode
+ * (NVFP4 with 128-key tiles).
  * The workspace holds the batched layout of B = nseq, N = the longest query
  * run, M = the longest key run (so sage_workspace_layout of that shape
  * locates the codes), then the sequence and work-item tables; compute and

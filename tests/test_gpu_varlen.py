@@ -43,6 +43,7 @@ CASES = [
     ("fp8_gqa", 1, 3, False, 8, 2, 128, 128, [90, 256, 17], [1000, 40, 17]),
     ("sagebwd_causal", 3, 1, True, 4, 2, 64, 64, [150, 65, 1], [150, 300, 2]),
     ("int8_per_token_q", 0, 1 | 0x10, True, 2, 2, 128, 64, [129, 400], [129, 401]),
+    ("nvfp4_causal_smooth", 2, 3, True, 4, 2, 128, 128, [200, 1, 300], [260, 1, 900]),
 ]
 
 
@@ -61,6 +62,8 @@ def test_varlen_matches_oracle(sage, case):
     got = o.float().cpu().numpy()
     m = output_metrics(got, oracle.bf16_round(ref))
     assert m["max_rel"] <= 1e-2 and m["rel_l1"] <= 2e-3, m
+    if mode == 2:
+        return  # NVFP4 codes sit in scale-factor atoms; the batched tests check them
     # codes and scales, sequence by sequence, at its batch index of the padded workspace
     w = read_workspace(ws, mode)
     for s, qz in enumerate(quants):
