@@ -89,6 +89,8 @@ def lib():
             L.orc_sagebwd_backward.argtypes = [C.POINTER(_Shape), i32, i32, i32, i32, dbl, vp, vp,
                                                C.POINTER(_Quant), vp, vp, vp, vp, vp, vp, vp]
             L.orc_sagebwd_backward.restype = i32
+            L.orc_sagebwd_prepare.argtypes = [C.POINTER(_Shape), i32, vp, vp, vp, vp, vp]
+            L.orc_sagebwd_prepare.restype = i32
             L.orc_attn_exact_rows.argtypes = [C.POINTER(_Shape), i32, dbl, vp, vp, vp, vp, i64, vp]
             L.orc_attn_exact_rows.restype = i32
             _lib = L
@@ -278,6 +280,23 @@ def sagebwd_backward(shape, flags, bq, bk, causal, sm_scale, q, k, v, qz: Quant,
     if rc:
         raise OracleError("orc_sagebwd_backward rc=%d" % rc)
     return dq, dk, dv
+
+
+def sagebwd_prepare(shape, bq, o, dout):
+    """(dO codes int8 [B,Hq,N,d], dO block scales [B,Hq,Tm], D [B,Hq,N]) of the
+    SageBwd backward; o fp64 [B,Hq,N,d], dout bf16 [B,Hq,N,d]."""
+    B, Hq, Hkv, N, M, d = shape
+    Tm = -(-N // bq)
+    db = _bits(dout)
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    assert o.size == B * Hq * N * d and db.size == o.size
+    doc = np.zeros((B, Hq, N, d), np.int8)
+    dos = np.zeros((B, Hq, Tm), np.float32)
+    D = np.zeros((B, Hq, N), np.float64)
+    rc = lib().orc_sagebwd_prepare(C.byref(_shape(*shape)), bq, _p(o), _p(db), _p(doc), _p(dos), _p(D))
+    if rc:
+        raise OracleError("orc_sagebwd_prepare rc=%d" % rc)
+    return doc, dos, D
 
 
 def attn_exact_rows(shape, causal, sm_scale, q, k, v, rows) -> np.ndarray:

@@ -682,6 +682,45 @@ static double int8_code64(double x, double scale) {
   return r;
 }
 
+/* The backward's inputs of one head: dO^ per bq-row block (binary32, as Q
+ * in the forward: a pre-pass quantizer) and D_r = sum_e dO[r,e] O[r,e]. */
+static void sagebwd_prepare_head(const uint16_t *dO, const double *O, int N, int d, int bq, int8_t *doc,
+                                 float *dos, double *Dr) {
+  const int64_t Tm = cdiv(N, bq);
+  int64_t i;
+  int r, e;
+  for (i = 0; i < Tm; ++i) {
+    const int r0 = (int)(i * bq), r1 = (int)((i + 1) * bq < N ? (i + 1) * bq : N);
+    float amax = 0.0f;
+    for (r = r0; r < r1; ++r)
+      for (e = 0; e < d; ++e)
+        if (fabsf(bf16f(dO[(int64_t)r * d + e])) > amax) amax = fabsf(bf16f(dO[(int64_t)r * d + e]));
+    dos[i] = orc_int8_scale(amax);
+    for (r = r0; r < r1; ++r)
+      for (e = 0; e < d; ++e) doc[(int64_t)r * d + e] = (int8_t)orc_int8_code(bf16f(dO[(int64_t)r * d + e]), dos[i]);
+  }
+  for (r = 0; r < N; ++r) {
+    double acc = 0.0;
+    for (e = 0; e < d; ++e) acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * O[(int64_t)r * d + e];
+    Dr[r] = acc;
+  }
+}
+
+int orc_sagebwd_prepare(const orc_shape *s, int bq, const double *o, const uint16_t *dout, int8_t *doc,
+                        float *dos, double *D) {
+  const int64_t N = s->N, d = s->d, Tm = cdiv(s->N, bq);
+  int64_t bh, n;
+  int rc = check_shape(s, ORC_SAGEBWD_I8, bq, 64);
+  if (rc) return rc;
+  n = (int64_t)s->B * s->Hq * N * d;
+  for (bh = 0; bh < n; ++bh)
+    if (!in_range(bf16f(dout[bh]))) return ORC_ERR_RANGE;
+  for (bh = 0; bh < (int64_t)s->B * s->Hq; ++bh)
+    sagebwd_prepare_head(dout + bh * N * d, o + bh * N * d, (int)N, (int)d, bq, doc + bh * N * d, dos + bh * Tm,
+                         D + bh * N);
+  return ORC_OK;
+}
+
 int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int causal, double sm_scale,
                          const uint16_t *q, const uint16_t *k, const orc_quant *qz, const uint16_t *v,
                          const double *o, const uint16_t *dout, const double *lse, double *dq,
@@ -729,25 +768,8 @@ int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int caus
       int64_t i, j;
       int r, c, e;
 
-      /* dO^: per-block INT8 over each bq-row block, binary32, as Q in the
-       * forward (a pre-pass quantizer) */
-      for (i = 0; i < Tm; ++i) {
-        const int r0 = (int)(i * bq), r1 = (int)((i + 1) * bq < N ? (i + 1) * bq : N);
-        float amax = 0.0f;
-        for (r = r0; r < r1; ++r)
-          for (e = 0; e < d; ++e)
-            if (fabsf(bf16f(dO[(int64_t)r * d + e])) > amax) amax = fabsf(bf16f(dO[(int64_t)r * d + e]));
-        dos[i] = orc_int8_scale(amax);
-        for (r = r0; r < r1; ++r)
-          for (e = 0; e < d; ++e)
-            doc[(int64_t)r * d + e] = (int8_t)orc_int8_code(bf16f(dO[(int64_t)r * d + e]), dos[i]);
-      }
-      /* D_r = sum_e dO[r,e] O[r,e] */
-      for (r = 0; r < N; ++r) {
-        double acc = 0.0;
-        for (e = 0; e < d; ++e) acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * o[(bh * N + r) * d + e];
-        Dr[r] = acc;
-      }
+      /* dO^ per block and D_r = rowsum(dO o O) */
+      sagebwd_prepare_head(dO, o + bh * N * d, N, d, bq, doc, dos, Dr);
 
       for (j = 0; j < Tn; ++j) {
         const int t0 = (int)(j * bk), nk = (int)((j + 1) * bk < M ? bk : M - j * bk);

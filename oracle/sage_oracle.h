@@ -179,6 +179,13 @@ int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int caus
                          const double *o, const uint16_t *dout, const double *lse, double *dq,
                          double *dk, double *dv);
 
+/* The SageBwd backward's inputs (its pre-pass): dO^ INT8 per bq-row block
+ * (binary32: scale fl(max|dO_i|/127), code clamp(rint(fl(x/scale)))), as int8
+ * [B,Hq,N,d] with scales [B,Hq,Tm], and D [B,Hq,N] = rowsum(dO o O) in fp64; o is
+ * the forward output [B,Hq,N,d] in fp64.  orc_sagebwd_backward forms the same. */
+int orc_sagebwd_prepare(const orc_shape *s, int bq, const double *o, const uint16_t *dout, int8_t *doc,
+                        float *dos, double *D);
+
 /* Plain softmax(Q K^T sm_scale) V in fp64 on the bf16 inputs, same masks. */
 int orc_attn_exact_rows(const orc_shape *s, int causal, double sm_scale, const uint16_t *q,
                         const uint16_t *k, const uint16_t *v, const int64_t *rows, int64_t nrows,

@@ -105,8 +105,10 @@ MUTATIONS = [
     # SageBwd backward
     ("backward dS without D_i", "x = P[r * bk + c] * (dp - Dr[r0 + r]);", "x = P[r * bk + c] * dp;"),
     ("backward dS without P", "x = P[r * bk + c] * (dp - Dr[r0 + r]);", "x = (dp - Dr[r0 + r]);"),
-    ("backward D_i from dO alone", "acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * o[(bh * N + r) * d + e];",
+    ("backward D_i from dO alone", "acc += orc_bf16_decode(dO[(int64_t)r * d + e]) * O[(int64_t)r * d + e];",
      "acc += orc_bf16_decode(dO[(int64_t)r * d + e]);"),
+    ("backward dO block maximum of one row", "    for (r = r0; r < r1; ++r)\n      for (e = 0; e < d; ++e)\n        if (fabsf(bf16f(dO",
+     "    for (r = r0; r < r0 + 1; ++r)\n      for (e = 0; e < d; ++e)\n        if (fabsf(bf16f(dO"),
     ("backward P not normalised by lse", "pv = exp((s0 + ds) * sm_scale - lse[bh * N + r0 + r]);",
      "pv = exp((s0 + ds) * sm_scale);"),
     ("backward s_P divisor", "sP = pmax / 127.0;", "sP = pmax / 128.0;"),

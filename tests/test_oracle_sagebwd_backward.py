@@ -183,3 +183,21 @@ def test_gaussian_gradients_close_to_autograd(orc, causal):
         err[flags] = [_cos_err(dq, gq), _cos_err(dk, gk), _cos_err(dv, gv)]
     assert max(err[orc.SMOOTH_K]) < 2.5e-3, err
     assert err[0][0] > 3.0 * err[orc.SMOOTH_K][0], err
+
+
+def test_prepare_restated(orc):
+    """dO^: per bq-row block (ragged last block), scale fl(max|dO_i| / 127), codes
+    clamp(rint(fl(x / scale))) -- restated here in numpy binary32; D = rowsum(dO o O)."""
+    B, Hq, Hkv, N, M, d, bq = 1, 2, 1, 200, 64, 32, 64
+    rng = np.random.default_rng(31)
+    dout = bf16_tensor(rng.standard_normal((B, Hq, N, d)) * 3.0)
+    o = rng.standard_normal((B, Hq, N, d))
+    doc, dos, D = orc.sagebwd_prepare((B, Hq, Hkv, N, M, d), bq, o, dout)
+    x = f64(dout).astype(np.float32)
+    for i in range(-(-N // bq)):
+        blk = x[:, :, i * bq:(i + 1) * bq]
+        sc = (np.abs(blk).max(axis=(2, 3)) / np.float32(127)).astype(np.float32)
+        assert np.array_equal(dos[:, :, i], sc), i
+        want = np.clip(np.rint(blk / sc[:, :, None, None]), -127, 127).astype(np.int8)
+        assert np.array_equal(doc[:, :, i * bq:(i + 1) * bq], want), i
+    assert np.allclose(D, (f64(dout) * o).sum(-1), rtol=1e-13, atol=1e-13)
