@@ -23,7 +23,8 @@ STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3:
 
 EXPORTS = ["sage_workspace_bytes", "sage_workspace_layout", "sage_quantize_qkv", "sage_attn_fwd",
            "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str",
-           "sage_quantize_qkv_static_scratch", "sage_varlen_workspace_bytes", "sage_attn_varlen"]
+           "sage_quantize_qkv_static_scratch", "sage_varlen_workspace_bytes", "sage_attn_varlen",
+           "sage_bwd_prepare"]
 
 
 class SageError(RuntimeError):
@@ -43,7 +44,7 @@ class WsLayout(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
                                           "qsf", "ksf", "vsf", "stats", "status", "total")] + \
                [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")] + \
-               [(n, C.c_size_t) for n in ("dqt", "dvb", "lse")]
+               [(n, C.c_size_t) for n in ("dqt", "dvb", "lse", "doc", "dos", "drow")]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -72,6 +73,8 @@ def _load():
     L.sage_attn_varlen.argtypes = [i32, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp, vp, vp, sz,
                                    vp, vp]
     L.sage_attn_varlen.restype = i32
+    L.sage_bwd_prepare.argtypes = [P(Shape), i32, i32, i32, vp, vp, vp, sz, vp]
+    L.sage_bwd_prepare.restype = i32
     L.sage_read_status.restype = i32
     L.sage_status_str.argtypes, L.sage_status_str.restype = [i32], C.c_char_p
     return L
@@ -293,6 +296,26 @@ def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, sm_scale
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(ws.buf), need, _ptr(out), _stream(stream)),
            "sage_attn_varlen")
     return out, ws
+
+
+def sage_bwd_prepare(ws: Workspace, o, dout, stream=None):
+    """The SageBwd backward's inputs into a mode-3 workspace: dO codes and
+    scales, D = rowsum(dO o O); o and dout bf16 [B, Hq, N, d] on the device.
+    Returns views (dO codes as fp16 [B, Hq, N, d], scales [B, Hq, Tm], D [B, Hq, N])."""
+    if ws.mode != SAGE_SAGEBWD_I8:
+        raise ValueError("the backward's inputs live in a mode 3 (SageBwd) workspace")
+    s, L = ws.shape, ws.layout
+    want = (s.B, s.Hq, s.N, s.d)
+    for t, n in ((o, "o"), (dout, "dout")):
+        _bf16_cuda(t, n)
+        if tuple(t.shape) != want:
+            raise ValueError("%s must have the shape [B, Hq, N, d] = %s" % (n, want))
+    _check(lib.sage_bwd_prepare(C.byref(s), ws.mode, ws.bq, ws.bk, _ptr(o), _ptr(dout), _ptr(ws.buf),
+                                ws.buf.numel(), _stream(stream)), "sage_bwd_prepare")
+    doc = ws.region("doc", s.B * s.Hq * L.N_pad * s.d * 2).view(torch.float16).view(s.B, s.Hq, L.N_pad, s.d)
+    dos = ws.region("dos", s.B * s.Hq * L.Tm * 4).view(torch.float32).view(s.B, s.Hq, L.Tm)
+    drow = ws.region("drow", s.B * s.Hq * L.N_pad * 4).view(torch.float32).view(s.B, s.Hq, L.N_pad)
+    return doc[:, :, :s.N], dos, drow[:, :, :s.N]
 
 
 def sage_lse(ws: Workspace) -> torch.Tensor:

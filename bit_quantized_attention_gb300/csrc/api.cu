@@ -241,6 +241,18 @@ sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_se
   return launch_attn_q8(P.shape, causal, sm_scale, quant_mode, flags, bk, workspace, P.L, o, cs, var);
 }
 
+sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, int bk, const void *o,
+                             const void *dout, void *workspace, size_t workspace_bytes, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (quant_mode != SAGE_SAGEBWD_I8) return SAGE_ERR_UNSUPPORTED;
+  if (!o || !dout || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  return launch_bwd_prepare(*shape, o, dout, workspace, L, (cudaStream_t)stream);
+}
+
 sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,
                              int *code, int *site) {
   sage_ws_layout L;

@@ -40,6 +40,10 @@ sage_status launch_attn_q8_var(const sage_shape &s, int causal, float sm_scale, 
                                const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream,
                                const VarDev &var);
 
+// The SageBwd backward's pre-pass (quantize.cu): dO codes and scales, D.
+sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
+                               const sage_ws_layout &L, cudaStream_t stream);
+
 // Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
                             const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var = VarDev());

@@ -86,6 +86,10 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   L->dqt = take((size_t)(B * Hq * N_pad * 4));
   L->dvb = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hkv * Tn * 4) : 0);
   L->lse = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * 4) : 0);
+  // the backward's inputs (sage_bwd_prepare)
+  L->doc = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * d * 2) : 0);
+  L->dos = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * Tm * 4) : 0);
+  L->drow = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * 4) : 0);
   L->total = off;
   L->N_pad = (int)N_pad;
   L->M_pad = (int)M_pad;

@@ -971,6 +971,50 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 
 // Enqueue init, statistics, finalize and quantize on `stream`, with the
 // statistics scratch at `st`.
+// ------------------------------------------------------------------ SageBwd backward inputs
+// One CTA per 128-row block of one (b, head): dO^ with the Q quantizer (no
+// mean, scale fl(max|dO_i| / 127), the same binary32 steps, range check
+// included), then D_r = sum_c dO[r,c] O[r,c] in fp32, the VPR threads of a row
+// (consecutive lanes) combining their 8-channel partial sums by shuffles.
+template <int D>
+__global__ void __launch_bounds__(kThreads, kQuantCtas)
+    bwd_prepare_kernel(const uint4 *__restrict__ o, const uint4 *__restrict__ dout, int N, int N_pad, int Tm,
+                       uint8_t *doc, float *dos, float *drow, int *status) {
+  constexpr int VPR = D / 8, RPP = kThreads / VPR;
+  constexpr int kPool = qk_pool_bytes<D>();
+  __shared__ __align__(16) unsigned char pool[kPool];
+  const int i = blockIdx.x % Tm, bh = blockIdx.x / Tm;
+  const int r0 = i * 128;
+  const int valid = max(0, min(128, N - r0));
+  quant_block<D, true>(dout + ((size_t)bh * N + r0) * VPR, valid, 128, false, nullptr,
+                       doc + ((size_t)bh * N_pad + r0) * D * 2, dos + (size_t)bh * Tm + i, nullptr, status, 5, pool);
+  const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  for (int r = rr; r < 128; r += RPP) {  // every lane of a warp runs every shuffle
+    float acc = 0.0f;
+    if (r < valid) {
+      float a[8], g[8];
+      unpack_bf16x8(o[((size_t)bh * N + r0 + r) * VPR + vc], a);
+      unpack_bf16x8(dout[((size_t)bh * N + r0 + r) * VPR + vc], g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
+    }
+#pragma unroll
+    for (int x = 1; x < VPR; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+    if (vc == 0) drow[(size_t)bh * N_pad + r0 + r] = (r < valid) ? acc : 0.0f;
+  }
+}
+
+sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
+                               const sage_ws_layout &L, cudaStream_t stream) {
+  char *w = (char *)ws;
+  const unsigned grid = (unsigned)(s.B * s.Hq * L.Tm);
+  auto kern = s.d == 64 ? bwd_prepare_kernel<64> : bwd_prepare_kernel<128>;
+  kern<<<grid, kThreads, 0, stream>>>((const uint4 *)o, (const uint4 *)dout, s.N, L.N_pad, L.Tm,
+                                      (uint8_t *)(w + L.doc), (float *)(w + L.dos), (float *)(w + L.drow),
+                                      (int *)(w + L.status));
+  return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
 // the quantize instance of a request: head dim, mode (INT8 / E4M3 Q and K;
 // SageBwd V), per-row Q scales, packed sequences
 template <bool kVar>

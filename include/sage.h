@@ -111,12 +111,16 @@ typedef struct {
  *          INT8 codes as fp16 values)
  *   lse    [B*Hq*N_pad]   fp32 log-sum-exp of each row's scaled scores,
  *          ln sum_j exp(S_ij sm_scale) (mode 3; rows past N not written)
+ *   doc    [B*Hq*N_pad, d] dO codes, INT8 per 128-row block held as fp16 values
+ *   dos    [B*Hq*Tm]      their scales
+ *   drow   [B*Hq*N_pad]   D = rowsum(dO o O), fp32
+ *          (the SageBwd backward's inputs, written by sage_bwd_prepare; mode 3)
  * N_pad = N rounded up to 128, M_pad = M rounded up to 128, Tm = N_pad/bq,
  * Tn = ceil(M/bk). */
 typedef struct {
   size_t qhat, dq, qbar, khat, dk, kbar, vhat, dv, vm, qsf, ksf, vsf, stats, status, total;
   int N_pad, M_pad, Tm, Tn;
-  size_t dqt, dvb, lse;
+  size_t dqt, dvb, lse, doc, dos, drow;
 } sage_ws_layout;
 
 /* Workspace size in bytes for a shape and mode; 0 if the request is invalid
@@ -202,6 +206,16 @@ sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_se
                              int causal, float sm_scale, int quant_mode, int flags, int bq, int bk, const void *q,
                              const void *k, const void *v, void *workspace, size_t workspace_bytes, void *o,
                              sage_stream_t stream);
+
+/* The SageBwd backward's pre-pass (SageAttention3 summary, "SageBwd Backward
+ * Pass": dV takes P^T dO^ with dO INT8 per block, dS takes D = rowsum(dO o O)):
+ * reads o (the forward's bf16 output) and dout (the output gradient, bf16),
+ * both [B, Hq, N, d] contiguous, and writes doc / dos / drow of a mode-3
+ * workspace.  dO is quantized like Q (scale fl(max|dO_i|/127) per 128-row
+ * block, code rint(fl(x/scale))); D is summed in fp32.  A non-finite or
+ * |x| >= 2^16 gradient sets SAGE_ERR_RANGE in the status word. */
+sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, int bk, const void *o,
+                             const void *dout, void *workspace, size_t workspace_bytes, sage_stream_t stream);
 
 /* Copy the device status word back (blocking on that copy only): *code is a
  * sage_status (SAGE_OK, SAGE_ERR_RANGE or SAGE_ERR_TIMEOUT), *site says where

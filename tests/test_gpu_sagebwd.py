@@ -73,3 +73,24 @@ def test_sagebwd_attention_and_lse_match_oracle(sage, cfg):
 def test_sagebwd_rejects_128_key_tiles(sage):
     s = sage.Shape(1, 2, 2, 256, 256, 64)
     assert sage.sage_workspace_bytes(s, 3, 128, 128) == 0
+
+
+@pytest.mark.parametrize("cfg", [CASES[0], CASES[2]], ids=[CASES[0].name, CASES[2].name])
+def test_backward_inputs_match_oracle(sage, cfg):
+    """sage_bwd_prepare: dO codes and scales bit-identical to the oracle's
+    quantizer, D = rowsum(dO o O) within fp32 summation of d products."""
+    q, k, v = make_inputs(cfg)
+    ws, o, _ = _run(sage, cfg, q, k, v)
+    rng = np.random.default_rng(7)
+    dout = torch.from_numpy(rng.standard_normal((cfg.B, cfg.Hq, cfg.N, cfg.d)).astype(np.float32)).to(torch.bfloat16)
+    o_bf16 = torch.from_numpy(o.astype(np.float32)).to(torch.bfloat16)   # the forward's bf16 output
+    doc, dos, drow = sage.sage_bwd_prepare(ws, o_bf16.cuda(), dout.cuda())
+    torch.cuda.synchronize()
+    assert sage.sage_read_status(ws) == (0, 0)
+    shape = (cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d)
+    rc, rs, rD = oracle.sagebwd_prepare(shape, 128, o_bf16.double().numpy(), dout)
+    gc = doc.float().cpu().numpy()
+    assert np.array_equal(gc, rc.astype(np.float32))
+    assert np.array_equal(dos.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    gD = drow.cpu().numpy().astype(np.float64)
+    assert np.abs(gD - rD).max() <= 1e-5 * max(1.0, np.abs(rD).max())
