@@ -133,7 +133,6 @@ def shape_of(q: torch.Tensor, k: torch.Tensor) -> Shape:
     return Shape(B, Hq, Hkv, N, M, d)
 
 
-
 def sage_workspace_layout(shape: Shape, mode: int, bq: int, bk: int) -> WsLayout:
     L = WsLayout()
     _check(lib.sage_workspace_layout(C.byref(shape), mode, bq, bk, C.byref(L)), "sage_workspace_layout")

@@ -12,7 +12,7 @@ module imports nothing from the product or from the oracle.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 
 # quant_mode values (same meaning on both sides of the check)
 MODE_Q8_PV8 = 0     # INT8 per-block Q/K, FP8 E4M3 P~ (scale 1/448) and per-channel FP8 V
