@@ -24,6 +24,7 @@ P_DIRECT = 8  # NVFP4 ablation: phi on P~ directly (no level-1 scale)
 Q_PER_TOKEN = 0x10  # one Q scale per query row (INT8 / E4M3 modes)
 EXACT_QK, EXACT_PV = 0x100, 0x200
 EXACT_BWD = 0x400  # backward: P, dO, dS unquantized
+BWD_INT8_DP = 0x800  # backward ablation: dP = dO V^T from INT8 dO^ and V^
 
 _lock = threading.Lock()
 _lib = None

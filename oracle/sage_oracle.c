@@ -810,7 +810,9 @@ int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int caus
               }
             }
 
-          /* dP = dO V^T unquantized; dS = P o (dP - D) */
+          /* dP = dO V^T unquantized (ORC_BWD_INT8_DP, the ablation the pages
+           * measure against it: INT8 dO^ times the forward's INT8 V^, plus V_m);
+           * dS = P o (dP - D) */
           for (r = 0; r < nq; ++r)
             for (c = 0; c < bk; ++c) {
               double dp = 0.0, x;
@@ -818,9 +820,16 @@ int orc_sagebwd_backward(const orc_shape *s, int flags, int bq, int bk, int caus
                 dS[r * bk + c] = 0.0;
                 continue;
               }
-              for (e = 0; e < d; ++e)
-                dp += orc_bf16_decode(dO[(int64_t)(r0 + r) * d + e]) *
-                      orc_bf16_decode(v[(hk * M + t0 + c) * d + e]);
+              if (flags & ORC_BWD_INT8_DP) {
+                for (e = 0; e < d; ++e)
+                  dp += (double)doc[(int64_t)(r0 + r) * d + e] * (double)dos[i] *
+                        ((double)(int8_t)qz->vc[(hk * M + t0 + c) * d + e] * (double)qz->dvb[hk * Tn + j] +
+                         (double)qz->vm[hk * d + e]);
+              } else {
+                for (e = 0; e < d; ++e)
+                  dp += orc_bf16_decode(dO[(int64_t)(r0 + r) * d + e]) *
+                        orc_bf16_decode(v[(hk * M + t0 + c) * d + e]);
+              }
               x = P[r * bk + c] * (dp - Dr[r0 + r]);
               dS[r * bk + c] = x;
               if (fabs(x) > smax) smax = fabs(x);

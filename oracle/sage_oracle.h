@@ -69,6 +69,10 @@ extern "C" {
 #define ORC_EXACT_QK 0x100 /* S from the unrounded smoothed Q, K in fp64 */
 #define ORC_EXACT_PV 0x200 /* R from unquantized P~ and unquantized V' in fp64 */
 #define ORC_EXACT_BWD 0x400 /* backward: P, dO and dS unquantized in fp64 */
+/* backward ablation (SageAttention3 summary, "SageBwd Backward Pass and the
+ * Critical dOV^T Decision"): dP = dO V^T from INT8 dO^ and the forward's
+ * per-block INT8 V^ instead of the unquantized operands */
+#define ORC_BWD_INT8_DP 0x800
 
 /* error codes */
 #define ORC_OK 0

@@ -201,3 +201,23 @@ def test_prepare_restated(orc):
         want = np.clip(np.rint(blk / sc[:, :, None, None]), -127, 127).astype(np.int8)
         assert np.array_equal(doc[:, :, i * bq:(i + 1) * bq], want), i
     assert np.allclose(D, (f64(dout) * o).sum(-1), rtol=1e-13, atol=1e-13)
+
+
+def test_int8_dov_ablation_hurts_dq(orc):
+    """The pages' reason to keep dO V^T unquantized: with INT8 dO^ and V^ in dP,
+    dQ's error grows with V's channel means (the dO dV^T term does not average
+    out), while dK and dV stay put.  Measured here: dQ 1 - cos 1.6e-3 -> 2.5e-2
+    (V offsets N(0, 1)) -> 0.16 (N(0, 3^2)); dK, dV within 2x."""
+    shape = (1, 4, 2, 128, 192, 64)
+    B, Hq, Hkv, N, M, d = shape
+    q, k, v = rand_qkv(*shape, seed=13, koff=3.0, voff=3.0)
+    dout = bf16_tensor(np.random.default_rng(14).standard_normal((B, Hq, N, d)))
+    gq, gk, gv, o, _ = autograd(f64(q), f64(k), f64(v), f64(dout), False, 0.125)
+    qz, _, lse = _forward(orc, shape, orc.SMOOTH_K, 64, 64, False, 0.125, q, k, v)
+    err = {}
+    for flags in (orc.SMOOTH_K, orc.SMOOTH_K | orc.BWD_INT8_DP):
+        dq, dk, dv = orc.sagebwd_backward(shape, flags, 64, 64, False, 0.125, q, k, v, qz, o, dout, lse)
+        err[flags] = [_cos_err(dq, gq), _cos_err(dk, gk), _cos_err(dv, gv)]
+    base, int8 = err[orc.SMOOTH_K], err[orc.SMOOTH_K | orc.BWD_INT8_DP]
+    assert int8[0] > 20 * base[0], err
+    assert int8[1] < 2 * base[1] and int8[2] < 2 * base[2], err
