@@ -455,23 +455,3 @@ def test_simulator_statistics(orc):
     assert 0.5 * g["rel_l1_smooth_k"] < rel[orc.SMOOTH_K] < 2.0 * g["rel_l1_smooth_k"]
     assert rel[orc.SMOOTH_K] < 0.75 * rel[0]
 
-
-@pytest.mark.parametrize("mode,factor", [(0, 3.0), (2, 10.0)])
-def test_k_smoothing_ablation(orc, mode, factor):
-    """The pages' case for smoothing K: with channel offsets on K (shared by all
-    tokens) the per-block quantizers spend their range on the offsets.  Here,
-    offsets N(0, 10^2): INT8 1 - cos 2.9e-3 unsmoothed against 7.1e-4 smoothed,
-    NVFP4 0.33 against 0.019; without offsets smoothing changes nothing."""
-    shape = (1, 4, 2, 256, 256, 64)
-    bk = 64 if mode == 0 else 128
-    rows = np.arange(4 * 256)
-
-    def err(koff, flags):
-        q, k, v = rand_qkv(*shape, seed=41, koff=koff)
-        ref = orc.attn_exact_rows(shape, False, 0.125, q, k, v, rows)
-        qz = orc.quantize(shape, mode, flags, 128, bk, q, k, v)
-        got = orc.attn_rows(shape, mode, flags, 128, bk, False, 0.125, q, k, v, qz, rows)
-        return 1.0 - (got * ref).sum() / math.sqrt((got * got).sum() * (ref * ref).sum())
-
-    assert err(10.0, 0) > factor * err(10.0, orc.SMOOTH_K)
-    assert abs(err(0.0, 0) - err(0.0, orc.SMOOTH_K)) < 0.1 * err(0.0, orc.SMOOTH_K)
