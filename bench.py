@@ -69,8 +69,8 @@ def peak_source(mode: int, src: str, bf16: float) -> str:
 ATTN_KERNEL = {0: "attn_q8_kernel", 1: "attn_q8_kernel", 2: "attn_fp4_kernel"}
 # the files each attention kernel is compiled from (its DRAM traffic depends on
 # nothing else in the library)
-ATTN_SOURCES = {0: ("attn_q8.cu", "sm103.cuh", "layout.h", "launch.h"),
-                1: ("attn_q8.cu", "sm103.cuh", "layout.h", "launch.h"),
+ATTN_SOURCES = {0: ("attn_q8.cu", "attn_q8.cuh", "sm103.cuh", "layout.h", "launch.h"),
+                1: ("attn_q8.cu", "attn_q8.cuh", "sm103.cuh", "layout.h", "launch.h"),
                 2: ("attn_fp4.cu", "sm103.cuh", "layout.h", "launch.h")}
 
 
@@ -278,7 +278,8 @@ def workload_config(cfg):
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "N": cfg.N, "M": cfg.M, "d": cfg.d,
             "causal": cfg.causal, "quant_mode": ["int8_qk_fp8_pv", "fp8_qk_fp8_pv", "nvfp4"][cfg.mode],
             "flags": {"smooth_k": bool(cfg.flags & 1), "smooth_q": bool(cfg.flags & 2),
-                      "smooth_v": bool(cfg.flags & 4)},
+                      "smooth_v": bool(cfg.flags & 4), "p_direct": bool(cfg.flags & 8),
+                      "q_per_token": bool(cfg.flags & 0x10)},
             "bq": cfg.bq, "bk": cfg.bk,
             "l2": "inputs larger than L2 (%.0f MB of bf16 Q/K/V per step), no flush" % (
                 2.0 * cfg.d * (cfg.B * cfg.Hq * cfg.N + 2 * cfg.B * cfg.Hkv * cfg.M) / 1e6),
@@ -406,6 +407,66 @@ def run_gpu(args, cfg):
         pg.destroy_process_group()
 
 
+def run_ablation(args, cfg):
+    """The method's switches on one workload, timed like the bench (CUDA events,
+    inputs larger than L2): step = pre-pass + attention, and the attention
+    alone.  Prints a markdown table (no JSON line): Q / V smoothing on and off,
+    per-token Q scales, E4M3 Q/K, direct P~ (NVFP4), the tiles-in-turn softmax
+    schedule, and the SageBwd forward's quantizers on the same inputs."""
+    import torch
+
+    import bit_quantized_attention_gb300 as sage
+    from workload import make_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    qh, kh, vh = make_inputs(cfg)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    shape = sage.shape_of(q, k)
+    stream = torch.cuda.current_stream(dev)
+    variants = [("as configured", cfg, None)]
+    variants.append(("Q smoothing %s" % ("off" if cfg.flags & 2 else "on"), cfg.with_(flags=cfg.flags ^ 2), None))
+    variants.append(("V smoothing %s" % ("off" if cfg.flags & 4 else "on"), cfg.with_(flags=cfg.flags ^ 4), None))
+    if cfg.mode in (0, 1):
+        variants.append(("per-token Q scales", cfg.with_(flags=cfg.flags | 0x10), None))
+        variants.append(("tiles in turn", cfg, "1"))
+    if cfg.mode == 0:
+        variants.append(("E4M3 Q/K", cfg.with_(mode=1), None))
+        variants.append(("SageBwd forward (bk 64)", cfg.with_(mode=3, bk=64), None))
+    if cfg.mode == 2:
+        variants.append(("direct P~", cfg.with_(flags=cfg.flags | 8), None))
+        variants.append(("tiles in turn", cfg, "1"))
+    rows = []
+    for name, c, ping in variants:
+        if ping:
+            os.environ["SAGE_PINGPONG"] = ping
+        else:
+            os.environ.pop("SAGE_PINGPONG", None)
+        ws = sage.new_workspace(shape, c.mode, c.flags, c.bq, c.bk, dev)
+        o = torch.empty_like(q)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps + args.warmup)]
+        for i in range(args.steps + args.warmup):
+            evs[i][0].record(stream)
+            sage.sage_quantize_qkv(q, k, v, c.mode, c.flags, c.bq, c.bk, workspace=ws, stream=stream)
+            evs[i][1].record(stream)
+            sage.sage_attn_fwd(ws, c.causal, c.sm_scale, out=o, stream=stream)
+            evs[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        st = sage.sage_read_status(ws)
+        t = evs[args.warmup:]
+        step = sum(a.elapsed_time(c_) for a, _, c_ in t) / len(t)
+        attn = sum(b.elapsed_time(c_) for _, b, c_ in t) / len(t)
+        rows.append((name, c.mode, c.flags, c.bk, step, attn, st))
+        del ws
+    os.environ.pop("SAGE_PINGPONG", None)
+    base = rows[0]
+    print("| variant | mode | flags | bk | step ms | attention ms | attention vs as configured | status |")
+    print("|---|---|---|---|---|---|---|---|")
+    for name, m, f, bk, step, attn, st in rows:
+        print("| %s | %d | 0x%x | %d | %.3f | %.3f | %.3f | %s |" % (name, m, f, bk, step, attn, attn / base[5], st))
+
+
 def kernel_hash(files=None) -> str:
     """Hash of CUDA/C++ sources' code (the given csrc files, else all of them):
     comments dropped and whitespace runs collapsed, so an edit to the
@@ -436,6 +497,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     ap.add_argument("--heads", type=int, default=0, help="override Hq (Hkv scaled to keep the group size)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="time the method's switches on the workload and print a table (no JSON line)")
+    ap.add_argument("--flags", type=lambda x: int(x, 0), default=None,
+                    help="override the workload's flags (ablations: 1 smooth K, 2 smooth Q, 4 smooth V, "
+                         "8 direct P~ in the NVFP4 mode, 0x10 per-token Q scales)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -445,12 +511,18 @@ def main():
         cfg = cfg.with_(bk=args.bk)
     if args.batch:
         cfg = cfg.with_(B=args.batch)
+    if args.flags is not None:
+        cfg = cfg.with_(flags=args.flags)
     if args.heads:
         g = cfg.Hq // cfg.Hkv
         if args.heads % g:
             ap.error("--heads must be a multiple of the workload's group size %d" % g)
         cfg = cfg.with_(Hq=args.heads, Hkv=args.heads // g)
-    if args.impl == "reference":
+    if args.ablation:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_ablation(args, cfg)
+    elif args.impl == "reference":
         run_reference(args, cfg)
     else:
         import __graft_entry__

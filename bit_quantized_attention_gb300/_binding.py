@@ -15,14 +15,16 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsage.so")
 
-SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4 = 0, 1, 2
+SAGE_Q8_PV8, SAGE_QF8_PV8, SAGE_NVFP4, SAGE_SAGEBWD_I8 = 0, 1, 2, 3
 SAGE_SMOOTH_K, SAGE_SMOOTH_Q, SAGE_SMOOTH_V = 1, 2, 4
+SAGE_P_DIRECT, SAGE_Q_PER_TOKEN = 8, 0x10
 STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3: "SAGE_ERR_WORKSPACE",
           4: "SAGE_ERR_RANGE", 5: "SAGE_ERR_TIMEOUT", 6: "SAGE_ERR_CUDA"}
 
 EXPORTS = ["sage_workspace_bytes", "sage_workspace_layout", "sage_quantize_qkv", "sage_attn_fwd",
            "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str",
-           "sage_quantize_qkv_static_scratch"]
+           "sage_quantize_qkv_static_scratch", "sage_varlen_workspace_bytes", "sage_attn_varlen",
+           "sage_bwd_prepare"]
 
 
 class SageError(RuntimeError):
@@ -41,7 +43,8 @@ class Shape(C.Structure):
 class WsLayout(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm",
                                           "qsf", "ksf", "vsf", "stats", "status", "total")] + \
-               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")]
+               [(n, C.c_int) for n in ("N_pad", "M_pad", "Tm", "Tn")] + \
+               [(n, C.c_size_t) for n in ("dqt", "dvb", "lse", "doc", "dos", "drow")]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -65,6 +68,13 @@ def _load():
     L.sage_attn_host.argtypes = [P(Shape), i32, f32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     L.sage_attn_host.restype = i32
     L.sage_read_status.argtypes = [P(Shape), i32, i32, i32, vp, P(i32), P(i32)]
+    L.sage_varlen_workspace_bytes.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32, i32]
+    L.sage_varlen_workspace_bytes.restype = sz
+    L.sage_attn_varlen.argtypes = [i32, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                   vp, vp]
+    L.sage_attn_varlen.restype = i32
+    L.sage_bwd_prepare.argtypes = [P(Shape), i32, i32, i32, vp, vp, vp, sz, vp]
+    L.sage_bwd_prepare.restype = i32
     L.sage_read_status.restype = i32
     L.sage_status_str.argtypes, L.sage_status_str.restype = [i32], C.c_char_p
     return L
@@ -229,6 +239,92 @@ def sage_attn_host(shape: Shape, causal: bool, sm_scale: float, mode: int, flags
 
 def sage_status_str(code: int) -> str:
     return lib.sage_status_str(code).decode()
+
+
+def _cu(cu, name: str):
+    """cu_seqlens (ints, or a CPU int tensor) -> (ctypes int32 array, list)"""
+    if isinstance(cu, torch.Tensor):
+        if cu.is_cuda:
+            raise ValueError("%s must be on the host (the library sizes the work from it)" % name)
+        cu = cu.tolist()
+    vals = [int(x) for x in cu]
+    if len(vals) < 2:
+        raise ValueError("%s needs nseq + 1 >= 2 entries" % name)
+    return (C.c_int * len(vals))(*vals), vals
+
+
+def sage_varlen_workspace_bytes(cu_seqlens_q, cu_seqlens_k, Hq: int, Hkv: int, d: int, mode: int, bq: int = 128,
+                                bk: int = 64) -> int:
+    aq, lq = _cu(cu_seqlens_q, "cu_seqlens_q")
+    ak, lk = _cu(cu_seqlens_k, "cu_seqlens_k")
+    if len(lq) != len(lk):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    return int(lib.sage_varlen_workspace_bytes(len(lq) - 1, aq, ak, Hq, Hkv, d, mode, bq, bk))
+
+
+def sage_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, sm_scale: float, mode: int = SAGE_Q8_PV8,
+                     flags: int = SAGE_SMOOTH_K, bq: int = 128, bk: int = 64, out=None, stream=None):
+    """Packed sequences: q [total_q, Hq, d], k and v [total_k, Hkv, d] (bf16, CUDA,
+    contiguous), cu_seqlens on the host.  Returns (o [total_q, Hq, d], the
+    Workspace: the batched layout of (nseq, Hq, Hkv, longest query run, longest
+    key run, d), for sage_read_status and sage_lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not (t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3 and t.is_cuda):
+            raise ValueError("%s must be a contiguous 3-D bf16 CUDA tensor [total, H, d]" % n)
+    if tuple(v.shape) != tuple(k.shape) or q.shape[2] != k.shape[2]:
+        raise ValueError("v must have k's shape and q, k the same head dim")
+    aq, lq = _cu(cu_seqlens_q, "cu_seqlens_q")
+    ak, lk = _cu(cu_seqlens_k, "cu_seqlens_k")
+    if len(lq) != len(lk) or lq[-1] != q.shape[0] or lk[-1] != k.shape[0]:
+        raise ValueError("cu_seqlens must end at the packed lengths and have the same number of entries")
+    nseq, Hq, Hkv, d = len(lq) - 1, q.shape[1], k.shape[1], q.shape[2]
+    need = sage_varlen_workspace_bytes(lq, lk, Hq, Hkv, d, mode, bq, bk)
+    if need == 0:
+        raise SageError(2, "sage_varlen_workspace_bytes")
+    shape = Shape(nseq, Hq, Hkv, max(b - a for a, b in zip(lq, lq[1:])), max(b - a for a, b in zip(lk, lk[1:])), d)
+    L = sage_workspace_layout(shape, mode, bq, bk)
+    buf = torch.empty(need + 1024, dtype=torch.uint8, device=q.device)
+    off = (-buf.data_ptr()) % 1024
+    ws = Workspace(buf[off:off + need], shape, mode, flags, bq, bk, L)
+    if out is None:
+        out = torch.empty_like(q)
+    elif not (out.dtype == torch.bfloat16 and out.is_contiguous() and tuple(out.shape) == tuple(q.shape)
+              and out.device == q.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped and placed like q")
+    _check(lib.sage_attn_varlen(nseq, aq, ak, Hq, Hkv, d, int(bool(causal)), float(sm_scale), mode, flags, bq, bk,
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(ws.buf), need, _ptr(out), _stream(stream)),
+           "sage_attn_varlen")
+    return out, ws
+
+
+def sage_bwd_prepare(ws: Workspace, o, dout, stream=None):
+    """The SageBwd backward's inputs into a mode-3 workspace: dO codes and
+    scales, D = rowsum(dO o O); o and dout bf16 [B, Hq, N, d] on the device.
+    Returns views (dO codes as fp16 [B, Hq, N, d], scales [B, Hq, Tm], D [B, Hq, N])."""
+    if ws.mode != SAGE_SAGEBWD_I8:
+        raise ValueError("the backward's inputs live in a mode 3 (SageBwd) workspace")
+    s, L = ws.shape, ws.layout
+    want = (s.B, s.Hq, s.N, s.d)
+    for t, n in ((o, "o"), (dout, "dout")):
+        _bf16_cuda(t, n)
+        if tuple(t.shape) != want:
+            raise ValueError("%s must have the shape [B, Hq, N, d] = %s" % (n, want))
+    _check(lib.sage_bwd_prepare(C.byref(s), ws.mode, ws.bq, ws.bk, _ptr(o), _ptr(dout), _ptr(ws.buf),
+                                ws.buf.numel(), _stream(stream)), "sage_bwd_prepare")
+    doc = ws.region("doc", s.B * s.Hq * L.N_pad * s.d * 2).view(torch.float16).view(s.B, s.Hq, L.N_pad, s.d)
+    dos = ws.region("dos", s.B * s.Hq * L.Tm * 4).view(torch.float32).view(s.B, s.Hq, L.Tm)
+    drow = ws.region("drow", s.B * s.Hq * L.N_pad * 4).view(torch.float32).view(s.B, s.Hq, L.N_pad)
+    return doc[:, :, :s.N], dos, drow[:, :, :s.N]
+
+
+def sage_lse(ws: Workspace) -> torch.Tensor:
+    """The per-row log-sum-exp the SageBwd forward (mode 3) wrote into the
+    workspace, ln sum_j exp(S_ij sm_scale), as a float32 view [B, Hq, N]."""
+    if ws.mode != SAGE_SAGEBWD_I8:
+        raise ValueError("the log-sum-exp is written by the SageBwd forward (mode 3) only")
+    s, L = ws.shape, ws.layout
+    t = ws.region("lse", s.B * s.Hq * L.N_pad * 4).view(torch.float32)
+    return t.view(s.B, s.Hq, L.N_pad)[:, :, :s.N]
 
 
 def sage_attn(q, k, v, causal: bool, sm_scale: float, mode: int = SAGE_Q8_PV8, flags: int = SAGE_SMOOTH_K,

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -89,13 +90,22 @@ sage_status sage_workspace_layout(const sage_shape *shape, int quant_mode, int b
   return request_layout(shape, quant_mode, bq, bk, out);
 }
 
+// Flag bits: unknown bits are an invalid argument; per-token Q scales exist in
+// the INT8 / FP8 modes only (NVFP4 scales Q per 1x16 block already).
+static sage_status check_flags(int quant_mode, int flags) {
+  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V | SAGE_P_DIRECT | SAGE_Q_PER_TOKEN))
+    return SAGE_ERR_INVALID_ARG;
+  if ((flags & SAGE_Q_PER_TOKEN) && quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
+  return SAGE_OK;
+}
+
 sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags, int bq, int bk, const void *q,
                               const void *k, const void *v, void *workspace, size_t workspace_bytes,
                               sage_stream_t stream) {
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
@@ -106,7 +116,8 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
 // the causal alignment, and the NVFP4 kernel's 128-key tiles.
 static sage_status check_attn_args(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags,
                                    int bk) {
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  sage_status st = check_flags(quant_mode, flags);
+  if (st != SAGE_OK) return st;
   if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return SAGE_ERR_INVALID_ARG;
   if (causal && shape->N > shape->M) return SAGE_ERR_UNSUPPORTED;
   if (quant_mode == SAGE_NVFP4 && bk != 128) return SAGE_ERR_UNSUPPORTED;
@@ -118,7 +129,7 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!workspace || !o || !aligned16(o) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
   st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
@@ -134,7 +145,7 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  if (flags & ~(SAGE_SMOOTH_K | SAGE_SMOOTH_Q | SAGE_SMOOTH_V)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_flags(quant_mode, flags)) != SAGE_OK) return st;
   if (!q || !k || !v || !workspace) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
@@ -184,6 +195,62 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
   if (st != SAGE_OK) return st;
   if (cudaMemcpyAsync(o_host, dO, qn, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return SAGE_ERR_CUDA;
   return SAGE_OK;
+}
+
+size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,
+                                   int d, int quant_mode, int bq, int bk) {
+  VarlenPlan P;
+  if (plan_varlen(nseq, cu_seqlens_q, cu_seqlens_k, Hq, Hkv, d, quant_mode, bq, bk, 0, &P) != SAGE_OK) return 0;
+  sage_ws_layout L;
+  if (request_layout(&P.shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
+  return P.total;
+}
+
+sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv, int d,
+                             int causal, float sm_scale, int quant_mode, int flags, int bq, int bk, const void *q,
+                             const void *k, const void *v, void *workspace, size_t workspace_bytes, void *o,
+                             sage_stream_t stream) {
+  VarlenPlan P;
+  sage_status st = plan_varlen(nseq, cu_seqlens_q, cu_seqlens_k, Hq, Hkv, d, quant_mode, bq, bk, causal, &P);
+  if (st != SAGE_OK) return st;
+  sage_ws_layout L;
+  if ((st = request_layout(&P.shape, quant_mode, bq, bk, &L)) != SAGE_OK) return st;  // the int-range checks
+  if ((st = check_attn_args(&P.shape, causal, sm_scale, quant_mode, flags, bk)) != SAGE_OK) return st;
+  if (!q || !k || !v || !o || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)workspace & 1023))
+    return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < P.total) return SAGE_ERR_WORKSPACE;
+  // the sequence and work item tables, one host-to-device copy (from pageable
+  // memory: the call returns once the source has been staged)
+  char *ws = (char *)workspace;
+  std::vector<char> tabs(P.total - P.seq_off, 0);
+  memcpy(tabs.data(), P.seqs.data(), sizeof(VarSeq) * P.seqs.size());
+  memcpy(tabs.data() + (P.item_off - P.seq_off), P.item_codes.data(), sizeof(int) * P.item_codes.size());
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(ws + P.seq_off, tabs.data(), tabs.size(), cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return SAGE_ERR_CUDA;
+  const VarSeq *seq = (const VarSeq *)(ws + P.seq_off);
+  st = launch_quantize_q8(P.shape, quant_mode, flags, bq, bk, q, k, v, workspace, P.L, cs, seq);
+  if (st != SAGE_OK) return st;
+  VarDev var;
+  var.item_tab = (const int *)(ws + P.item_off);
+  var.items = P.items;
+  var.seq = seq;
+  if (quant_mode == SAGE_NVFP4)
+    return launch_attn_fp4(P.shape, causal, sm_scale, flags, bk, workspace, P.L, o, cs, var);
+  return launch_attn_q8(P.shape, causal, sm_scale, quant_mode, flags, bk, workspace, P.L, o, cs, var);
+}
+
+sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, int bk, const void *o,
+                             const void *dout, void *workspace, size_t workspace_bytes, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (quant_mode != SAGE_SAGEBWD_I8) return SAGE_ERR_UNSUPPORTED;
+  if (!o || !dout || !workspace) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  return launch_bwd_prepare(*shape, o, dout, workspace, L, (cudaStream_t)stream);
 }
 
 sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,

@@ -7,6 +7,7 @@
 //   m_ij  = max(m_i,j-1, rowmax S_ij sm_scale),   P~ = exp(S sm_scale - m_ij)
 //   l_ij  = e^(m_i,j-1 - m_ij) l + rowsum P~        (unquantized P~)
 //   s_P1  = rowmax P~_ij / (448 * 6) = exp(rowmax S_ij sm_scale - m_ij) / 2688
+//           (1 under the direct-P~ ablation, which quantizes P~ itself)
 //   P2    = P~ / s_P1;  (s_P2, P2^) = phi(P2) over 1x16 blocks of keys
 //   R_ij  = FP4MMA(P2^, s_P2, V^_j, s_V)            tile partial, this tile only
 //   O_ij  = e^(m_i,j-1 - m_ij) O_i,j-1 + s_P1 R_ij  FP32 running output
@@ -31,6 +32,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "layout.h"
 #include "launch.h"
@@ -53,7 +55,10 @@ constexpr float kLog2_2688 = 11.392317422778762f;
 // named barriers (0 is __syncthreads): 1 + half, one softmax warpgroup (dS)
 constexpr int kBarDs0 = 1;
 
-template <int D>
+// kPing: the softmax warpgroups take whole key tiles in turn (one more
+// [NB][128] float array: each tile's row sum, from which the accumulation
+// warpgroup keeps l)
+template <int D, bool kPing = false>
 struct Fp4Cfg {
   static constexpr int QROW = D / 2;  // bytes per Q / K row (packed E2M1)
   static constexpr int QK_SW = QROW;  // 64-byte (d=128) or 32-byte (d=64) swizzle
@@ -69,7 +74,7 @@ struct Fp4Cfg {
   static constexpr int FIXED = Q_BYTES + QSF_BYTES + NB * (P_BYTES + PSF_BYTES);
   static constexpr int STAGES = 4;
   static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 128 /*s_P1*/ + 2 * 128 /*l*/ + 4 * 128 /*max*/ +
-                                2 * D + 4 * BK /*dS*/;
+                                2 * D + 4 * BK /*dS*/ + (kPing ? NB * 128 : 0) /*row sums*/;
   static constexpr int SMEM_TOTAL = 1024 + FIXED + STAGES * STAGE + NFLOAT * 4 + 512;
   static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory");
   // TMEM columns: NB S/R regions, then scale factors, 4 columns per 64-wide K
@@ -102,13 +107,17 @@ struct Fp4Params {
   __nv_bfloat16 *o;
   int *status;
   long long spin;
+  // packed sequences (kVar): block b of the grid takes work item item_tab[b]
+  // (code bh * Tm + qi); seq holds each sequence's lengths and first rows
+  const int *item_tab;
+  const VarSeq *seq;
 };
 
-template <int D>
+template <int D, bool kPing, bool kVar>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fp4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Fp4Params p) {
-  using C = Fp4Cfg<D>;
+  using C = Fp4Cfg<D, kPing>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -127,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_vm = s_mx + 4 * 128;                          // [D]
   float *s_qbar = s_vm + D;                              // [D]
   float *s_dsc = s_qbar + D;                             // [2 buffers][2 halves][BK]
-  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_dsc + 4 * BK) + 7) & ~(uintptr_t)7);
+  float *s_rs = s_dsc + 4 * BK;                          // [NB][128] row sums (tiles in turn)
+  uint64_t *bars = (uint64_t *)(((uintptr_t)(s_rs + (kPing ? NB * 128 : 0)) + 7) & ~(uintptr_t)7);
   uint64_t *q_full = bars;
   uint64_t *k_full = q_full + 1;     // [ST]
   uint64_t *v_full = k_full + ST;    // [ST]
@@ -143,14 +153,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.Tm;
-  const int qi = p.Tm - 1 - blockIdx.x % p.Tm;  // longest causal rows first
+  // this block's query block: longest causal rows first (batched: by block
+  // index; packed sequences: the table's order); Nq, Mk its sequence's counts
+  int bh, qi, Nq = p.N, Mk = p.M, q0 = 0;
+  if constexpr (kVar) {
+    const int code = p.item_tab[blockIdx.x];
+    bh = code / p.Tm;
+    qi = code % p.Tm;
+    const VarSeq sq = p.seq[bh / p.Hq];
+    Nq = sq.N;
+    Mk = sq.M;
+    q0 = sq.q0;
+  } else {
+    bh = blockIdx.x / p.Tm;
+    qi = p.Tm - 1 - blockIdx.x % p.Tm;
+  }
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int hkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int row0 = qi * 128;
-  const int last_row = min(p.N, row0 + 128) - 1;
-  const int T = p.causal ? min(p.Tn, (last_row + p.M - p.N) / BK + 1) : p.Tn;
+  const int last_row = min(Nq, row0 + 128) - 1;
+  const int Tn = kVar ? (Mk + BK - 1) / BK : p.Tn;
+  const int T = p.causal ? min(Tn, (last_row + Mk - Nq) / BK + 1) : Tn;
   const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
+  const bool direct = (p.flags & SAGE_P_DIRECT) != 0;  // phi on P~ itself (ablation)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -161,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < NB; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 2 * kWG);
+      mbar_init(&p_full[x], kPing ? kWG : 2 * kWG);  // one or both softmax warpgroups
       mbar_init(&r_full[x], 1);
       mbar_init(&sr_free[x], kWG);
     }
@@ -298,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float o[D];  // this thread's row of the FP32 running output
 #pragma unroll
     for (int c = 0; c < D; ++c) o[c] = 0.0f;
+    float lsum = 0.0f;  // l, kept here when the softmax warpgroups take tiles in turn
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int b = j % NB;
@@ -310,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float a = s_alpha[b * 128 + r], sp1 = s_sp1[b * 128 + r];
+      if constexpr (kPing) lsum = fmaf(a, lsum, s_rs[b * 128 + r]);
       const float2 a2 = make_float2(a, a), sp2 = make_float2(sp1, sp1);
       const uint32_t tR = tmem + lane_off + b * C::SRW;
 #pragma unroll
@@ -331,9 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O / l + V_m in bf16
     if (ok && T >= 1) {
       const int row = row0 + r;
-      if (row < p.N) {
-        const float inv_l = 1.0f / (s_l[r] + s_l[128 + r]);
-        __nv_bfloat16 *dst = p.o + ((size_t)bh * p.N + row) * D;
+      if (row < Nq) {
+        const float inv_l = 1.0f / (kPing ? lsum : s_l[r] + s_l[128 + r]);
+        // the output row: batched [B, Hq, N, d], or packed [total_q, Hq, d]
+        __nv_bfloat16 *dst = kVar ? p.o + ((size_t)(q0 + row) * p.Hq + h) * D : p.o + ((size_t)bh * p.N + row) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 8) {
           uint32_t w[4];
@@ -347,13 +375,182 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if constexpr (kPing) {
+    reg_alloc<kSoftmaxRegs>();
+    // ------------------------------------------------------------ softmax + two-level P, whole tiles in turn
+    // Warpgroup w takes tiles j with j % 2 == w, all BK keys of its rows,
+    // streamed from TMEM in 32-column chunks twice: the 16-key block maxima
+    // first, then P2 and its E2M1 codes.  Only the running maximum passes
+    // between the warpgroups (s_mx[j % NB] and mx_full[j % NB], published
+    // before the exponentials); the tile's row sum goes to the accumulation
+    // warpgroup (s_rs), which keeps l.  With Q smoothing the warpgroup computes
+    // the tile's dS for all its keys first (thread r takes key r), into a
+    // buffer of its own that alternates between its tiles.
+    static_assert(NB % 2 == 1, "the reader of a running maximum is its next writer");
+    const int r = threadIdx.x & (kWG - 1);
+    const int wg = warp >> 2;
+    const uint32_t tS0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int diag = row0 + r + Mk - Nq;  // last key visible to this row (causal)
+    const float c2 = p.sm_log2;
+    const float xs = smooth_q ? 1.0f : c2;  // x -> t
+    bool stop = false;  // a wait failed late in this warp's previous tile
+    for (int j = wg; j < T; j += 2) {
+      const int bb = j % NB;
+      float *dsc = s_dsc + (((j >> 1) & 1) * 2 + wg) * BK;
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], (j / NB) & 1, status, 32, s_abort, p.spin));
+      if (smooth_q) {
+        const int s = j % ST;
+        const bool fail = stop || !mbar_wait(&k_full[s], (j / ST) & 1, status, 31, s_abort, p.spin);
+        if (!fail) {
+          const int key = r;
+          const uint8_t *kt = sK + s * C::K_BYTES;
+          const uint8_t *ksf = sKsf + s * C::QSF_BYTES;
+          float acc = 0.0f;
+#pragma unroll
+          for (int c16 = 0; c16 < C::QROW / 16; ++c16) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(kt + swz_off<C::QK_SW>(key, c16));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int blk = c16 * 2 + hb;  // 16-channel block
+              const float sc = e4m3_to_float(ksf[(blk >> 2) * 512 + (key & 31) * 16 + (key >> 5) * 4 + (blk & 3)]);
+              float part = 0.0f;
+#pragma unroll
+              for (int q4 = 0; q4 < 2; ++q4) {
+                uint32_t hv[4];
+                cvt_e2m1x8_to_f16(ww[hb * 2 + q4], hv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hv[e]));
+                  const int d0 = blk * 16 + q4 * 8 + 2 * e;
+                  part = fmaf(s_qbar[d0], f.x, part);
+                  part = fmaf(s_qbar[d0 + 1], f.y, part);
+                }
+              }
+              acc = fmaf(part, sc, acc);
+            }
+          }
+          dsc[key] = acc * c2;
+        }
+        // the warpgroup leaves together: a warp that stopped alone would strand
+        // the others at this barrier in its next tile
+        if (named_bar_any(kBarDs0 + wg, kWG, stop || fail || !okw || *s_abort)) break;
+      } else if (stop || !okw) {
+        break;
+      }
+      tc_fence_after();
+      const int lim = (p.causal ? min(Mk, diag + 1) : Mk) - j * BK;  // tile keys >= lim are invisible
+      const bool edge = (j * BK + BK > Mk) || (p.causal && j * BK + BK - 1 > row0 + Mk - Nq);
+      const uint32_t tSb = tS0 + bb * C::SRW;
+      // pass 1: 16-key block maxima in x (raw S, or t with dS)
+      float bm[BK / 16];
+#pragma unroll
+      for (int ch = 0; ch < BK / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tSb + ch * 32, v);
+        tmem_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          x[e] = __uint_as_float(v[e]);
+          if (smooth_q) x[e] = fmaf(x[e], c2, dsc[ch * 32 + e]);
+          if (edge && ch * 32 + e >= lim) x[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          float a = fmax3(x[16 * g], x[16 * g + 1], x[16 * g + 2]);
+#pragma unroll
+          for (int u = 3; u < 15; u += 2) a = fmax3(a, x[16 * g + u], x[16 * g + u + 1]);
+          bm[2 * ch + g] = fmaxf(a, x[16 * g + 15]);
+        }
+      }
+      float mx = bm[0];
+#pragma unroll
+      for (int g = 1; g < BK / 16; ++g) mx = fmaxf(mx, bm[g]);
+      const float mt = (mx == -INFINITY) ? -INFINITY : mx * xs;  // row max of t over the tile
+      float m_prev = -INFINITY;
+      if (j > 0) {
+        const int pb = (j - 1) % NB;
+        if (!__all_sync(0xffffffffu, mbar_wait(&mx_full[pb], ((j - 1) / NB) & 1, status, 33, s_abort, p.spin))) {
+          stop = true;
+          if (!smooth_q) break;
+          continue;  // leave with the warpgroup at the next dS barrier
+        }
+        m_prev = s_mx[pb * 128 + r];
+      }
+      const float m_new = fmaxf(m_prev, mt);
+      s_mx[bb * 128 + r] = m_new;
+      mbar_arrive(&mx_full[bb]);
+      const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m_prev - m_new);
+      const bool any = mt != -INFINITY;
+      const float sp1 = !any ? 0.0f : direct ? 1.0f : ex2_approx(mt - m_new) * (1.0f / 2688.0f);
+      // P2 = P~ / s_P1 = exp2(t - bias): 2688 exp2(t - m_tile), or P~ itself
+      // (direct); nothing visible -> every P2 is 0
+      const float bias = !any ? INFINITY : direct ? m_new : mt - kLog2_2688;
+      float mult[BK / 16];
+      uint32_t scw[BK / 64];
+#pragma unroll
+      for (int q = 0; q < BK / 64; ++q) scw[q] = 0;
+#pragma unroll
+      for (int g = 0; g < BK / 16; ++g) {
+        // s_P2 = E4M3(max P2 / 6) from the block's largest score
+        const float amax = (bm[g] == -INFINITY) ? 0.0f : ex2_approx(fmaf(bm[g], xs, -bias));
+        const uint32_t sc = cvt_e4m3x2(amax * (1.0f / 6.0f), 0.0f) & 0xFF;
+        const float s2 = e4m3_to_float(sc);
+        mult[g] = s2 > 0.0f ? __fdividef(1.0f, s2) : 0.0f;
+        scw[g >> 2] |= sc << (8 * (g & 3));
+      }
+      // pass 2: P2, its E2M1 codes (32 keys = one 16-byte chunk of the 64-byte row)
+      uint8_t *prow = sP + bb * C::P_BYTES;
+      float2 rs2 = make_float2(0.0f, 0.0f);
+      const float2 xs2 = make_float2(xs, xs), nb2 = make_float2(-bias, -bias);
+#pragma unroll
+      for (int ch = 0; ch < BK / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tSb + ch * 32, v);
+        tmem_wait_ld();
+        float qv[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+          if (smooth_q) {
+            x0 = fmaf(x0, c2, dsc[ch * 32 + e]);
+            x1 = fmaf(x1, c2, dsc[ch * 32 + e + 1]);
+          }
+          if (edge) {
+            x0 = (ch * 32 + e < lim) ? x0 : -INFINITY;
+            x1 = (ch * 32 + e + 1 < lim) ? x1 : -INFINITY;
+          }
+          const float2 arg = __ffma2_rn(make_float2(x0, x1), xs2, nb2);
+          const float p0 = ex2_approx(arg.x), p1 = ex2_approx(arg.y);
+          rs2 = __fadd2_rn(rs2, make_float2(p0, p1));
+          const float mu = mult[2 * ch + (e >> 4)];
+          qv[e] = p0 * mu;
+          qv[e + 1] = p1 * mu;
+        }
+        const uint32_t w0 = cvt_e2m1x8(qv[0], qv[1], qv[2], qv[3], qv[4], qv[5], qv[6], qv[7]);
+        const uint32_t w1 = cvt_e2m1x8(qv[8], qv[9], qv[10], qv[11], qv[12], qv[13], qv[14], qv[15]);
+        const uint32_t w2 = cvt_e2m1x8(qv[16], qv[17], qv[18], qv[19], qv[20], qv[21], qv[22], qv[23]);
+        const uint32_t w3 = cvt_e2m1x8(qv[24], qv[25], qv[26], qv[27], qv[28], qv[29], qv[30], qv[31]);
+        *reinterpret_cast<uint4 *>(prow + swz_off<64>(r, ch)) = make_uint4(w0, w1, w2, w3);
+      }
+#pragma unroll
+      for (int q = 0; q < BK / 64; ++q)
+        *reinterpret_cast<uint32_t *>(sPsf + bb * C::PSF_BYTES + q * 512 + (r & 31) * 16 + (r >> 5) * 4) = scw[q];
+      s_alpha[bb * 128 + r] = alpha;
+      s_sp1[bb * 128 + r] = sp1;
+      s_rs[bb * 128 + r] = sp1 * (rs2.x + rs2.y);  // this tile's sum of P~ against m_new
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[bb]);
+    }
   } else {
     reg_alloc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax + two-level P quantization
     const int r = threadIdx.x & (kWG - 1);
     const int hf = warp >> 2;  // which half of the key tile
     const uint32_t tS0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int diag = row0 + r + p.M - p.N;  // last key visible to this row (causal)
+    const int diag = row0 + r + Mk - Nq;  // last key visible to this row (causal)
     const float c2 = p.sm_log2;
     float m = -INFINITY, l = 0.0f;
     bool stop = false;  // a wait failed late in the previous tile
@@ -412,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // m_tile then enters as one factor, P2 = 2688 exp2(t - m_tile) =
       // e * 2688 exp2(m_half - m_tile), so neither half waits on the other
       // before its exponentials.
-      const int lim = (p.causal ? min(p.M, diag + 1) : p.M) - j * BK;  // tile keys >= lim are invisible
-      const bool edge = (j * BK + BK > p.M) || (p.causal && j * BK + BK - 1 > row0 + p.M - p.N);
+      const int lim = (p.causal ? min(Mk, diag + 1) : Mk) - j * BK;  // tile keys >= lim are invisible
+      const bool edge = (j * BK + BK > Mk) || (p.causal && j * BK + BK - 1 > row0 + Mk - Nq);
       const int oh = hf ^ 1;
       float x[HALF];
       float bm[HALF / 16];
@@ -465,8 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m, mt);
       const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
       const bool any = mt != -INFINITY;
-      const float sp1 = any ? ex2_approx(mt - m_new) * (1.0f / 2688.0f) : 0.0f;
-      const float f = (any && mh != -INFINITY) ? ex2_approx(mht - mt) * 2688.0f : 0.0f;  // P2 = e f
+      // direct P~ (ablation): s_P1 = 1 and P2 = P~ = e exp2(m_half - m_new)
+      const float sp1 = !any ? 0.0f : direct ? 1.0f : ex2_approx(mt - m_new) * (1.0f / 2688.0f);
+      const float f = (!any || mh == -INFINITY) ? 0.0f
+                      : direct                 ? ex2_approx(mht - m_new)
+                                               : ex2_approx(mht - mt) * 2688.0f;  // P2 = e f
       uint8_t *prow = sP + bb * C::P_BYTES;
       uint32_t scw = 0;
       uint32_t pk[8];
@@ -517,10 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQkWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool kPing, bool kVar>
 sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags, const void *ws,
-                     const sage_ws_layout &L, void *o, cudaStream_t stream) {
-  using C = Fp4Cfg<D>;
+                     const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var) {
+  using C = Fp4Cfg<D, kPing>;
   const char *w = (const char *)ws;
   CUtensorMap tq, tk, tv;
   sage_status st;
@@ -550,24 +750,36 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
-  auto kern = attn_fp4_kernel<D>;
+  p.item_tab = var.item_tab;
+  p.seq = var.seq;
+  auto kern = attn_fp4_kernel<D, kPing, kVar>;
   // the register split assumes the block launches with kLaunchRegs per thread
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
   if (fa.numRegs != kLaunchRegs) return SAGE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL) != cudaSuccess)
     return SAGE_ERR_CUDA;
-  kern<<<(unsigned)(s.B * s.Hq * L.Tm), kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  const int blocks = kVar ? var.items : s.B * s.Hq * L.Tm;
+  if (blocks <= 0) return SAGE_OK;
+  kern<<<(unsigned)blocks, kThreads, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
 }  // namespace
 
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
-                            const sage_ws_layout &L, void *o, cudaStream_t stream) {
+                            const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var) {
   if (bk != BK) return SAGE_ERR_UNSUPPORTED;
-  return s.d == 64 ? launch_t<64>(s, causal, sm_scale, flags, ws, L, o, stream)
-                   : launch_t<128>(s, causal, sm_scale, flags, ws, L, o, stream);
+  if (var.item_tab)  // packed sequences: the split schedule
+    return s.d == 64 ? launch_t<64, false, true>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                     : launch_t<128, false, true>(s, causal, sm_scale, flags, ws, L, o, stream, var);
+  // whole key tiles in turn between the softmax warpgroups (SAGE_PINGPONG=1)
+  const char *pp = getenv("SAGE_PINGPONG");
+  if (pp && pp[0] == '1')
+    return s.d == 64 ? launch_t<64, true, false>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                     : launch_t<128, true, false>(s, causal, sm_scale, flags, ws, L, o, stream, var);
+  return s.d == 64 ? launch_t<64, false, false>(s, causal, sm_scale, flags, ws, L, o, stream, var)
+                   : launch_t<128, false, false>(s, causal, sm_scale, flags, ws, L, o, stream, var);
 }
 
 }  // namespace sage

@@ -4,13 +4,22 @@
 #include <cuda_runtime.h>
 
 #include "../../include/sage.h"
+#include "layout.h"
 
 namespace sage {
+
+// Packed-sequence tables in device memory (null for a batched request): the
+// work item codes, their count, and the per-sequence lengths / first rows.
+struct VarDev {
+  const int *item_tab = nullptr;
+  int items = 0;
+  const VarSeq *seq = nullptr;
+};
 
 // Pre-pass for SAGE_Q8_PV8 / SAGE_QF8_PV8 (quantize.cu).
 sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
                                const void *k, const void *v, void *ws, const sage_ws_layout &L,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const VarSeq *seq = nullptr);
 
 // Same pre-pass with its statistics scratch in a device array inside the
 // library (quantize.cu); B*Hkv*d must not exceed 32768.
@@ -20,11 +29,24 @@ sage_status launch_quantize_q8_static_scratch(const sage_shape &s, int mode, int
 
 // Attention for SAGE_Q8_PV8 / SAGE_QF8_PV8 (attn_q8.cu).
 sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
-                           const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream);
+                           const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream,
+                           const VarDev &var = VarDev());
+
+// The tiles-in-turn schedule (attn_q8_ping.cu) and packed sequences
+// (attn_q8_var.cu) of the same attention, called by launch_attn_q8.
+sage_status launch_attn_q8_ping(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
+                                const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream);
+sage_status launch_attn_q8_var(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bk,
+                               const void *ws, const sage_ws_layout &L, void *o, cudaStream_t stream,
+                               const VarDev &var);
+
+// The SageBwd backward's pre-pass (quantize.cu): dO codes and scales, D.
+sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
+                               const sage_ws_layout &L, cudaStream_t stream);
 
 // Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
-                            const sage_ws_layout &L, void *o, cudaStream_t stream);
+                            const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var = VarDev());
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (api.cu).
 // A 2-D byte tensor [rows][cols] with row pitch `pitch` bytes, box {box_cols, box_rows}.

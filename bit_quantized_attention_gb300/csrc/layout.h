@@ -4,6 +4,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "../../include/sage.h"
 
 namespace sage {
@@ -34,12 +37,14 @@ inline sage_status check_request(const sage_shape *s, int mode, int bq, int bk) 
   if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->N <= 0 || s->M <= 0 || s->d <= 0)
     return SAGE_ERR_INVALID_ARG;
   if (s->Hq % s->Hkv != 0) return SAGE_ERR_INVALID_ARG;
-  if (mode < SAGE_Q8_PV8 || mode > SAGE_NVFP4) return SAGE_ERR_INVALID_ARG;
+  if (mode < SAGE_Q8_PV8 || mode > SAGE_SAGEBWD_I8) return SAGE_ERR_INVALID_ARG;
   if (bq <= 0 || bk <= 0) return SAGE_ERR_INVALID_ARG;
   if (s->N > kMaxTokens || s->M > kMaxTokens) return SAGE_ERR_UNSUPPORTED;
   if (s->d != 64 && s->d != 128) return SAGE_ERR_UNSUPPORTED;
   if (bq != 128) return SAGE_ERR_UNSUPPORTED;
   if (bk != 64 && bk != 128) return SAGE_ERR_UNSUPPORTED;
+  // SageBwd: 16-bit P^ and V^ tiles fit the shared memory with 64-key tiles
+  if (mode == SAGE_SAGEBWD_I8 && bk != 64) return SAGE_ERR_UNSUPPORTED;
   if ((int64_t)s->B * s->Hq > (1 << 20) || (int64_t)s->B * s->Hkv > (1 << 20)) return SAGE_ERR_UNSUPPORTED;
   return SAGE_OK;
 }
@@ -50,9 +55,10 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   const int64_t B = s->B, Hq = s->Hq, Hkv = s->Hkv, d = s->d;
   const int64_t N_pad = align_up((size_t)s->N, 128), M_pad = align_up((size_t)s->M, 128);
   const int64_t Tm = N_pad / bq, Tn = cdiv(s->M, bk);
-  // bytes per stored code: fp16 integer (mode 0), E4M3 byte (1), packed E2M1 (2)
-  const double code_bytes = (mode == SAGE_Q8_PV8) ? 2.0 : (mode == SAGE_QF8_PV8 ? 1.0 : 0.5);
-  const double v_bytes = (mode == SAGE_NVFP4) ? 0.5 : 1.0;
+  // bytes per stored code: fp16 integer (modes 0, 3), E4M3 byte (1), packed E2M1 (2)
+  const bool i8 = (mode == SAGE_Q8_PV8 || mode == SAGE_SAGEBWD_I8);
+  const double code_bytes = i8 ? 2.0 : (mode == SAGE_QF8_PV8 ? 1.0 : 0.5);
+  const double v_bytes = (mode == SAGE_NVFP4) ? 0.5 : (mode == SAGE_SAGEBWD_I8 ? 2.0 : 1.0);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -77,11 +83,89 @@ inline sage_status compute_layout(const sage_shape *s, int mode, int bq, int bk,
   L->vsf = take(fp4 ? (size_t)(B * Hkv * cdiv(d, 128) * 128 * (M_pad / 16)) : 0);
   L->stats = take(stats_bytes(*s));
   L->status = take(16);
+  L->dqt = take((size_t)(B * Hq * N_pad * 4));
+  L->dvb = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hkv * Tn * 4) : 0);
+  L->lse = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * 4) : 0);
+  // the backward's inputs (sage_bwd_prepare)
+  L->doc = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * d * 2) : 0);
+  L->dos = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * Tm * 4) : 0);
+  L->drow = take(mode == SAGE_SAGEBWD_I8 ? (size_t)(B * Hq * N_pad * 4) : 0);
   L->total = off;
   L->N_pad = (int)N_pad;
   L->M_pad = (int)M_pad;
   L->Tm = (int)Tm;
   L->Tn = (int)Tn;
+  return SAGE_OK;
+}
+
+// ------------------------------------------------------------------ packed sequences
+// A packed-sequence request runs on the batched workspace layout with B = the
+// number of sequences, N = the longest query run and M = the longest key run:
+// sequence b's codes sit where batch b's would, so every tensor map and
+// workspace index stays as in the batched case, and each kernel takes the
+// sequence's own lengths from this table.  q0 / k0: the sequence's first row
+// in the packed [total, H, d] inputs.
+struct VarSeq {
+  int N, M, q0, k0;
+};
+
+struct VarlenPlan {
+  sage_shape shape;     // B = nseq, N = max query run, M = max key run
+  sage_ws_layout L;     // the batched layout of that shape
+  size_t seq_off;       // VarSeq[nseq], after the batched regions
+  size_t item_off;      // int[items]: work item codes bh * Tm + qi
+  size_t total;         // workspace bytes
+  int items;            // work items (query blocks of non-empty sequences)
+  std::vector<VarSeq> seqs;
+  std::vector<int> item_codes;
+};
+
+// Checks cu_seqlens (host, nseq + 1 entries each, starting at 0, non-decreasing,
+// every run within the token limit; a sequence with queries needs keys, and
+// under a causal mask at least as many keys as queries) and builds the plan:
+// work items longest first (most key tiles), as in the batched kernels.
+inline sage_status plan_varlen(int nseq, const int *cu_q, const int *cu_k, int Hq, int Hkv, int d, int mode,
+                               int bq, int bk, int causal, VarlenPlan *P) {
+  if (nseq <= 0 || !cu_q || !cu_k || !P) return SAGE_ERR_INVALID_ARG;
+  if (cu_q[0] != 0 || cu_k[0] != 0) return SAGE_ERR_INVALID_ARG;
+  int max_q = 0, max_k = 0;
+  P->seqs.assign((size_t)nseq, VarSeq{0, 0, 0, 0});
+  for (int b = 0; b < nseq; ++b) {
+    const long long nq = (long long)cu_q[b + 1] - cu_q[b], nk = (long long)cu_k[b + 1] - cu_k[b];
+    if (nq < 0 || nk < 0) return SAGE_ERR_INVALID_ARG;
+    if (nq > kMaxTokens || nk > kMaxTokens) return SAGE_ERR_UNSUPPORTED;
+    if (nq > 0 && nk == 0) return SAGE_ERR_INVALID_ARG;
+    if (causal && nq > nk) return SAGE_ERR_UNSUPPORTED;
+    P->seqs[b] = VarSeq{(int)nq, (int)nk, cu_q[b], cu_k[b]};
+    max_q = std::max(max_q, (int)nq);
+    max_k = std::max(max_k, (int)nk);
+  }
+  if (max_q == 0) return SAGE_ERR_INVALID_ARG;  // nothing to attend
+  P->shape = sage_shape{nseq, Hq, Hkv, max_q, max_k, d};
+  sage_status st = compute_layout(&P->shape, mode, bq, bk, &P->L);
+  if (st != SAGE_OK) return st;
+  const int Tm = P->L.Tm;
+  std::vector<std::pair<int, int>> work;  // (key tiles, code)
+  for (int b = 0; b < nseq; ++b) {
+    const VarSeq &q = P->seqs[b];
+    const int tm = (int)cdiv(q.N, 128), tn = (int)cdiv(q.M, bk);
+    for (int h = 0; h < Hq; ++h)
+      for (int i = 0; i < tm; ++i) {
+        const int last_row = std::min(q.N, i * 128 + 128) - 1;
+        const int T = causal ? std::min(tn, (last_row + q.M - q.N) / bk + 1) : tn;
+        work.emplace_back(T, (b * Hq + h) * Tm + i);
+      }
+  }
+  std::stable_sort(work.begin(), work.end(), [](const std::pair<int, int> &x, const std::pair<int, int> &y) {
+    return x.first > y.first;
+  });
+  if (work.size() >= ((size_t)1 << 31)) return SAGE_ERR_UNSUPPORTED;
+  P->items = (int)work.size();
+  P->item_codes.resize(work.size());
+  for (size_t i = 0; i < work.size(); ++i) P->item_codes[i] = work[i].second;
+  P->seq_off = P->L.total;
+  P->item_off = align_up(P->seq_off + sizeof(VarSeq) * (size_t)nseq, 1024);
+  P->total = align_up(P->item_off + sizeof(int) * work.size() + 4, 1024);
   return SAGE_OK;
 }
 

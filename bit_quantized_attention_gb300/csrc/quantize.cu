@@ -134,9 +134,13 @@ __global__ void init_kernel(StatsView st, int n, int *status) {
 // issued in batches of kBatch rows so several are in flight.  Min / max run
 // on packed bf16 pairs with NaN propagation (they are exact, and a NaN or an
 // out-of-range value shows in the extremes).
-template <int D, bool kSumK, bool kSumV>
+// Packed sequences (seq non-null): batch b is sequence b, its M its own key
+// count, and its rows sit at (k0 + t) * Hkv + h of the packed [total, Hkv, d]
+// inputs; CTAs past the sequence's keys have nothing to do.
+template <int D, bool kSumK, bool kSumV, bool kVar>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                                         int M, StatsView st, int *status) {
+                                                         int M, StatsView st, int *status, const VarSeq *seq,
+                                                         int Hkv) {
   constexpr int VPR = D / 8;               // 16-byte vectors per row (threads per row)
   constexpr int RPP = kThreads / VPR;      // rows per pass
   constexpr int kBatch = 4;
@@ -148,6 +152,15 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
   const int hb = blockIdx.y;
   const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
   const int t0 = blockIdx.x * kStatTokens;
+  // row of token t: hb * M + t (batched) or (k0 + t) * Hkv + h (packed)
+  long long row_base = (long long)hb * M, row_step = 1;
+  if constexpr (kVar) {
+    const VarSeq sq = seq[hb / Hkv];
+    M = sq.M;
+    row_base = (long long)sq.k0 * Hkv + hb % Hkv;
+    row_step = Hkv;
+    if (t0 >= M) return;  // the whole CTA: nothing of this sequence here
+  }
   const int t1 = min(M, t0 + kStatTokens);
   int klo[8], khi[8], vlo[8], vhi[8];
   __nv_bfloat162 kmn[4], kmx[4], vmn[4], vmx[4];
@@ -169,7 +182,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int t = tb + i * RPP;
-      const size_t off = ((size_t)hb * M + min(t, t1 - 1)) * VPR + vc;
+      const size_t off = kVar ? (size_t)(row_base + (long long)min(t, t1 - 1) * row_step) * VPR + vc
+                              : ((size_t)hb * M + min(t, t1 - 1)) * VPR + vc;
       kb[i] = k[off];
       vb[i] = v[off];
     }
@@ -263,26 +277,37 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const uint4 *__restrict
 
 template <int D>
 void launch_stats(dim3 grid, int flags, const void *k, const void *v, int M, StatsView st, int *status,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const VarSeq *seq, int Hkv) {
   const bool sk = (flags & SAGE_SMOOTH_K) != 0, sv = (flags & SAGE_SMOOTH_V) != 0;
   const uint4 *k4 = (const uint4 *)k, *v4 = (const uint4 *)v;
-  if (sk && sv)
-    stats_kernel<D, true, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
-  else if (sk)
-    stats_kernel<D, true, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
-  else if (sv)
-    stats_kernel<D, false, true><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+  using Kern = void (*)(const uint4 *, const uint4 *, int, StatsView, int *, const VarSeq *, int);
+  Kern kern;
+  if (seq)
+    kern = sk ? (sv ? stats_kernel<D, true, true, true> : stats_kernel<D, true, false, true>)
+              : (sv ? stats_kernel<D, false, true, true> : stats_kernel<D, false, false, true>);
   else
-    stats_kernel<D, false, false><<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status);
+    kern = sk ? (sv ? stats_kernel<D, true, true, false> : stats_kernel<D, true, false, false>)
+              : (sv ? stats_kernel<D, false, true, false> : stats_kernel<D, false, false, false>);
+  kern<<<grid, kThreads, 0, stream>>>(k4, v4, M, st, status, seq, Hkv);
 }
 
 // ------------------------------------------------------------------ finalize
 // One thread per (b, kv-head, channel): k_bar and V_m from the fixed-point
 // sums (when smoothed), and delta_V = max_t |fl(V - V_m)| / 448 from the channel
 // min and max (rounded subtraction is monotone).
-__global__ void finalize_kernel(StatsView st, int n, int M, int flags, float *kbar, float *vm, float *dv) {
+// Packed sequences: the mean of (b, h) is over sequence b's M (a sequence
+// with no keys has no mean and no use for one: 0).
+__global__ void finalize_kernel(StatsView st, int n, int M, int flags, float *kbar, float *vm, float *dv,
+                                const VarSeq *seq, int per_seq) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  if (seq) {
+    M = seq[i / per_seq].M;
+    if (M == 0) {
+      kbar[i] = vm[i] = dv[i] = 0.0f;
+      return;
+    }
+  }
   kbar[i] = (flags & SAGE_SMOOTH_K) ? mean_from_sum(st.ksum[i], M) : 0.0f;
   const float mu = (flags & SAGE_SMOOTH_V) ? mean_from_sum(st.vsum[i], M) : 0.0f;
   const float hi = order_val(st.vmax[i]), lo = order_val(st.vmin[i]);
@@ -297,6 +322,9 @@ struct QuantArgs {
   int mode, flags;
   uint8_t *qhat, *khat, *vhat;
   float *dq, *qbar, *dk, *kbar, *dv, *vm;
+  float *dqt;  // per-row Q scales (SAGE_Q_PER_TOKEN)
+  float *dvb;  // per-block V scales (SageBwd forward)
+  const VarSeq *seq;  // packed sequences: per-sequence lengths and first rows (null: batched)
   StatsView st;
   int *status;
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
@@ -384,6 +412,9 @@ __device__ __forceinline__ void encode8(const float (&f)[8], const float (&mu)[8
 // One block of `rows` rows (<= 128) of a [*, D] bf16 matrix: optional
 // per-block mean (fixed point over the valid rows) or a given mean, then the
 // per-block absmax scale and the codes.  Rows past `valid_rows` get code 0.
+// kPerRow: each row takes its own scale, max over its channels of
+// |fl(x - mu)| / 127 (or / 448), written to row_delta_out[r] (0 past
+// valid_rows), and *delta_out is 0.
 // The absmax max_r |fl(x_r - mu)| of a channel is taken from the channel's
 // extremes (rounded subtraction is monotone), which packed bf16 min / max
 // track exactly; they also carry the range check (NaN propagates).
@@ -395,10 +426,11 @@ __host__ __device__ constexpr int qk_pool_bytes() { return (kThreads / (D / 8)) 
 template <int D>
 __host__ __device__ constexpr int v_pool_bytes() { return 3 * D * 4 + D * 33 * 4; }
 
-template <int D, bool kInt8>
+template <int D, bool kInt8, bool kPerRow = false>
 __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int rows, bool own_mean,
                             const float *__restrict__ given_mean, uint8_t *dst, float *delta_out,
-                            float *mean_out, int *status, int site, unsigned char *pool) {
+                            float *mean_out, int *status, int site, unsigned char *pool,
+                            float *row_delta_out = nullptr, int src_stride = D / 8) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
   long long (*ssum)[D] = reinterpret_cast<long long (*)[D]>(pool);
   float *smean = reinterpret_cast<float *>(pool + RPP * D * 8);
@@ -411,7 +443,7 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
-    x[p] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+    x[p] = (r < valid_rows) ? src[(size_t)r * src_stride + vc] : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
@@ -463,10 +495,38 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
     }
     if (bad) raise_status(status, SAGE_ERR_RANGE, site);
   }
+  constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
+  if constexpr (kPerRow) {
+    // per-row scales: the VPR threads of a row are consecutive lanes of one
+    // warp (VPR divides 32), so the row maximum is a shuffle reduction; every
+    // lane runs every shuffle
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int r = rr + p * RPP;
+      float f[8];
+      unpack_bf16x8(x[p], f);
+      float am = 0.0f;
+      if (r < valid_rows) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(f[e], mu[e])));
+      }
+#pragma unroll
+      for (int o = 1; o < VPR; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float dr = __fdiv_rn(am, kInt8 ? 127.0f : 448.0f);
+      const float rc = __frcp_rn(dr);
+      if (r < rows) {
+        encode8<kInt8>(f, mu, dr, rc, r < valid_rows && dr != 0.0f, dst + ((size_t)r * D + vc * 8) * CB);
+        if (vc == 0) row_delta_out[r] = dr;
+      }
+    }
+    if (threadIdx.x == 0) *delta_out = 0.0f;
+    if (mean_out)
+      for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
+    return;
+  }
   amax = block_max(amax, red);
   const float delta = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
   const float rcp = __frcp_rn(delta);
-  constexpr int CB = kInt8 ? 2 : 1;  // bytes per stored code
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int r = rr + p * RPP;
@@ -480,7 +540,11 @@ __device__ void quant_block(const uint4 *__restrict__ src, int valid_rows, int r
     for (int c = threadIdx.x; c < D; c += kThreads) mean_out[c] = smean[c];
 }
 
-template <int D, bool kInt8>
+// kPerRow: per-row Q scales (SAGE_Q_PER_TOKEN), an instance of its own so that
+// the per-block instances keep their register allocation.  kVBlk: the SageBwd
+// forward's V (per-block INT8 over 64-token blocks, fp16 integer codes).
+// kVar: packed sequences (per-sequence lengths, packed [total, H, d] inputs).
+template <int D, bool kInt8, bool kPerRow, bool kVBlk, bool kVar>
 __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArgs a) {
   constexpr int CB = kInt8 ? 2 : 1;
   constexpr int kPool = qk_pool_bytes<D>() > v_pool_bytes<D>() ? qk_pool_bytes<D>() : v_pool_bytes<D>();
@@ -490,12 +554,21 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     // ---- Q block (b, h, i)
     const int i = cta % a.Tm, bh = cta / a.Tm;
     const int r0 = i * 128;
-    const int valid = max(0, min(128, a.N - r0));
+    // rows of this block in the input: batched [B, Hq, N, d], or packed [total, Hq, d]
+    int Nb = a.N, stride = D / 8;
+    const uint4 *src = a.q + ((size_t)bh * a.N + r0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[bh / a.Hq];
+      Nb = sq.N;
+      stride = a.Hq * (D / 8);
+      src = a.q + ((size_t)(sq.q0 + r0) * a.Hq + bh % a.Hq) * (D / 8);
+    }
+    const int valid = max(0, min(128, Nb - r0));
     const bool smooth = (a.flags & SAGE_SMOOTH_Q) != 0;
     float *qbar = a.qbar + ((size_t)bh * a.Tm + i) * D;
-    quant_block<D, kInt8>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, 128, smooth && valid > 0, nullptr,
-                          a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i, qbar,
-                          a.status, 3, pool);
+    quant_block<D, kInt8, kPerRow>(src, valid, 128, smooth && valid > 0, nullptr,
+                                   a.qhat + ((size_t)bh * a.N_pad + r0) * D * CB, a.dq + (size_t)bh * a.Tm + i,
+                                   qbar, a.status, 3, pool, a.dqt + (size_t)bh * a.N_pad + r0, stride);
     return;
   }
   cta -= a.nq;
@@ -503,13 +576,102 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
     // ---- K block (b, g, j): k_bar over all tokens from the finalize pass
     const int j = cta % a.Tn, hb = cta / a.Tn;
     const int t0 = j * a.bk;
-    const int valid = max(0, min(a.bk, a.M - t0));
-    quant_block<D, kInt8>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, a.bk, false, a.kbar + (size_t)hb * D,
+    int Mb = a.M, stride = D / 8;
+    const uint4 *src = a.k + ((size_t)hb * a.M + t0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      stride = a.Hkv * (D / 8);
+      src = a.k + ((size_t)(sq.k0 + t0) * a.Hkv + hb % a.Hkv) * (D / 8);
+    }
+    const int valid = max(0, min(a.bk, Mb - t0));
+    quant_block<D, kInt8>(src, valid, a.bk, false, a.kbar + (size_t)hb * D,
                           a.khat + ((size_t)hb * a.M_pad + t0) * D * CB, a.dk + (size_t)hb * a.Tn + j, nullptr,
-                          a.status, 1, pool);
+                          a.status, 1, pool, nullptr, stride);
     return;
   }
   cta -= a.nk;
+  if constexpr (kVBlk) {
+    // ---- V token chunk (b, g, 128 tokens), SageBwd forward (SageAttention3
+    // summary, "SageBwd Forward Pass"): the chunk holds two 64-token blocks;
+    // per block s_V = max |fl(V - V_m)| / 127 over its tokens and all
+    // channels, codes rint(fl(V' / s_V)) as fp16 integers written transposed
+    // (token-contiguous per channel).  Work item = 4 consecutive tokens x 8
+    // channels; the 32 lanes of a warp take 32 consecutive token groups of the
+    // same channels, so lanes 0-15 hold block 0 and 16-31 block 1, and each
+    // code store of a warp is 256 contiguous bytes.  Tokens past M get code 0
+    // (the attention's masked keys read them).  The raw rows stay in
+    // registers between the maximum and the codes.
+    constexpr int VPR = D / 8;
+    constexpr int IPT = 32 * VPR / kThreads;  // work items per thread
+    static_assert(IPT >= 1 && IPT * kThreads == 32 * VPR, "whole work items per thread");
+    const int nchunk = a.M_pad / 128;
+    const int ch = cta % nchunk, hb = cta / nchunk;
+    // this (b, kv-head)'s keys: batched rows hb * M + t, or packed (k0 + t) * Hkv + h
+    int Mb = a.M;
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
+    float *vmean = reinterpret_cast<float *>(pool);
+    unsigned *bmax = reinterpret_cast<unsigned *>(vmean + D);  // block maxima (non-negative floats as bits)
+    for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
+    if (threadIdx.x < 2) bmax[threadIdx.x] = 0u;
+    __syncthreads();
+    const int t0 = ch * 128;
+    const int tg = threadIdx.x & 31, blk = tg >> 4;  // token group (the lane) and its 64-token block
+    uint4 raw[IPT][4];
+    float am = 0.0f;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      const int cg = (threadIdx.x + k * kThreads) >> 5;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 4 * tg + u;
+        const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + cg : ((size_t)hb * a.M + t) * VPR + cg;
+        raw[k][u] = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
+        if (t < Mb) {
+          float f[8];
+          unpack_bf16x8(raw[k][u], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(f[e], vmean[cg * 8 + e])));
+        }
+      }
+    }
+    // half-warp maxima (lanes 0-15 block 0, 16-31 block 1), then one atomic each
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if ((tg & 15) == 0) atomicMax(&bmax[blk], __float_as_uint(am));
+    __syncthreads();
+    const float delta = __fdiv_rn(__uint_as_float(bmax[blk]), 127.0f);
+    const float rcp = __frcp_rn(delta);
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      const int cg = (threadIdx.x + k * kThreads) >> 5;
+      float f[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) unpack_bf16x8(raw[k][u], f[u]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float c4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          c4[u] = (delta != 0.0f && t0 + 4 * tg + u < Mb)
+                      ? int8_code(__fsub_rn(f[u][e], vmean[cg * 8 + e]), delta, rcp) : 0.0f;
+        const __half2 h01 = __floats2half2_rn(c4[0], c4[1]), h23 = __floats2half2_rn(c4[2], c4[3]);
+        *reinterpret_cast<uint2 *>(a.vhat + (((size_t)hb * D + cg * 8 + e) * a.M_pad + t0 + 4 * tg) * 2) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+      }
+    }
+    if (threadIdx.x < 2) {
+      const int j = t0 / 64 + threadIdx.x;  // 64-token block index
+      if (j < a.Tn) a.dvb[(size_t)hb * a.Tn + j] = __fdiv_rn(__uint_as_float(bmax[threadIdx.x]), 127.0f);
+    }
+    return;
+  }
   // ---- V token chunk (b, g, 128 tokens): per-channel scales from the stats,
   // E4M3 codes written transposed (token-contiguous per channel).  Each work
   // item is 4 consecutive tokens x 8 channels: the 4 codes of a channel pack
@@ -519,6 +681,14 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
   {
     const int nchunk = a.M_pad / 128;
     const int ch = cta % nchunk, hb = cta / nchunk;
+    int Mb = a.M;
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
     float *vmean = reinterpret_cast<float *>(pool), *vdelta = vmean + D, *vrcp = vdelta + D;
     uint32_t (*tile)[33] = reinterpret_cast<uint32_t (*)[33]>(vrcp + D);
     for (int c = threadIdx.x; c < D; c += kThreads) {
@@ -536,12 +706,13 @@ __global__ void __launch_bounds__(kThreads, kQuantCtas) quantize_kernel(QuantArg
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = t0 + 4 * tg + u;
-        raw[u] = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + cg] : make_uint4(0, 0, 0, 0);
+        const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + cg : ((size_t)hb * a.M + t) * VPR + cg;
+        raw[u] = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
       }
       uint32_t word[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (t0 + 4 * tg + u >= a.M) continue;
+        if (t0 + 4 * tg + u >= Mb) continue;
         float f[8];
         unpack_bf16x8(raw[u], f);
 #pragma unroll
@@ -606,7 +777,7 @@ __device__ __forceinline__ size_t atom_off(int r, int blk) { return (size_t)(r &
 template <int D>
 __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, bool own_mean,
                               const float *__restrict__ given_mean, uint8_t *codes, uint8_t *atoms,
-                              float *mean_out, int *status, int site) {
+                              float *mean_out, int *status, int site, int src_stride = D / 8) {
   constexpr int VPR = D / 8, RPP = kThreads / VPR, PASSES = 128 / RPP;
   __shared__ long long ssum[RPP][D];
   __shared__ float smean[D];
@@ -616,7 +787,7 @@ __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, boo
 #pragma unroll
   for (int pp = 0; pp < PASSES; ++pp) {
     const int r = rr + pp * RPP;
-    x[pp] = (r < valid_rows) ? src[(size_t)r * VPR + vc] : make_uint4(0, 0, 0, 0);
+    x[pp] = (r < valid_rows) ? src[(size_t)r * src_stride + vc] : make_uint4(0, 0, 0, 0);
   }
   if (own_mean) {
     long long sacc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -680,6 +851,8 @@ __device__ void fp4_row_block(const uint4 *__restrict__ src, int valid_rows, boo
 struct Fp4Args {
   const uint4 *q, *k, *v;
   int N, M, N_pad, M_pad, Tm, flags;
+  int Hq, Hkv;
+  const VarSeq *seq;  // packed sequences (kVar instances)
   uint8_t *qhat, *khat, *vhat, *qsf, *ksf, *vsf;
   const float *kbar, *vm;
   float *qbar;
@@ -687,18 +860,27 @@ struct Fp4Args {
   int nq, nk;
 };
 
-template <int D>
+// kVar: packed sequences (each sequence's own lengths, packed [total, H, d] inputs)
+template <int D, bool kVar>
 __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
   int cta = blockIdx.x;
   if (cta < a.nq) {
     // ---- Q block (b, h, i) of 128 rows, optional per-block mean
     const int i = cta % a.Tm, bh = cta / a.Tm;
     const int r0 = i * 128;
-    const int valid = max(0, min(128, a.N - r0));
-    fp4_row_block<D>(a.q + ((size_t)bh * a.N + r0) * (D / 8), valid, (a.flags & SAGE_SMOOTH_Q) && valid > 0,
-                     nullptr, a.qhat + ((size_t)bh * a.N_pad + r0) * (D / 2),
+    int Nb = a.N, stride = D / 8;
+    const uint4 *src = a.q + ((size_t)bh * a.N + r0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[bh / a.Hq];
+      Nb = sq.N;
+      stride = a.Hq * (D / 8);
+      src = a.q + ((size_t)(sq.q0 + r0) * a.Hq + bh % a.Hq) * (D / 8);
+    }
+    const int valid = max(0, min(128, Nb - r0));
+    fp4_row_block<D>(src, valid, (a.flags & SAGE_SMOOTH_Q) && valid > 0, nullptr,
+                     a.qhat + ((size_t)bh * a.N_pad + r0) * (D / 2),
                      a.qsf + ((size_t)bh * a.Tm + i) * (D / 64) * 512, a.qbar + ((size_t)bh * a.Tm + i) * D,
-                     a.status, 3);
+                     a.status, 3, stride);
     return;
   }
   cta -= a.nq;
@@ -707,10 +889,17 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
     // ---- K block (b, g, 128 rows) with k_bar over all tokens
     const int ch = cta % nchunk, hb = cta / nchunk;
     const int t0 = ch * 128;
-    const int valid = max(0, min(128, a.M - t0));
-    fp4_row_block<D>(a.k + ((size_t)hb * a.M + t0) * (D / 8), valid, false, a.kbar + (size_t)hb * D,
-                     a.khat + ((size_t)hb * a.M_pad + t0) * (D / 2),
-                     a.ksf + ((size_t)hb * nchunk + ch) * (D / 64) * 512, nullptr, a.status, 1);
+    int Mb = a.M, stride = D / 8;
+    const uint4 *src = a.k + ((size_t)hb * a.M + t0) * (D / 8);
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      stride = a.Hkv * (D / 8);
+      src = a.k + ((size_t)(sq.k0 + t0) * a.Hkv + hb % a.Hkv) * (D / 8);
+    }
+    const int valid = max(0, min(128, Mb - t0));
+    fp4_row_block<D>(src, valid, false, a.kbar + (size_t)hb * D, a.khat + ((size_t)hb * a.M_pad + t0) * (D / 2),
+                     a.ksf + ((size_t)hb * nchunk + ch) * (D / 64) * 512, nullptr, a.status, 1, stride);
     return;
   }
   cta -= a.nk;
@@ -721,13 +910,22 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
     const int t0 = ch * 128;
     constexpr int VPR = D / 8, RPP = kThreads / VPR;
     constexpr int CA = (D + 127) / 128;  // channel atoms
+    int Mb = a.M;  // this (b, kv-head)'s keys; rows hb * M + t, or (k0 + t) * Hkv + h packed
+    long long vrow = (long long)hb * a.M, vstep = 1;
+    if constexpr (kVar) {
+      const VarSeq sq = a.seq[hb / a.Hkv];
+      Mb = sq.M;
+      vrow = (long long)sq.k0 * a.Hkv + hb % a.Hkv;
+      vstep = a.Hkv;
+    }
     __shared__ __nv_bfloat16 tile[128][D + 2];
     __shared__ float vmean[D];
     for (int c = threadIdx.x; c < D; c += kThreads) vmean[c] = a.vm[(size_t)hb * D + c];
     const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
     for (int r = rr; r < 128; r += RPP) {
       const int t = t0 + r;
-      const uint4 u = (t < a.M) ? a.v[((size_t)hb * a.M + t) * VPR + vc] : make_uint4(0, 0, 0, 0);
+      const size_t vi = kVar ? (size_t)(vrow + (long long)t * vstep) * VPR + vc : ((size_t)hb * a.M + t) * VPR + vc;
+      const uint4 u = (t < Mb) ? a.v[vi] : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -740,10 +938,10 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const int t = t0 + tb * 16 + u;
-        g[u] = (t < a.M) ? __fsub_rn(__bfloat162float(tile[tb * 16 + u][c]), vmean[c]) : 0.0f;
+        g[u] = (t < Mb) ? __fsub_rn(__bfloat162float(tile[tb * 16 + u][c]), vmean[c]) : 0.0f;
         amax = fmaxf(amax, fabsf(g[u]));
       }
-      const bool any = t0 + tb * 16 < a.M;
+      const bool any = t0 + tb * 16 < Mb;
       const uint32_t sc = any ? nvfp4_scale(amax) : 0;
       const float d = e4m3_value(sc);
       uint32_t w0 = 0, w1 = 0;
@@ -752,12 +950,12 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 #pragma unroll
         for (int u = 0; u < 8; u += 2) {
           const int t = t0 + tb * 16 + u;
-          w0 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * u);
+          w0 |= (t < Mb ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * u);
         }
 #pragma unroll
         for (int u = 8; u < 16; u += 2) {
           const int t = t0 + tb * 16 + u;
-          w1 |= (t < a.M ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * (u - 8));
+          w1 |= (t < Mb ? e2m1_code2(g[u], g[u + 1], d, rcp) : 0) << (4 * (u - 8));
         }
       }
       // a token past M inside a pair contributes a zero nibble (its value is 0 anyway)
@@ -773,19 +971,79 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(Fp4Args a) {
 
 // Enqueue init, statistics, finalize and quantize on `stream`, with the
 // statistics scratch at `st`.
+// ------------------------------------------------------------------ SageBwd backward inputs
+// One CTA per 128-row block of one (b, head): dO^ with the Q quantizer (no
+// mean, scale fl(max|dO_i| / 127), the same binary32 steps, range check
+// included), then D_r = sum_c dO[r,c] O[r,c] in fp32, the VPR threads of a row
+// (consecutive lanes) combining their 8-channel partial sums by shuffles.
+template <int D>
+__global__ void __launch_bounds__(kThreads, kQuantCtas)
+    bwd_prepare_kernel(const uint4 *__restrict__ o, const uint4 *__restrict__ dout, int N, int N_pad, int Tm,
+                       uint8_t *doc, float *dos, float *drow, int *status) {
+  constexpr int VPR = D / 8, RPP = kThreads / VPR;
+  constexpr int kPool = qk_pool_bytes<D>();
+  __shared__ __align__(16) unsigned char pool[kPool];
+  const int i = blockIdx.x % Tm, bh = blockIdx.x / Tm;
+  const int r0 = i * 128;
+  const int valid = max(0, min(128, N - r0));
+  quant_block<D, true>(dout + ((size_t)bh * N + r0) * VPR, valid, 128, false, nullptr,
+                       doc + ((size_t)bh * N_pad + r0) * D * 2, dos + (size_t)bh * Tm + i, nullptr, status, 5, pool);
+  const int vc = threadIdx.x % VPR, rr = threadIdx.x / VPR;
+  for (int r = rr; r < 128; r += RPP) {  // every lane of a warp runs every shuffle
+    float acc = 0.0f;
+    if (r < valid) {
+      float a[8], g[8];
+      unpack_bf16x8(o[((size_t)bh * N + r0 + r) * VPR + vc], a);
+      unpack_bf16x8(dout[((size_t)bh * N + r0 + r) * VPR + vc], g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
+    }
+#pragma unroll
+    for (int x = 1; x < VPR; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+    if (vc == 0) drow[(size_t)bh * N_pad + r0 + r] = (r < valid) ? acc : 0.0f;
+  }
+}
+
+sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
+                               const sage_ws_layout &L, cudaStream_t stream) {
+  char *w = (char *)ws;
+  const unsigned grid = (unsigned)(s.B * s.Hq * L.Tm);
+  auto kern = s.d == 64 ? bwd_prepare_kernel<64> : bwd_prepare_kernel<128>;
+  kern<<<grid, kThreads, 0, stream>>>((const uint4 *)o, (const uint4 *)dout, s.N, L.N_pad, L.Tm,
+                                      (uint8_t *)(w + L.doc), (float *)(w + L.dos), (float *)(w + L.drow),
+                                      (int *)(w + L.status));
+  return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
+}
+
+// the quantize instance of a request: head dim, mode (INT8 / E4M3 Q and K;
+// SageBwd V), per-row Q scales, packed sequences
+template <bool kVar>
+static void (*pick_quantize(int d, int mode, bool pr))(QuantArgs) {
+  if (mode == SAGE_SAGEBWD_I8)
+    return d == 64 ? (pr ? quantize_kernel<64, true, true, true, kVar> : quantize_kernel<64, true, false, true, kVar>)
+                   : (pr ? quantize_kernel<128, true, true, true, kVar> : quantize_kernel<128, true, false, true, kVar>);
+  if (mode == SAGE_Q8_PV8)
+    return d == 64 ? (pr ? quantize_kernel<64, true, true, false, kVar> : quantize_kernel<64, true, false, false, kVar>)
+                   : (pr ? quantize_kernel<128, true, true, false, kVar> : quantize_kernel<128, true, false, false, kVar>);
+  return d == 64 ? (pr ? quantize_kernel<64, false, true, false, kVar> : quantize_kernel<64, false, false, false, kVar>)
+                 : (pr ? quantize_kernel<128, false, true, false, kVar> : quantize_kernel<128, false, false, false, kVar>);
+}
+
 static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, const void *q, const void *k,
-                              const void *v, void *ws, const sage_ws_layout &L, StatsView st, cudaStream_t stream) {
+                              const void *v, void *ws, const sage_ws_layout &L, StatsView st, cudaStream_t stream,
+                              const VarSeq *seq = nullptr) {
   char *w = (char *)ws;
   int *status = (int *)(w + L.status);
   const int n = s.B * s.Hkv * s.d;
   init_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, status);
   dim3 sg((unsigned)cdiv(s.M, kStatTokens), (unsigned)(s.B * s.Hkv));
   if (s.d == 64)
-    launch_stats<64>(sg, flags, k, v, s.M, st, status, stream);
+    launch_stats<64>(sg, flags, k, v, s.M, st, status, stream, seq, s.Hkv);
   else
-    launch_stats<128>(sg, flags, k, v, s.M, st, status, stream);
+    launch_stats<128>(sg, flags, k, v, s.M, st, status, stream, seq, s.Hkv);
   finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(st, n, s.M, flags, (float *)(w + L.kbar),
-                                                        (float *)(w + L.vm), (float *)(w + L.dv));
+                                                        (float *)(w + L.vm), (float *)(w + L.dv), seq,
+                                                        s.Hkv * s.d);
   if (mode == SAGE_NVFP4) {
     Fp4Args f;
     f.q = (const uint4 *)q;
@@ -797,6 +1055,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
     f.M_pad = L.M_pad;
     f.Tm = L.Tm;
     f.flags = flags;
+    f.Hq = s.Hq;
+    f.Hkv = s.Hkv;
+    f.seq = seq;
     f.qhat = (uint8_t *)(w + L.qhat);
     f.khat = (uint8_t *)(w + L.khat);
     f.vhat = (uint8_t *)(w + L.vhat);
@@ -812,10 +1073,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
     const unsigned g4 = (unsigned)(f.nq + 2 * f.nk);  // Q blocks, K blocks, V chunks
     // the V-scale atoms of d = 64 use half their rows: clear them first
     if (s.d % 128 != 0 && cudaMemsetAsync(f.vsf, 0, L.stats - L.vsf, stream) != cudaSuccess) return SAGE_ERR_CUDA;
-    if (s.d == 64)
-      quantize_fp4_kernel<64><<<g4, kThreads, 0, stream>>>(f);
-    else
-      quantize_fp4_kernel<128><<<g4, kThreads, 0, stream>>>(f);
+    auto fk = seq ? (s.d == 64 ? quantize_fp4_kernel<64, true> : quantize_fp4_kernel<128, true>)
+                  : (s.d == 64 ? quantize_fp4_kernel<64, false> : quantize_fp4_kernel<128, false>);
+    fk<<<g4, kThreads, 0, stream>>>(f);
     return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
   }
   QuantArgs a;
@@ -838,6 +1098,9 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.khat = (uint8_t *)(w + L.khat);
   a.vhat = (uint8_t *)(w + L.vhat);
   a.dq = (float *)(w + L.dq);
+  a.dqt = (float *)(w + L.dqt);
+  a.dvb = (float *)(w + L.dvb);
+  a.seq = seq;
   a.qbar = (float *)(w + L.qbar);
   a.dk = (float *)(w + L.dk);
   a.kbar = (float *)(w + L.kbar);
@@ -849,26 +1112,17 @@ static sage_status enqueue_q8(const sage_shape &s, int mode, int flags, int bk, 
   a.nk = s.B * s.Hkv * L.Tn;
   const int nv = s.B * s.Hkv * (L.M_pad / 128);
   const unsigned grid = (unsigned)(a.nq + a.nk + nv);
-  const bool i8 = (mode == SAGE_Q8_PV8);
-  if (s.d == 64) {
-    if (i8)
-      quantize_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
-  } else {
-    if (i8)
-      quantize_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      quantize_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
-  }
+  const bool pr = (flags & SAGE_Q_PER_TOKEN) != 0;
+  void (*kern)(QuantArgs) = seq ? pick_quantize<true>(s.d, mode, pr) : pick_quantize<false>(s.d, mode, pr);
+  kern<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
 
 sage_status launch_quantize_q8(const sage_shape &s, int mode, int flags, int bq, int bk, const void *q,
                                const void *k, const void *v, void *ws, const sage_ws_layout &L,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const VarSeq *seq) {
   (void)bq;
-  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, stats_view(ws, L, s), stream);
+  return enqueue_q8(s, mode, flags, bk, q, k, v, ws, L, stats_view(ws, L, s), stream, seq);
 }
 
 }  // namespace sage

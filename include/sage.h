@@ -60,14 +60,29 @@ typedef enum {
 enum {
   SAGE_Q8_PV8 = 0,  /* INT8 per-block Q/K, FP8 E4M3 P~ (1/448) and per-channel FP8 V */
   SAGE_QF8_PV8 = 1, /* FP8 E4M3 per-block Q/K, FP8 P~ / V as above */
-  SAGE_NVFP4 = 2    /* NVFP4 Q/K/V (E2M1, 1x16 blocks, E4M3 scales), two-level P~ */
+  SAGE_NVFP4 = 2,   /* NVFP4 Q/K/V (E2M1, 1x16 blocks, E4M3 scales), two-level P~ */
+  /* SageBwd forward (SageAttention3 summary, "SageBwd Forward Pass"): INT8
+   * per-block Q and K as in mode 0, INT8 per-block V (one scale per bk-token
+   * block), INT8 P~ with one scale per row and key tile,
+   * s_P = exp(rowmax S_ij - m_ij) / 127; bk = 64.  The attention also writes
+   * each row's log-sum-exp (region lse), which a backward pass needs */
+  SAGE_SAGEBWD_I8 = 3
 };
 
 /* flags */
 enum {
   SAGE_SMOOTH_K = 1, /* subtract mean(K) over tokens (always exact) */
   SAGE_SMOOTH_Q = 2, /* subtract the per-block mean of Q, add dS back */
-  SAGE_SMOOTH_V = 4  /* subtract mean(V) over tokens, add it back to O */
+  SAGE_SMOOTH_V = 4, /* subtract mean(V) over tokens, add it back to O */
+  /* ablation of the NVFP4 mode (SageAttention3 summary §3.4, "Two-Level
+   * Quantization for P"): phi applied to P~ itself, no level-1 scale; accepted
+   * and without effect in modes 0 and 1, whose P~ quantization is direct */
+  SAGE_P_DIRECT = 8,
+  /* one Q scale per query row instead of one per 128-row block (modes 0, 1);
+   * q_bar stays per block.  Per-thread / per-token granularity is what the
+   * SageAttention summaries trade against the MMA layout; on tcgen05 each
+   * softmax thread owns a whole row of S, so it costs the kernel one load */
+  SAGE_Q_PER_TOKEN = 0x10
 };
 
 typedef struct {
@@ -91,11 +106,21 @@ typedef struct {
  *   qsf, ksf, vsf         E4M3 block scales (mode 2), layouts in the .cu file
  *   stats                 reduction scratch of sage_quantize_qkv
  *   status                int32[4]: code, site, detail, spare
+ *   dqt    [B*Hq*N_pad]   fp32 per-row Q scale (SAGE_Q_PER_TOKEN; 0 on pad rows)
+ *   dvb    [B*Hkv*Tn]     fp32 per-block V scale (mode 3, whose vhat holds the
+ *          INT8 codes as fp16 values)
+ *   lse    [B*Hq*N_pad]   fp32 log-sum-exp of each row's scaled scores,
+ *          ln sum_j exp(S_ij sm_scale) (mode 3; rows past N not written)
+ *   doc    [B*Hq*N_pad, d] dO codes, INT8 per 128-row block held as fp16 values
+ *   dos    [B*Hq*Tm]      their scales
+ *   drow   [B*Hq*N_pad]   D = rowsum(dO o O), fp32
+ *          (the SageBwd backward's inputs, written by sage_bwd_prepare; mode 3)
  * N_pad = N rounded up to 128, M_pad = M rounded up to 128, Tm = N_pad/bq,
  * Tn = ceil(M/bk). */
 typedef struct {
   size_t qhat, dq, qbar, khat, dk, kbar, vhat, dv, vm, qsf, ksf, vsf, stats, status, total;
   int N_pad, M_pad, Tm, Tn;
+  size_t dqt, dvb, lse, doc, dos, drow;
 } sage_ws_layout;
 
 /* Workspace size in bytes for a shape and mode; 0 if the request is invalid
@@ -155,6 +180,42 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
                            int flags, int bq, int bk, const void *q_host, const void *k_host,
                            const void *v_host, void *o_host, void *dev_buf, size_t dev_bytes,
                            sage_stream_t stream);
+
+/* Packed sequences (the SageAttention production guide, "Handling Varying
+ * Sequence Lengths with VarLen Kernels": sageattn_varlen).  q is bf16
+ * [total_q, Hq, d], k and v bf16 [total_k, Hkv, d], o bf16 [total_q, Hq, d],
+ * all contiguous; sequence s holds query rows cu_seqlens_q[s] ..
+ * cu_seqlens_q[s+1] - 1 and key rows cu_seqlens_k[s] .. cu_seqlens_k[s+1] - 1.
+ * cu_seqlens_q and cu_seqlens_k are HOST int32 arrays of nseq + 1 entries,
+ * starting at 0 and non-decreasing; a sequence with queries needs keys, and a
+ * causal mask (bottom-right aligned within each sequence) needs at least as many
+ * keys as queries.  Each sequence is its own attention problem: its own means,
+ * scales and query / key blocks, starting at its first token.  Every mode
+ * (NVFP4 with 128-key tiles).
+ * The workspace holds the batched layout of B = nseq, N = the longest query
+ * run, M = the longest key run (so sage_workspace_layout of that shape
+ * locates the codes), then the sequence and work-item tables; compute and
+ * traffic follow the sequences' own lengths.  sage_attn_varlen runs the
+ * pre-pass and the attention on `stream`; its tables reach the device by one
+ * copy from pageable host memory, so the call returns only after the runtime
+ * has staged them (not capturable into a CUDA graph).
+ * sage_varlen_workspace_bytes returns 0 for an invalid or unsupported request. */
+size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,
+                                   int d, int quant_mode, int bq, int bk);
+sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv, int d,
+                             int causal, float sm_scale, int quant_mode, int flags, int bq, int bk, const void *q,
+                             const void *k, const void *v, void *workspace, size_t workspace_bytes, void *o,
+                             sage_stream_t stream);
+
+/* The SageBwd backward's pre-pass (SageAttention3 summary, "SageBwd Backward
+ * Pass": dV takes P^T dO^ with dO INT8 per block, dS takes D = rowsum(dO o O)):
+ * reads o (the forward's bf16 output) and dout (the output gradient, bf16),
+ * both [B, Hq, N, d] contiguous, and writes doc / dos / drow of a mode-3
+ * workspace.  dO is quantized like Q (scale fl(max|dO_i|/127) per 128-row
+ * block, code rint(fl(x/scale))); D is summed in fp32.  A non-finite or
+ * |x| >= 2^16 gradient sets SAGE_ERR_RANGE in the status word. */
+sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, int bk, const void *o,
+                             const void *dout, void *workspace, size_t workspace_bytes, sage_stream_t stream);
 
 /* Copy the device status word back (blocking on that copy only): *code is a
  * sage_status (SAGE_OK, SAGE_ERR_RANGE or SAGE_ERR_TIMEOUT), *site says where

@@ -13,14 +13,14 @@ def read_workspace(ws, mode: int) -> dict:
     s, L = ws.shape, ws.layout
     B, Hq, Hkv, N, M, d = s.B, s.Hq, s.Hkv, s.N, s.M, s.d
     Np, Mp, Tm, Tn = L.N_pad, L.M_pad, L.Tm, L.Tn
-    cb = 2 if mode == 0 else 1
+    cb = 2 if mode in (0, 3) else 1  # INT8 codes (modes 0 and 3) are held as fp16 values
 
     def f32(name, n):
         return _np(ws.region(name, 4 * n).view(torch.float32))
 
     qraw = ws.region("qhat", B * Hq * Np * d * cb)
     kraw = ws.region("khat", B * Hkv * Mp * d * cb)
-    if mode == 0:
+    if mode in (0, 3):
         qc = _np(qraw.view(torch.float16)).astype(np.float32).reshape(B, Hq, Np, d)[:, :, :N]
         kc = _np(kraw.view(torch.float16)).astype(np.float32).reshape(B, Hkv, Mp, d)[:, :, :M]
         assert np.all(qc == np.round(qc)) and np.all(np.abs(qc) <= 127)
@@ -29,8 +29,19 @@ def read_workspace(ws, mode: int) -> dict:
     else:
         qc = _np(qraw).reshape(B, Hq, Np, d)[:, :, :N]
         kc = _np(kraw).reshape(B, Hkv, Mp, d)[:, :, :M]
-    vt = _np(ws.region("vhat", B * Hkv * d * Mp)).reshape(B, Hkv, d, Mp)[..., :M]
-    return dict(
+    if mode == 3:  # SageBwd: per-block INT8 V as fp16 values
+        vf = _np(ws.region("vhat", B * Hkv * d * Mp * 2).view(torch.float16)).astype(np.float32)
+        vf = vf.reshape(B, Hkv, d, Mp)
+        assert np.all(vf == np.round(vf)) and np.all(np.abs(vf) <= 127)
+        vt = vf[..., :M].astype(np.int8).view(np.uint8)
+        pad_v = vf[..., M:]
+    else:
+        vt = _np(ws.region("vhat", B * Hkv * d * Mp)).reshape(B, Hkv, d, Mp)[..., :M]
+        pad_v = vt_pad(ws, B, Hkv, d, Mp, M)
+    extra = {}
+    if mode == 3:
+        extra["dvb"] = f32("dvb", B * Hkv * Tn).reshape(B, Hkv, Tn)
+    return dict(extra,
         qc=np.ascontiguousarray(qc), kc=np.ascontiguousarray(kc),
         vc=np.ascontiguousarray(vt.transpose(0, 1, 3, 2)),
         dq=f32("dq", B * Hq * Tm).reshape(B, Hq, Tm),
@@ -39,8 +50,9 @@ def read_workspace(ws, mode: int) -> dict:
         kbar=f32("kbar", B * Hkv * d).reshape(B, Hkv, d),
         dv=f32("dv", B * Hkv * d).reshape(B, Hkv, d),
         vm=f32("vm", B * Hkv * d).reshape(B, Hkv, d),
+        dqt=f32("dqt", B * Hq * Np).reshape(B, Hq, Np)[:, :, :N],
         pad_q=_np(qraw).reshape(B, Hq, Np, d * cb)[:, :, N:],
-        pad_v=vt_pad(ws, B, Hkv, d, Mp, M),
+        pad_v=pad_v,
     )
 
 
@@ -132,14 +144,20 @@ def compare_codes(got: dict, ref, mode: int, flags: int):
     qc, kc, vc = got["qc"], got["kc"], got["vc"]
     if mode == 1:
         qc, kc, qc_ref, kc_ref = map(fold_neg_zero_e4m3, (qc, kc, qc_ref, kc_ref))
-    vc, vc_ref = fold_neg_zero_e4m3(vc), fold_neg_zero_e4m3(vc_ref)
+    if mode != 3:  # E4M3 V codes
+        vc, vc_ref = fold_neg_zero_e4m3(vc), fold_neg_zero_e4m3(vc_ref)
     out = {}
     out["dq"] = np.array_equal(bits(got["dq"]), bits(ref.dq))
     out["dk"] = np.array_equal(bits(got["dk"]), bits(ref.dk))
-    out["dv"] = np.array_equal(bits(got["dv"]), bits(ref.dv))
+    if mode == 3:  # per-block V scales (the per-channel ones are not part of this mode)
+        out["dvb"] = np.array_equal(bits(got["dvb"]), bits(ref.dvb))
+    else:
+        out["dv"] = np.array_equal(bits(got["dv"]), bits(ref.dv))
     out["kbar"] = np.array_equal(bits(got["kbar"]), bits(ref.kbar))
     out["vm"] = np.array_equal(bits(got["vm"]), bits(ref.vm))
     out["qbar"] = np.array_equal(bits(got["qbar"]), bits(ref.qbar))
+    if flags & 0x10:  # per-token Q scales
+        out["dqt"] = np.array_equal(bits(got["dqt"]), bits(ref.dqt))
     out["qc"] = np.array_equal(qc, qc_ref)
     out["kc"] = np.array_equal(kc, kc_ref)
     out["vc"] = np.array_equal(vc, vc_ref)

@@ -46,7 +46,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
         s = sage.Shape(*shp)
         L = sage.sage_workspace_layout(s, mode, 128, bk).as_dict()
         offs = [L[k] for k in ("qhat", "dq", "qbar", "khat", "dk", "kbar", "vhat", "dv", "vm", "qsf", "ksf",
-                               "vsf", "stats", "status", "total")]
+                               "vsf", "stats", "status", "dqt", "total")]
         assert all(o % 1024 == 0 for o in offs)
         assert offs == sorted(offs)
         assert L["N_pad"] % 128 == 0 and L["N_pad"] >= shp[3]
@@ -54,6 +54,7 @@ def test_workspace_layout_is_aligned_and_ordered(sage):
         assert L["Tn"] == -(-shp[4] // bk)
         code_b = 2 if mode == 0 else 1
         assert L["dq"] - L["qhat"] >= shp[0] * shp[1] * L["N_pad"] * shp[5] * code_b
+        assert L["total"] - L["dqt"] >= shp[0] * shp[1] * L["N_pad"] * 4     # one Q scale per row
         assert sage.sage_workspace_bytes(s, mode, 128, bk) == L["total"]
 
 
@@ -117,6 +118,8 @@ def test_host_call_checks_everything_before_its_first_copy(sage):
     assert call(buf=C.c_void_p((1 << 30) + 512)) == 1                    # device buffer alignment
     assert call(n=need - 1) == 3                                          # too small
     assert call(flags=64) == 1                                            # unknown flag
+    assert call(mode=2, bk=128, flags=1 | 0x10, n=sage.lib.sage_host_buffer_bytes(C.byref(s), 2, 128, 128)) == 2
+    # (per-token Q scales are for the INT8 / FP8 modes)
     assert call(scale=0.0) == 1 and call(scale=float("nan")) == 1
     s2 = sage.Shape(1, 2, 2, 512, 256, 64)
     need2 = sage.lib.sage_host_buffer_bytes(C.byref(s2), 0, 128, 64)
@@ -138,3 +141,61 @@ def test_package_has_no_fallback():
     assert "raise ImportError" in src
     for bad in ("import oracle", "from oracle", "sage_oracle"):
         assert bad not in src
+
+
+def test_sagebwd_layout(sage):
+    """Mode 3 (SageBwd forward): fp16 V codes, per-block V scales, per-row
+    log-sum-exp; 64-key tiles only."""
+    shp = (2, 8, 4, 1000, 1500, 128)
+    s = sage.Shape(*shp)
+    L = sage.sage_workspace_layout(s, 3, 128, 64).as_dict()
+    B, Hq, Hkv, N, M, d = shp
+    assert L["dv"] - L["vhat"] >= B * Hkv * d * L["M_pad"] * 2
+    assert L["lse"] - L["dvb"] >= B * Hkv * L["Tn"] * 4
+    assert L["total"] - L["lse"] >= B * Hq * L["N_pad"] * 4
+    assert all(L[k] % 1024 == 0 for k in ("dqt", "dvb", "lse", "total"))
+    assert sage.sage_workspace_bytes(s, 3, 128, 128) == 0
+    with pytest.raises(sage.SageError):
+        sage.sage_workspace_layout(s, 3, 128, 128)
+
+
+def _cu(vals):
+    return (C.c_int * len(vals))(*vals)
+
+
+def test_varlen_workspace_plan(sage):
+    """Packed sequences: the batched layout of the longest runs plus the tables;
+    invalid cu_seqlens give 0 bytes."""
+    f = sage.lib.sage_varlen_workspace_bytes
+    cq, ck = [0, 100, 100, 400, 401], [0, 150, 160, 700, 702]
+    n = f(4, _cu(cq), _cu(ck), 8, 2, 128, 0, 128, 64)
+    padded = sage.sage_workspace_bytes(sage.Shape(4, 8, 2, 300, 540, 128), 0, 128, 64)
+    assert n > padded and n % 1024 == 0
+    assert n - padded < 1 << 16                     # the tables: 4 sequences, a few dozen work items
+    assert f(4, _cu(cq), _cu(ck), 8, 2, 128, 2, 128, 128) > 0           # NVFP4 too
+    assert f(2, _cu([1, 5, 9]), _cu([0, 5, 9]), 8, 2, 128, 0, 128, 64) == 0   # must start at 0
+    assert f(2, _cu([0, 5, 4]), _cu([0, 5, 9]), 8, 2, 128, 0, 128, 64) == 0   # decreasing
+    assert f(2, _cu([0, 5, 9]), _cu([0, 5, 5]), 8, 2, 128, 0, 128, 64) == 0   # queries without keys
+    assert f(2, _cu([0, 0, 0]), _cu([0, 5, 5]), 8, 2, 128, 0, 128, 64) == 0   # no queries at all
+    assert f(2, _cu([0, 5, 9]), _cu([0, 5, 9]), 3, 2, 128, 0, 128, 64) == 0   # Hq % Hkv
+    assert f(2, _cu([0, 5, 9]), _cu([0, 5, 9]), 8, 2, 128, 3, 128, 128) == 0  # SageBwd: 64-key tiles
+
+
+def test_varlen_call_checks_before_any_copy(sage):
+    """Argument errors come back before the tables' copy (which would fail here
+    without a GPU as SAGE_ERR_CUDA)."""
+    g = sage.lib.sage_attn_varlen
+    cq, ck = _cu([0, 64, 100]), _cu([0, 64, 200])
+    need = sage.lib.sage_varlen_workspace_bytes(2, cq, ck, 4, 2, 64, 0, 128, 64)
+    p = C.c_void_p(1 << 20)          # never dereferenced
+    ws = C.c_void_p(1 << 30)
+
+    def call(cqa=cq, cka=ck, causal=0, scale=0.125, mode=0, flags=1, bk=64, q=p, k=p, v=p, w=ws, n=need, o=p):
+        return g(2, cqa, cka, 4, 2, 64, causal, scale, mode, flags, 128, bk, q, k, v, w, n, o, None)
+    assert call(q=None) == 1 and call(o=None) == 1 and call(w=None) == 1
+    assert call(w=C.c_void_p((1 << 30) + 512)) == 1          # workspace alignment
+    assert call(q=C.c_void_p((1 << 20) + 8)) == 1            # 16-byte alignment of the inputs
+    assert call(n=need - 1) == 3
+    assert call(flags=64) == 1 and call(scale=0.0) == 1
+    assert call(mode=2, bk=64) == 2                          # NVFP4 attention takes 128-key tiles
+    assert call(cka=_cu([0, 32, 200]), causal=1) == 2        # causal: sequence 0 has 64 queries, 32 keys

@@ -69,3 +69,27 @@ def test_host_call_tensors_match_the_shape():
         sage.sage_attn_host(s, False, 0.125, 0, 1, 128, 64, q.float(), k, v, o, buf)
     with pytest.raises(ValueError, match="dev_buf"):  # host tensors right: the device buffer is checked next
         sage.sage_attn_host(s, False, 0.125, 0, 1, 128, 64, q, k, v, o, buf)
+
+
+def test_lse_only_from_the_sagebwd_forward():
+    s = sage.Shape(1, 2, 2, 64, 96, 64)
+    L = sage.sage_workspace_layout(s, 0, 128, 64)
+    ws = sage.Workspace(torch.empty(L.total, dtype=torch.uint8), s, 0, 1, 128, 64, L)
+    with pytest.raises(ValueError, match="mode 3"):
+        sage.sage_lse(ws)
+    L3 = sage.sage_workspace_layout(s, 3, 128, 64)
+    ws3 = sage.Workspace(torch.zeros(L3.total, dtype=torch.uint8), s, 3, 1, 128, 64, L3)
+    assert tuple(sage.sage_lse(ws3).shape) == (1, 2, 64)
+
+
+def test_backward_inputs_need_a_sagebwd_workspace():
+    s = sage.Shape(1, 2, 2, 64, 96, 64)
+    L = sage.sage_workspace_layout(s, 0, 128, 64)
+    ws = sage.Workspace(torch.empty(L.total, dtype=torch.uint8), s, 0, 1, 128, 64, L)
+    with pytest.raises(ValueError, match="mode 3"):
+        sage.sage_bwd_prepare(ws, _t(1, 2, 64, 64), _t(1, 2, 64, 64))
+    L3 = sage.sage_workspace_layout(s, 3, 128, 64)
+    ws3 = sage.Workspace(torch.empty(L3.total, dtype=torch.uint8), s, 3, 1, 128, 64, L3)
+    with pytest.raises(ValueError, match="CUDA"):
+        sage.sage_bwd_prepare(ws3, _t(1, 2, 64, 64), _t(1, 2, 64, 64))
+    assert L3.drow - L3.doc >= 1 * 2 * L3.N_pad * 64 * 2

@@ -29,6 +29,10 @@ int main(void) {
   printf("null_ws %d\n", (int)sage_attn_fwd(&s, 0, 0.125f, SAGE_Q8_PV8, SAGE_SMOOTH_K, 128, 128, NULL, 0, NULL, NULL));
   printf("flags %d\n", (int)sage_quantize_qkv(&s, SAGE_Q8_PV8, 64, 128, 128, NULL, NULL, NULL, NULL, 0, NULL));
   printf("str %s\n", sage_status_str(SAGE_ERR_WORKSPACE));
+  {
+    const int cq[4] = {0, 100, 100, 400}, ck[4] = {0, 150, 160, 700};
+    printf("varlen %zu\n", sage_varlen_workspace_bytes(3, cq, ck, 8, 2, 128, SAGE_Q8_PV8, 128, 64));
+  }
   return 0;
 }
 """
@@ -61,3 +65,4 @@ def test_header_compiles_as_c99_and_links(program):
     assert int(vals["hq_hkv"]) == 0
     assert int(vals["null_ws"]) == 1 and int(vals["flags"]) == 1
     assert vals["str"] == "workspace too small"
+    assert int(vals["varlen"]) > sage.sage_workspace_bytes(sage.Shape(3, 8, 2, 300, 540, 128), 0, 128, 64)

@@ -39,6 +39,10 @@ SMALL = [
     _small("d128_bk64_i8", d=128, N=129, M=1000, flags=5, k_outliers=3, k_outlier_shift=20.0),
     _small("fp8_d128", d=128, mode=1, N=64, M=64, flags=0),
     _small("single_token", N=1, M=1, flags=7),
+    # per-token Q scales (one per query row, q_bar still per block)
+    _small("per_token_q_i8", N=200, M=333, flags=7 | 0x10),
+    _small("per_token_q_fp8_d128", mode=1, N=130, M=300, d=128, bk=128, flags=3 | 0x10),
+    _small("per_token_q_i8_d128", d=128, N=257, M=129, flags=1 | 0x10, q_offset_std=4.0),
 ]
 
 
