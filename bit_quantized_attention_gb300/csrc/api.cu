@@ -58,6 +58,11 @@ long long spin_limit_cycles() {
   return v;
 }
 
+int test_stall() {
+  const char *e = getenv("SAGE_TEST_STALL");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 }  // namespace sage
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
@@ -150,7 +155,6 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)workspace & 1023)) return SAGE_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
   if ((long long)shape->B * shape->Hkv * shape->d > 32768) return SAGE_ERR_UNSUPPORTED;
-  if (quant_mode == SAGE_NVFP4) return SAGE_ERR_UNSUPPORTED;
   return launch_quantize_q8_static_scratch(*shape, quant_mode, flags, bq, bk, q, k, v, workspace, L,
                                            (cudaStream_t)stream);
 }

@@ -107,6 +107,7 @@ struct Fp4Params {
   __nv_bfloat16 *o;
   int *status;
   long long spin;
+  int stall;  // test hook: the QK issuer first waits on a barrier nothing arrives on
   // packed sequences (kVar): block b of the grid takes work item item_tab[b]
   // (code bh * Tm + qi); seq holds each sequence's lengths and first rows
   const int *item_tab;
@@ -236,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // before leaving, let the copies in flight land (bounded)
       volatile int no_abort = 0;
-      mbar_wait(q_full, 0, status, 11, &no_abort, p.spin);
+      mbar_wait(q_full, 0, status, 11, &no_abort, kDrainSpin);
       for (int j = max(0, issued - ST); j < issued; ++j) {
         const int s = j % ST, n = j / ST;
-        mbar_wait(&k_full[s], n & 1, status, 11, &no_abort, p.spin);
-        mbar_wait(&v_full[s], n & 1, status, 11, &no_abort, p.spin);
+        mbar_wait(&k_full[s], n & 1, status, 11, &no_abort, kDrainSpin);
+        mbar_wait(&v_full[s], n & 1, status, 11, &no_abort, kDrainSpin);
       }
     } else if (warp == kQkWarp) {
       // ---------------------------------------------------------- QK issuer (whole warp, one lane issues)
@@ -248,7 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulation has consumed R of tile j - NB, which also means every
       // MMA that read them has completed.
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, status, 23, s_abort, p.spin));
+      // test hook (SAGE_TEST_STALL): qk_done completes its first phase only
+      // after this warp's final commit, so the wait runs out (at half the
+      // limit, before any other wait of the CTA could) and the CTA unwinds
+      bool ok = !p.stall || __all_sync(0xffffffffu, mbar_wait(qk_done, 0, status, 29, s_abort, p.spin >> 1));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(q_full, 0, status, 23, s_abort, p.spin));
       tc_fence_after();
       if (ok && elect_one())
         for (int a = 0; a < D / 64; ++a) tmem_cp_32x128b_x4(tmem + C::T_SFQ + 4 * a, smem_u32(sQsf + a * 512));
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit(qk_done);
       __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(qk_done, 0, status, 25, &no_abort, p.spin);
+      mbar_wait(qk_done, 0, status, 25, &no_abort, kDrainSpin);
     } else if (warp == kPvWarp) {
       // ---------------------------------------------------------- PV issuer (whole warp, one lane issues)
       // PV of tile j writes R into S/R region j % NB once the softmax has read
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit(pv_done);
       __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(pv_done, 0, status, 27, &no_abort, p.spin);
+      mbar_wait(pv_done, 0, status, 27, &no_abort, kDrainSpin);
     }
   } else if (warp >= kCorrWarp0) {
     reg_alloc<kCorrRegs>();
@@ -750,6 +755,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
+  p.stall = test_stall();
   p.item_tab = var.item_tab;
   p.seq = var.seq;
   auto kern = attn_fp4_kernel<D, kPing, kVar>;

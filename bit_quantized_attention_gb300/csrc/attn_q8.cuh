@@ -137,6 +137,7 @@ struct AttnParams {
   __nv_bfloat16 *o;
   int *status;
   long long spin;
+  int stall;  // test hook: the QK issuer first waits on a barrier nothing arrives on
 };
 
 // byte offset of 16-byte chunk `c` of row `r` in a K-major swizzled tile whose
@@ -391,15 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: every load this warp issued lands before the CTA exits
       volatile int no_abort = 0;
-      if (qn > 0) mbar_wait(q_full, (qn - 1) & 1, status, 11, &no_abort, p.spin);
-      for (int j = max(0, gk - KST); j < gk; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, status, 11, &no_abort, p.spin);
-      for (int j = max(0, gv - VST); j < gv; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, status, 11, &no_abort, p.spin);
+      if (qn > 0) mbar_wait(q_full, (qn - 1) & 1, status, 11, &no_abort, kDrainSpin);
+      for (int j = max(0, gk - KST); j < gk; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, status, 11, &no_abort, kDrainSpin);
+      for (int j = max(0, gv - VST); j < gv; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, status, 11, &no_abort, kDrainSpin);
     } else if (warp == kQkWarp) {
       // ---------------------------------------------------------- QK issuer (whole warp, one lane issues)
       // S goes to S/R region gt % NB once the accumulation has consumed the R of
       // tile gt - NB there; the Q buffer is released after an item's last QK.
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
-      bool ok = true;
+      // test hook (SAGE_TEST_STALL): qk_done completes its first phase only
+      // after this warp's final commit, so the wait runs out (at half the
+      // limit, before any other wait of the CTA could) and the CTA unwinds
+      bool ok = !p.stall || __all_sync(0xffffffffu, mbar_wait(qk_done, 0, status, 29, s_abort, p.spin >> 1));
       int gt = 0;
       for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
         const Item it = item_of<kVar>(p, blockIdx.x + n * G, BK);
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit(qk_done);
       __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(qk_done, 0, status, 25, &no_abort, p.spin);
+      mbar_wait(qk_done, 0, status, 25, &no_abort, kDrainSpin);
     } else if (warp == kPvWarp) {
       // ---------------------------------------------------------- PV issuer (whole warp, one lane issues)
       // R = P^ V^, a fresh accumulator over one key tile, into S/R region gt % NB
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit(pv_done);
       __syncwarp();
       volatile int no_abort = 0;
-      mbar_wait(pv_done, 0, status, 27, &no_abort, p.spin);
+      mbar_wait(pv_done, 0, status, 27, &no_abort, kDrainSpin);
     }
   } else if (warp >= kCorrWarp0) {
     reg_alloc<kCorrRegs>();
@@ -1055,6 +1059,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.o = (__nv_bfloat16 *)o;
   p.status = (int *)(w + L.status);
   p.spin = spin_limit_cycles();
+  p.stall = test_stall();
   const bool sq = (flags & SAGE_SMOOTH_Q) != 0;
   auto kern = sq ? attn_q8_kernel<D, BK, kQK16, true, kPV16, kPing, kVar>
                  : attn_q8_kernel<D, BK, kQK16, false, kPV16, kPing, kVar>;

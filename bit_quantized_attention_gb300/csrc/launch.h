@@ -56,4 +56,10 @@ sage_status make_tmap_2d(CUtensorMap *map, const void *base, uint64_t cols, uint
 // Spin limit (clock cycles) for bounded waits inside kernels.
 long long spin_limit_cycles();
 
+// Test hook, read at every attention launch: SAGE_TEST_STALL=1 makes the QK
+// issuer of every CTA first wait on a barrier that nothing arrives on, so the
+// bounded wait runs out (SAGE_ERR_TIMEOUT, site 29) and the kernel takes its
+// unwind path.  Off (0) unless the variable is set.
+int test_stall();
+
 }  // namespace sage

@@ -68,6 +68,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
   return ok != 0;
 }
 
+// Limit of the waits a CTA makes on its own copies and MMAs before it leaves
+// (they always complete): about two seconds at GB300 clocks, independent of
+// the limit of the pipeline's waits, so an unwind never frees TMEM or shared
+// memory under a copy or an MMA still in flight.
+constexpr long long kDrainSpin = 4000000000LL;
+
 // A wait that gives up after `limit` clock cycles: it records `site` in the
 // status word [code, site] (first writer wins), sets the CTA-wide abort flag
 // and returns false, so the caller can unwind instead of spinning forever.

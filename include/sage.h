@@ -152,9 +152,12 @@ sage_status sage_quantize_qkv(const sage_shape *shape, int quant_mode, int flags
  * sage_attn_fwd reads it unchanged; its stats region is left untouched).
  * Limit: B * Hkv * d <= 32768 (a 768 KiB array, held on every GPU that loads
  * the library until the process exits); larger requests return
- * SAGE_ERR_UNSUPPORTED.  The first call on a device looks up the array's
- * device address with that device current; make that first call before any
- * stream capture.  The call allocates and frees nothing.  Every call shares
+ * SAGE_ERR_UNSUPPORTED.  Every quant_mode and flag of sage_quantize_qkv is
+ * accepted.  The first call on a device looks up the array's device address
+ * with that device current and keeps it for the life of the process; make that
+ * first call before any stream capture, and do not call this entry point again
+ * after a cudaDeviceReset of that device (the kept address would be stale).
+ * The call allocates and frees nothing.  Every call shares
  * the array and clears it before use; calls that overlap on the GPU race on
  * it and must be serialised by the caller. */
 sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_mode, int flags, int bq,

@@ -90,6 +90,41 @@ def test_static_scratch_matches_workspace_scratch(sage):
         assert err.sum() <= 2e-3 * np.abs(b).sum()
 
 
+def test_static_scratch_nvfp4_matches_workspace_scratch(sage):
+    """The NVFP4 pre-pass through the same entry point: packed E2M1 codes, E4M3
+    block-scale atoms and the means bit for bit, two calls in a row."""
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    for call, seed in enumerate((303, 404)):
+        cfg = _cfg(seed).with_(mode=2, bk=128, flags=1 | 2)
+        q, k, v = (t.to(dev) for t in make_inputs(cfg))
+        ref_ws = sage.sage_quantize_qkv(q, k, v, cfg.mode, cfg.flags, cfg.bq, cfg.bk)
+        shape = sage.shape_of(q, k)
+        ws = sage.new_workspace(shape, cfg.mode, cfg.flags, cfg.bq, cfg.bk, dev)
+        ws.buf.fill_(0xA5)
+        rc = sage.lib.sage_quantize_qkv_static_scratch(
+            C.byref(shape), cfg.mode, cfg.flags, cfg.bq, cfg.bk, C.c_void_p(q.data_ptr()),
+            C.c_void_p(k.data_ptr()), C.c_void_p(v.data_ptr()), C.c_void_p(ws.buf.data_ptr()),
+            ws.buf.numel(), C.c_void_p(stream.cuda_stream))
+        assert rc == 0, sage.sage_status_str(rc)
+        o = sage.sage_attn_fwd(ws, cfg.causal, cfg.sm_scale)
+        ref_o = sage.sage_attn_fwd(ref_ws, cfg.causal, cfg.sm_scale)
+        torch.cuda.synchronize()
+        assert sage.sage_read_status(ws) == (0, 0)
+        L = ws.layout
+        B, Hq, Hkv, d = shape.B, shape.Hq, shape.Hkv, shape.d
+        spans = {"qhat": B * Hq * L.N_pad * d // 2, "khat": B * Hkv * L.M_pad * d // 2,
+                 "vhat": B * Hkv * d * L.M_pad // 2, "qbar": B * Hq * L.Tm * d * 4, "kbar": B * Hkv * d * 4,
+                 "vm": B * Hkv * d * 4, "qsf": B * Hq * L.Tm * (d // 64) * 512,
+                 "ksf": B * Hkv * (L.M_pad // 128) * (d // 64) * 512, "vsf": B * Hkv * (L.M_pad // 64) * 512}
+        for name, n in spans.items():
+            off = getattr(L, name)
+            assert torch.equal(ws.buf[off:off + n], ref_ws.buf[off:off + n]), (call, name)
+        a = o.float().cpu().numpy().ravel()
+        b = ref_o.float().cpu().numpy().ravel()
+        assert np.array_equal(a, b), call  # same workspace bytes, same kernel
+
+
 def test_static_scratch_rejects_oversized_requests(sage):
     # B * Hkv * d = 4 * 64 * 128 = 32768 is the limit; one more kv-head is refused
     # before anything touches the device
