@@ -13,8 +13,15 @@ Extra keys on the JSON line:
   e2e          the same metric through sage_attn_host (pinned host buffers, the
                host->device copies and the device->host copy of O in the timed region)
   roofline     the attention kernel against the measured tensor peak
-  cpu_baseline the CPU oracle on a bounded sample of the same workload
+  cpu_baseline the CPU oracle on a bounded sample of the same workload (all
+               host cores, and one thread extrapolated)
   clocks       SM clocks and throttle reasons sampled during the timed region
+  per_workload the other workloads (LLM prefill, chunked GQA prefill, NVFP4),
+               each timed on its own with its roofline, pre-pass time and clocks
+  ablation     the method's switches timed on the video and NVFP4 workloads
+               (smoothing on/off, per-token Q, E4M3 Q/K, direct P~, SageBwd)
+The headline workload is the video-diffusion one (B2 H48 N=M=17776 d64, Q/K/V
+smoothing), the largest non-causal INT8 / FP8 case.
 Under torchrun (N > 1) every rank runs its own batch of the workload on its
 own GPU (independent problems, no collective on the data path): weak scaling.
 """
@@ -89,8 +96,10 @@ def read_traffic(key: str, mode: int = 0):
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms in the background; summary() keeps the
-    samples whose timestamps fall inside the timed window."""
+    """nvidia-smi sampled every PERIOD_MS in the background; summary() keeps
+    only the samples whose timestamps fall inside the timed window (none inside:
+    the clock is reported as null)."""
+    PERIOD_MS = 20
     FIELDS = "timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
@@ -107,7 +116,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
@@ -143,9 +152,10 @@ class ClockSampler:
                 continue
         os.unlink(self.path)
         inside = [r for r in rows if self.window and self.window[0] <= r["ts"] <= self.window[1]]
-        use = inside or rows
+        use = inside
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": len(rows), "samples_in_timed_region": 0,
+                    "reasons": ["no sample inside the timed region"]}
         sms = sorted(r["sm"] for r in use)
         reasons = set()
         for r in use:
@@ -286,11 +296,126 @@ def workload_config(cfg):
             "parallelism": "independent batch per GPU"}
 
 
+def time_steps(sage, cfg, q, k, v, dev, stream, steps, warmup, barrier=lambda: None, sampler=None):
+    """W warm-up steps, then K timed steps (pre-pass + attention) on inputs
+    resident in HBM: CUDA events on the launching stream around the whole
+    region and around each attention launch.  Returns (total ms, mean attention
+    ms, device status)."""
+    import torch
+    shape = sage.shape_of(q, k)
+    ws = sage.new_workspace(shape, cfg.mode, cfg.flags, cfg.bq, cfg.bk, dev)
+    o = torch.empty_like(q)
+
+    def step(ev=None):
+        sage.sage_quantize_qkv(q, k, v, cfg.mode, cfg.flags, cfg.bq, cfg.bk, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        sage.sage_attn_fwd(ws, cfg.causal, cfg.sm_scale, out=o, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert sage.sage_read_status(ws) == (0, 0), "device status after warm-up (%s)" % cfg.name
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler is not None:
+        sampler.mark(w0, time.time())
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    st = sage.sage_read_status(ws)
+    del ws, o
+    return total_ms, attn_ms, st
+
+
+def roofline_of(cfg, attn_ms):
+    """The attention kernel against the dense peak of its instruction mix."""
+    bf16, _, _, src = peaks()
+    peak, kinds = attention_peak(cfg.mode, bf16)
+    # algorithmic work of one launch: 4 d flops per visible (query, key) pair
+    algo_flops = 4.0 * cfg.d * cfg.B * cfg.Hq * cfg.visible_pairs
+    achieved = algo_flops / (attn_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": read_traffic(cfg.name + "_bk%d" % cfg.bk, cfg.mode),
+            "kernel": ATTN_KERNEL[cfg.mode] + " (sage_attn_fwd)", "instructions": kinds,
+            "peak_source": peak_source(cfg.mode, src, bf16), "attn_ms": attn_ms,
+            "flops_per_launch": algo_flops}
+
+
+def bench_workload(sage, cfg, dev, stream, steps, warmup, local):
+    """One workload timed on its own (same steps and warm-up as the headline),
+    with its roofline, pre-pass time and the clocks seen while it ran."""
+    from workload import make_inputs
+    qh, kh, vh = make_inputs(cfg)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    del qh, kh, vh
+    with ClockSampler(local) as clk:
+        total_ms, attn_ms, st = time_steps(sage, cfg, q, k, v, dev, stream, steps, warmup, sampler=clk)
+    ms = total_ms / steps
+    return {"config": workload_config(cfg), "value": cfg.ops / (ms * 1e-3) / 1e12, "unit": "TOPS",
+            "ms_per_step": ms, "attn_only_tops": cfg.ops / (attn_ms * 1e-3) / 1e12,
+            "prepass_ms": ms - attn_ms, "roofline": roofline_of(cfg, attn_ms), "clocks": clk.summary(),
+            "device_status": list(st)}
+
+
+def ablation_variants(cfg):
+    """The method's switches on one workload (the pages' technique-overhead and
+    granularity tables): (name, config, SAGE_PINGPONG value)."""
+    out = [("as configured", cfg, None),
+           ("Q smoothing %s" % ("off" if cfg.flags & 2 else "on"), cfg.with_(flags=cfg.flags ^ 2), None),
+           ("V smoothing %s" % ("off" if cfg.flags & 4 else "on"), cfg.with_(flags=cfg.flags ^ 4), None)]
+    if cfg.mode in (0, 1):
+        out.append(("per-token Q scales", cfg.with_(flags=cfg.flags | 0x10), None))
+        out.append(("tiles in turn", cfg, "1"))
+    if cfg.mode == 0:
+        out.append(("E4M3 Q/K", cfg.with_(mode=1), None))
+        out.append(("SageBwd forward (bk 64)", cfg.with_(mode=3, bk=64), None))
+    if cfg.mode == 2:
+        out.append(("direct P~", cfg.with_(flags=cfg.flags | 8), None))
+        out.append(("tiles in turn", cfg, "1"))
+    return out
+
+
+def ablation_rows(sage, cfg, dev, stream, steps, warmup):
+    """Each variant timed like the bench on the same inputs: step (pre-pass +
+    attention) and attention alone, in ms."""
+    from workload import make_inputs
+    qh, kh, vh = make_inputs(cfg)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    del qh, kh, vh
+    rows = []
+    try:
+        for name, c, ping in ablation_variants(cfg):
+            if ping:
+                os.environ["SAGE_PINGPONG"] = ping
+            else:
+                os.environ.pop("SAGE_PINGPONG", None)
+            total_ms, attn_ms, st = time_steps(sage, c, q, k, v, dev, stream, steps, warmup)
+            rows.append({"variant": name, "mode": c.mode, "flags": c.flags, "bk": c.bk,
+                         "step_ms": total_ms / steps, "attn_ms": attn_ms, "device_status": list(st)})
+    finally:
+        os.environ.pop("SAGE_PINGPONG", None)
+    base = rows[0]["attn_ms"]
+    for r in rows:
+        r["attn_vs_configured"] = r["attn_ms"] / base
+    return rows
+
+
 def run_gpu(args, cfg):
     import torch
 
     import bit_quantized_attention_gb300 as sage
-    from workload import make_inputs
+    from workload import CONFIGS, make_inputs
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -308,44 +433,15 @@ def run_gpu(args, cfg):
     qh, kh, vh = make_inputs(cfg)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     shape = sage.shape_of(q, k)
-    ws = sage.new_workspace(shape, cfg.mode, cfg.flags, cfg.bq, cfg.bk, dev)
-    o = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        sage.sage_quantize_qkv(q, k, v, cfg.mode, cfg.flags, cfg.bq, cfg.bk, workspace=ws, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        sage.sage_attn_fwd(ws, cfg.causal, cfg.sm_scale, out=o, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    assert sage.sage_read_status(ws) == (0, 0), "device status after warm-up"
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize(dev)
-        w0 = time.time()
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        clk.mark(w0, time.time())
-        barrier()
+        total_ms, attn_ms, code = time_steps(sage, cfg, q, k, v, dev, stream, args.steps, args.warmup,
+                                             barrier=barrier, sampler=clk)
     clocks = clk.summary()
-    total_ms = t_start.elapsed_time(t_end)
-    attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    code = sage.sage_read_status(ws)
     total_ms, attn_ms = max_over_ranks([total_ms, attn_ms], pg, dev)
     ms_per_step = total_ms / args.steps
     value = job_tops(cfg.ops, world, ms_per_step)
+    del q, k, v
 
     # ---- e2e through the C ABI on host buffers (pinned), copies inside the timed region
     q_pin, k_pin, v_pin = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
@@ -353,7 +449,6 @@ def run_gpu(args, cfg):
     nbytes = sage.sage_host_buffer_bytes(shape, cfg.mode, cfg.bq, cfg.bk)
     raw = torch.empty(nbytes + 1024, dtype=torch.uint8, device=dev)
     dev_buf = raw[(-raw.data_ptr()) % 1024:][:nbytes]
-    del ws
     for _ in range(max(1, args.warmup // 2)):
         sage.sage_attn_host(shape, cfg.causal, cfg.sm_scale, cfg.mode, cfg.flags, cfg.bq, cfg.bk,
                             q_pin, k_pin, v_pin, o_pin, dev_buf, stream=stream)
@@ -371,36 +466,44 @@ def run_gpu(args, cfg):
     e2e_val = job_tops(cfg.ops, world, e2e_ms)
     h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
     d2h = qh.numel() * 2
+    del raw, dev_buf, q_pin, k_pin, v_pin, o_pin
 
-    bf16, bf16_sus, hbm, src = peaks()
-    peak, kinds = attention_peak(cfg.mode, bf16)
-    # algorithmic work of one launch: 4 d flops per visible (query, key) pair
-    algo_flops = 4.0 * cfg.d * cfg.B * cfg.Hq * cfg.visible_pairs
-    achieved = algo_flops / (attn_ms * 1e-3) / 1e12
-    traffic = read_traffic(cfg.name + "_bk%d" % cfg.bk, cfg.mode)
     out = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ["int8/e4m3", "e4m3", "e2m1"][cfg.mode], "data": "synthetic",
+        "vs_baseline": None, "dtype": ["int8/e4m3", "e4m3", "e2m1", "int8"][cfg.mode], "data": "synthetic",
         "config": workload_config(cfg),
         "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": ATTN_KERNEL[cfg.mode] + " (sage_attn_fwd)", "instructions": kinds,
-                     "peak_source": peak_source(cfg.mode, src, bf16),
-                     "attn_ms": attn_ms},
+        "roofline": roofline_of(cfg, attn_ms),
         "attn_only_tops": cfg.ops / (attn_ms * 1e-3) / 1e12,
         "prepass_ms": ms_per_step - attn_ms,
         "clocks": clocks,
         "device_status": list(code),
     }
+    # the other workloads, each timed on its own in this process (rank 0 at N = 1:
+    # they describe the kernels, not the job)
+    if rank == 0 and world == 1 and args.per_workload:
+        per = {}
+        for name in args.per_workload.split(","):
+            if name and name != cfg.name:
+                c = CONFIGS[name].with_(bk=args.bk) if args.bk else CONFIGS[name]
+                per[name] = bench_workload(sage, c, dev, stream, args.steps, args.warmup, local)
+        out["per_workload"] = per
+    if rank == 0 and world == 1 and args.ablations:
+        abl = {}
+        for name in args.ablations.split(","):
+            if name:
+                c = CONFIGS[name].with_(bk=args.bk) if args.bk else CONFIGS[name]
+                abl[name] = ablation_rows(sage, c, dev, stream, args.steps, args.warmup)
+        out["ablation"] = abl
     if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the CPU baseline: rank 0 at N = 1 only
         smp, nrows = OracleSample.calibrated(cfg, args.ref_budget)
         tops, secs, _ = smp.run(nrows)
         out["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": smp.threads, "kind": "oracle",
-                               "sample": smp.describe(nrows), "seconds": secs}
+                               "sample": smp.describe(nrows), "seconds": secs,
+                               "single_thread": single_thread_baseline(cfg, args.ref_budget / 3)}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg is not None:
@@ -408,63 +511,34 @@ def run_gpu(args, cfg):
 
 
 def run_ablation(args, cfg):
-    """The method's switches on one workload, timed like the bench (CUDA events,
-    inputs larger than L2): step = pre-pass + attention, and the attention
-    alone.  Prints a markdown table (no JSON line): Q / V smoothing on and off,
-    per-token Q scales, E4M3 Q/K, direct P~ (NVFP4), the tiles-in-turn softmax
-    schedule, and the SageBwd forward's quantizers on the same inputs."""
+    """The method's switches on one workload as a markdown table (no JSON line):
+    Q / V smoothing on and off, per-token Q scales, E4M3 Q/K, direct P~
+    (NVFP4), the tiles-in-turn softmax schedule, and the SageBwd forward's
+    quantizers on the same inputs."""
     import torch
 
     import bit_quantized_attention_gb300 as sage
-    from workload import make_inputs
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    qh, kh, vh = make_inputs(cfg)
-    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
-    shape = sage.shape_of(q, k)
-    stream = torch.cuda.current_stream(dev)
-    variants = [("as configured", cfg, None)]
-    variants.append(("Q smoothing %s" % ("off" if cfg.flags & 2 else "on"), cfg.with_(flags=cfg.flags ^ 2), None))
-    variants.append(("V smoothing %s" % ("off" if cfg.flags & 4 else "on"), cfg.with_(flags=cfg.flags ^ 4), None))
-    if cfg.mode in (0, 1):
-        variants.append(("per-token Q scales", cfg.with_(flags=cfg.flags | 0x10), None))
-        variants.append(("tiles in turn", cfg, "1"))
-    if cfg.mode == 0:
-        variants.append(("E4M3 Q/K", cfg.with_(mode=1), None))
-        variants.append(("SageBwd forward (bk 64)", cfg.with_(mode=3, bk=64), None))
-    if cfg.mode == 2:
-        variants.append(("direct P~", cfg.with_(flags=cfg.flags | 8), None))
-        variants.append(("tiles in turn", cfg, "1"))
-    rows = []
-    for name, c, ping in variants:
-        if ping:
-            os.environ["SAGE_PINGPONG"] = ping
-        else:
-            os.environ.pop("SAGE_PINGPONG", None)
-        ws = sage.new_workspace(shape, c.mode, c.flags, c.bq, c.bk, dev)
-        o = torch.empty_like(q)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps + args.warmup)]
-        for i in range(args.steps + args.warmup):
-            evs[i][0].record(stream)
-            sage.sage_quantize_qkv(q, k, v, c.mode, c.flags, c.bq, c.bk, workspace=ws, stream=stream)
-            evs[i][1].record(stream)
-            sage.sage_attn_fwd(ws, c.causal, c.sm_scale, out=o, stream=stream)
-            evs[i][2].record(stream)
-        torch.cuda.synchronize(dev)
-        st = sage.sage_read_status(ws)
-        t = evs[args.warmup:]
-        step = sum(a.elapsed_time(c_) for a, _, c_ in t) / len(t)
-        attn = sum(b.elapsed_time(c_) for _, b, c_ in t) / len(t)
-        rows.append((name, c.mode, c.flags, c.bk, step, attn, st))
-        del ws
-    os.environ.pop("SAGE_PINGPONG", None)
-    base = rows[0]
+    rows = ablation_rows(sage, cfg, dev, torch.cuda.current_stream(dev), args.steps, args.warmup)
     print("| variant | mode | flags | bk | step ms | attention ms | attention vs as configured | status |")
     print("|---|---|---|---|---|---|---|---|")
-    for name, m, f, bk, step, attn, st in rows:
-        print("| %s | %d | 0x%x | %d | %.3f | %.3f | %.3f | %s |" % (name, m, f, bk, step, attn, attn / base[5], st))
+    for r in rows:
+        print("| %s | %d | 0x%x | %d | %.3f | %.3f | %.3f | %s |" % (
+            r["variant"], r["mode"], r["flags"], r["bk"], r["step_ms"], r["attn_ms"], r["attn_vs_configured"],
+            tuple(r["device_status"])))
+
+
+def single_thread_baseline(cfg, budget_s: float):
+    """The oracle on one host thread over a smaller sample of the same workload,
+    extrapolated to the metric's unit (TOPS)."""
+    smp = OracleSample(cfg, threads=1)
+    _, s1, n1 = smp.run(8)
+    n = int(max(8, min(smp.sub.Hq * smp.sub.N, n1 * budget_s / max(s1, 1e-6))))
+    tops, secs, rows = smp.run(n)
+    return {"value": tops, "unit": "TOPS", "cores": 1, "seconds": secs,
+            "sample": smp.describe(rows) + " on one thread (extrapolated to the whole workload by its row count)"}
 
 
 def kernel_hash(files=None) -> str:
@@ -490,7 +564,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llm_prefill")
+    ap.add_argument("--workload", default="video",
+                    help="the headline workload (video: the largest non-causal INT8 / FP8 one)")
+    ap.add_argument("--per-workload", default="llm_prefill,chunked_gqa,nvfp4",
+                    help="other workloads timed in the same run, each with its own roofline ('' for none)")
+    ap.add_argument("--ablations", default="video,nvfp4",
+                    help="workloads whose switch ablations go on the JSON line ('' for none)")
     ap.add_argument("--bk", type=int, default=128, help="key tile = K scale block (the workload leaves it open)")
     ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
