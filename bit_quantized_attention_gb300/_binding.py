@@ -24,7 +24,7 @@ STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3:
 EXPORTS = ["sage_workspace_bytes", "sage_workspace_layout", "sage_quantize_qkv", "sage_attn_fwd",
            "sage_host_buffer_bytes", "sage_attn_host", "sage_read_status", "sage_status_str",
            "sage_quantize_qkv_static_scratch", "sage_varlen_workspace_bytes", "sage_attn_varlen",
-           "sage_bwd_prepare"]
+           "sage_bwd_prepare", "sage_attn_bwd"]
 
 
 class SageError(RuntimeError):
@@ -75,6 +75,8 @@ def _load():
     L.sage_attn_varlen.restype = i32
     L.sage_bwd_prepare.argtypes = [P(Shape), i32, i32, i32, vp, vp, vp, sz, vp]
     L.sage_bwd_prepare.restype = i32
+    L.sage_attn_bwd.argtypes = [P(Shape), i32, f32, i32, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp]
+    L.sage_attn_bwd.restype = i32
     L.sage_read_status.restype = i32
     L.sage_status_str.argtypes, L.sage_status_str.restype = [i32], C.c_char_p
     return L
@@ -315,6 +317,34 @@ def sage_bwd_prepare(ws: Workspace, o, dout, stream=None):
     dos = ws.region("dos", s.B * s.Hq * L.Tm * 4).view(torch.float32).view(s.B, s.Hq, L.Tm)
     drow = ws.region("drow", s.B * s.Hq * L.N_pad * 4).view(torch.float32).view(s.B, s.Hq, L.N_pad)
     return doc[:, :, :s.N], dos, drow[:, :, :s.N]
+
+
+def sage_attn_bwd(ws: Workspace, causal: bool, sm_scale: float, v, dout, dq=None, dk=None, dv=None,
+                  stream=None):
+    """The SageBwd backward on a mode-3 workspace that sage_attn_fwd and
+    sage_bwd_prepare have filled: v the forward's bf16 V [B, Hkv, M, d], dout
+    the bf16 dO [B, Hq, N, d].  Returns (dq, dk, dv) as float32 tensors
+    (dq [B, Hq, N, d]; dk, dv [B, Hkv, M, d]), into the given ones if any."""
+    if ws.mode != SAGE_SAGEBWD_I8:
+        raise ValueError("the backward runs on a mode 3 (SageBwd) workspace")
+    s = ws.shape
+    qshape, kshape = (s.B, s.Hq, s.N, s.d), (s.B, s.Hkv, s.M, s.d)
+    _bf16_cuda(v, "v")
+    _bf16_cuda(dout, "dout")
+    if tuple(v.shape) != kshape or tuple(dout.shape) != qshape:
+        raise ValueError("v must be [B, Hkv, M, d] = %s and dout [B, Hq, N, d] = %s" % (kshape, qshape))
+    dev = ws.buf.device
+    outs = []
+    for t, shp, n in ((dq, qshape, "dq"), (dk, kshape, "dk"), (dv, kshape, "dv")):
+        if t is None:
+            t = torch.empty(shp, dtype=torch.float32, device=dev)
+        elif t.dtype != torch.float32 or tuple(t.shape) != shp or not t.is_contiguous() or t.device != dev:
+            raise ValueError("%s must be a contiguous float32 tensor %s on the workspace's device" % (n, shp))
+        outs.append(t)
+    _check(lib.sage_attn_bwd(C.byref(s), int(bool(causal)), float(sm_scale), ws.mode, ws.flags, ws.bq, ws.bk,
+                             _ptr(ws.buf), ws.buf.numel(), _ptr(v), _ptr(dout), _ptr(outs[0]), _ptr(outs[1]),
+                             _ptr(outs[2]), _stream(stream)), "sage_attn_bwd")
+    return tuple(outs)
 
 
 def sage_lse(ws: Workspace) -> torch.Tensor:

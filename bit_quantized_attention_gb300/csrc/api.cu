@@ -257,6 +257,25 @@ sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, in
   return launch_bwd_prepare(*shape, o, dout, workspace, L, (cudaStream_t)stream);
 }
 
+sage_status sage_attn_bwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
+                          int bk, const void *workspace, size_t workspace_bytes, const void *v, const void *dout,
+                          void *dq, void *dk, void *dv, sage_stream_t stream) {
+  sage_ws_layout L;
+  sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
+  if (st != SAGE_OK) return st;
+  if (quant_mode != SAGE_SAGEBWD_I8) return SAGE_ERR_UNSUPPORTED;
+  if ((st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk)) != SAGE_OK) return st;
+  // per-row Q scales vary along the reduction of dK = dS^T Q: not supported here
+  if (flags & SAGE_Q_PER_TOKEN) return SAGE_ERR_UNSUPPORTED;
+  if (!workspace || !v || !dout || !dq || !dk || !dv) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      ((uintptr_t)workspace & 1023))
+    return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  return launch_attn_bwd(*shape, causal, sm_scale, flags, workspace, L, v, dout, (float *)dq, (float *)dk,
+                         (float *)dv, (cudaStream_t)stream);
+}
+
 sage_status sage_read_status(const sage_shape *shape, int quant_mode, int bq, int bk, const void *workspace,
                              int *code, int *site) {
   sage_ws_layout L;

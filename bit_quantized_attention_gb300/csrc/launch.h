@@ -44,6 +44,11 @@ sage_status launch_attn_q8_var(const sage_shape &s, int causal, float sm_scale, 
 sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
                                const sage_ws_layout &L, cudaStream_t stream);
 
+// The SageBwd backward (attn_bwd.cu): dK and dV, then dQ, fp32 outputs.
+sage_status launch_attn_bwd(const sage_shape &s, int causal, float sm_scale, int flags, const void *ws,
+                            const sage_ws_layout &L, const void *v, const void *dout, float *dq, float *dk, float *dv,
+                            cudaStream_t stream);
+
 // Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
                             const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var = VarDev());

@@ -220,6 +220,26 @@ sage_status sage_attn_varlen(int nseq, const int *cu_seqlens_q, const int *cu_se
 sage_status sage_bwd_prepare(const sage_shape *shape, int quant_mode, int bq, int bk, const void *o,
                              const void *dout, void *workspace, size_t workspace_bytes, sage_stream_t stream);
 
+/* SageBwd backward (SageAttention3 summary, "SageBwd Backward Pass and the
+ * Critical dOV^T Decision", eq. 8 and Algorithm 3): dQ, dK, dV of the
+ * forward that sage_attn_fwd ran on this workspace in quant_mode
+ * SAGE_SAGEBWD_I8 (bk = 64), after sage_bwd_prepare wrote the dO codes and D.
+ * S and P = exp(S sm_scale - lse) are recomputed from the forward's INT8 Q and K
+ * codes and its log-sum-exp; P and dS go to INT8 per 128 x 64 tile (scale
+ * max / 127), dO to INT8 per 128-row block; dV = P^T dO, dK = dS^T Q and
+ * dQ = dS K run on those codes; dP = dO V^T stays 16-bit (bf16 operands); the
+ * K and Q smoothing corrections rowsum(dS) k_bar and colsum(dS) q_bar take the
+ * unquantized dS.  causal, sm_scale and flags must be the forward's
+ * (SAGE_Q_PER_TOKEN is not supported: SAGE_ERR_UNSUPPORTED).
+ * v: the forward's bf16 V [B,Hkv,M,d]; dout: bf16 dO [B,Hq,N,d] (the one given
+ * to sage_bwd_prepare); outputs fp32, caller-allocated, 16-byte aligned:
+ * dq [B,Hq,N,d], dk and dv [B,Hkv,M,d] (summed over the query heads of a kv
+ * head).  Deterministic: no atomics.  A bounded wait that gives up sets
+ * SAGE_ERR_TIMEOUT in the status word; the outputs are then undefined. */
+sage_status sage_attn_bwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
+                          int bk, const void *workspace, size_t workspace_bytes, const void *v, const void *dout,
+                          void *dq, void *dk, void *dv, sage_stream_t stream);
+
 /* Copy the device status word back (blocking on that copy only): *code is a
  * sage_status (SAGE_OK, SAGE_ERR_RANGE or SAGE_ERR_TIMEOUT), *site says where
  * it was raised.  The status word is cleared by every sage_quantize_qkv. */

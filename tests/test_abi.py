@@ -100,6 +100,28 @@ def test_pointer_workspace_and_flag_checks(sage):
     assert a(C.byref(s2), 1, 0.125, 0, 1, 128, 64, ok, need2, ok, None) == 2          # causal with N > M
 
 
+def test_backward_checks_before_any_launch(sage):
+    """sage_attn_bwd: the SageBwd mode only, no per-token Q scales, every
+    pointer present and aligned, a large enough workspace."""
+    s = sage.Shape(1, 2, 2, 256, 256, 64)
+    need = sage.sage_workspace_bytes(s, 3, 128, 64)
+    ok = C.c_void_p(1 << 20)
+    f = sage.lib.sage_attn_bwd
+
+    def call(shape=s, causal=0, scale=0.125, mode=3, flags=1, bk=64, ws=ok, n=need, v=ok, do=ok, dq=ok, dk=ok, dv=ok):
+        return f(C.byref(shape), causal, scale, mode, flags, 128, bk, ws, n, v, do, dq, dk, dv, None)
+    assert call(mode=0, n=sage.sage_workspace_bytes(s, 0, 128, 64)) == 2     # not the SageBwd mode
+    assert call(bk=128) == 2                                                 # SageBwd takes 64-key blocks
+    assert call(flags=1 | 0x10) == 2                                         # per-token Q scales
+    assert call(flags=64) == 1 and call(scale=0.0) == 1
+    assert call(v=None) == 1 and call(do=None) == 1 and call(dq=None) == 1 and call(dk=None) == 1
+    assert call(dv=C.c_void_p((1 << 20) + 4)) == 1                           # misaligned output
+    assert call(ws=C.c_void_p((1 << 20) + 512)) == 1                         # workspace alignment
+    assert call(n=need - 1) == 3
+    s2 = sage.Shape(1, 2, 2, 512, 256, 64)
+    assert call(shape=s2, causal=1, n=sage.sage_workspace_bytes(s2, 3, 128, 64)) == 2   # causal with N > M
+
+
 def test_host_call_checks_everything_before_its_first_copy(sage):
     """sage_attn_host validates all of its own and its two calls' arguments
     before it enqueues anything (a copy attempted here, without a GPU, would

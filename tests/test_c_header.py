@@ -30,6 +30,11 @@ int main(void) {
   printf("flags %d\n", (int)sage_quantize_qkv(&s, SAGE_Q8_PV8, 64, 128, 128, NULL, NULL, NULL, NULL, 0, NULL));
   printf("str %s\n", sage_status_str(SAGE_ERR_WORKSPACE));
   {
+    sage_shape sb = {1, 2, 2, 256, 256, 64};
+    printf("bwd_null %d\n", (int)sage_attn_bwd(&sb, 0, 0.125f, SAGE_SAGEBWD_I8, SAGE_SMOOTH_K, 128, 64, NULL, 0,
+                                                  NULL, NULL, NULL, NULL, NULL, NULL));
+  }
+  {
     const int cq[4] = {0, 100, 100, 400}, ck[4] = {0, 150, 160, 700};
     printf("varlen %zu\n", sage_varlen_workspace_bytes(3, cq, ck, 8, 2, 128, SAGE_Q8_PV8, 128, 64));
   }
@@ -65,4 +70,5 @@ def test_header_compiles_as_c99_and_links(program):
     assert int(vals["hq_hkv"]) == 0
     assert int(vals["null_ws"]) == 1 and int(vals["flags"]) == 1
     assert vals["str"] == "workspace too small"
+    assert int(vals["bwd_null"]) == 1
     assert int(vals["varlen"]) > sage.sage_workspace_bytes(sage.Shape(3, 8, 2, 300, 540, 128), 0, 128, 64)
