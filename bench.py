@@ -20,6 +20,8 @@ Extra keys on the JSON line:
                each timed on its own with its roofline, pre-pass time and clocks
   ablation     the method's switches timed on the video and NVFP4 workloads
                (smoothing on/off, per-token Q, E4M3 Q/K, direct P~, SageBwd)
+  backward     the SageBwd training step on the LLM prefill shape: forward,
+               the backward's pre-pass and the backward, with its roofline
 The headline workload is the video-diffusion one (B2 H48 N=M=17776 d64, Q/K/V
 smoothing), the largest non-causal INT8 / FP8 case.
 Under torchrun (N > 1) every rank runs its own batch of the workload on its
@@ -286,7 +288,7 @@ METRIC = "quantized attention TOPS (4*B*H*N*M*d/s, causal halved) and % of tenso
 
 def workload_config(cfg):
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "N": cfg.N, "M": cfg.M, "d": cfg.d,
-            "causal": cfg.causal, "quant_mode": ["int8_qk_fp8_pv", "fp8_qk_fp8_pv", "nvfp4"][cfg.mode],
+            "causal": cfg.causal, "quant_mode": ["int8_qk_fp8_pv", "fp8_qk_fp8_pv", "nvfp4", "sagebwd_int8"][cfg.mode],
             "flags": {"smooth_k": bool(cfg.flags & 1), "smooth_q": bool(cfg.flags & 2),
                       "smooth_v": bool(cfg.flags & 4), "p_direct": bool(cfg.flags & 8),
                       "q_per_token": bool(cfg.flags & 0x10)},
@@ -366,6 +368,65 @@ def bench_workload(sage, cfg, dev, stream, steps, warmup, local):
             "ms_per_step": ms, "attn_only_tops": cfg.ops / (attn_ms * 1e-3) / 1e12,
             "prepass_ms": ms - attn_ms, "roofline": roofline_of(cfg, attn_ms), "clocks": clk.summary(),
             "device_status": list(st)}
+
+
+def bench_backward(sage, cfg, dev, stream, steps, warmup, local):
+    """The SageBwd training step on one workload: the forward in the SageBwd
+    mode (pre-pass + attention with its log-sum-exp), the backward's pre-pass
+    (dO codes, D = rowsum(dO o O)) and the backward (dQ, dK, dV), each timed
+    with CUDA events; the backward against the bf16 dense peak (all of its
+    products run as kind::f16)."""
+    import torch
+    from workload import make_inputs
+    qh, kh, vh = make_inputs(cfg)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    del qh, kh, vh
+    gen = torch.Generator(device=dev).manual_seed(5)
+    dout = torch.randn(q.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    shape = sage.shape_of(q, k)
+    ws = sage.new_workspace(shape, cfg.mode, cfg.flags, cfg.bq, cfg.bk, dev)
+    o = torch.empty_like(q)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps + warmup)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        w0 = time.time()
+        for i in range(steps + warmup):
+            if i == warmup:
+                torch.cuda.synchronize(dev)
+                w0 = time.time()
+            ev[i][0].record(stream)
+            sage.sage_quantize_qkv(q, k, v, cfg.mode, cfg.flags, cfg.bq, cfg.bk, workspace=ws, stream=stream)
+            sage.sage_attn_fwd(ws, cfg.causal, cfg.sm_scale, out=o, stream=stream)
+            ev[i][1].record(stream)
+            sage.sage_bwd_prepare(ws, o, dout, stream=stream)
+            ev[i][2].record(stream)
+            sage.sage_attn_bwd(ws, cfg.causal, cfg.sm_scale, v, dout, dq=dq, dk=dk, dv=dv, stream=stream)
+            ev[i][3].record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark(w0, time.time())
+    st = sage.sage_read_status(ws)
+    t = ev[warmup:]
+    fwd = sum(a.elapsed_time(b) for a, b, _, _ in t) / steps
+    prep = sum(b.elapsed_time(c) for _, b, c, _ in t) / steps
+    bwd = sum(c.elapsed_time(d) for _, _, c, d in t) / steps
+    bf16, _, _, src = peaks()
+    pairs = cfg.B * cfg.Hq * cfg.visible_pairs
+    algo = 10.0 * cfg.d * pairs        # five products of 2 d flops per visible pair
+    achieved = algo / (bwd * 1e-3) / 1e12
+    return {"config": workload_config(cfg), "fwd_ms": fwd, "bwd_prepare_ms": prep, "bwd_ms": bwd,
+            "step_ms": fwd + prep + bwd,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                         "frac": achieved / bf16, "traffic": None,
+                         "kernel": "bwd_dkdv_kernel + bwd_dq_kernel (sage_attn_bwd)",
+                         "instructions": "kind::f16 (INT8 codes as fp16, bf16 dO V^T)",
+                         "peak_source": "%s bf16 burst %.1f TFLOP/s" % (src, bf16),
+                         "flops_per_launch": algo,
+                         "flops_executed_per_launch": 14.0 * cfg.d * pairs,
+                         "note": "algorithmic: 5 products; the two kernels run 7 (S and dP are formed in both)"},
+            "clocks": clk.summary(), "device_status": list(st)}
 
 
 def ablation_variants(cfg):
@@ -491,6 +552,9 @@ def run_gpu(args, cfg):
                 c = CONFIGS[name].with_(bk=args.bk) if args.bk else CONFIGS[name]
                 per[name] = bench_workload(sage, c, dev, stream, args.steps, args.warmup, local)
         out["per_workload"] = per
+    if rank == 0 and world == 1 and args.backward:
+        c = CONFIGS[args.backward].with_(mode=3, bk=64)
+        out["backward"] = bench_backward(sage, c, dev, stream, args.steps, args.warmup, local)
     if rank == 0 and world == 1 and args.ablations:
         abl = {}
         for name in args.ablations.split(","):
@@ -568,6 +632,8 @@ def main():
                     help="the headline workload (video: the largest non-causal INT8 / FP8 one)")
     ap.add_argument("--per-workload", default="llm_prefill,chunked_gqa,nvfp4",
                     help="other workloads timed in the same run, each with its own roofline ('' for none)")
+    ap.add_argument("--backward", default="llm_prefill",
+                    help="workload whose SageBwd forward + backward is timed on the JSON line ('' for none)")
     ap.add_argument("--ablations", default="video,nvfp4",
                     help="workloads whose switch ablations go on the JSON line ('' for none)")
     ap.add_argument("--bk", type=int, default=128, help="key tile = K scale block (the workload leaves it open)")
