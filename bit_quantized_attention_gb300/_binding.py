@@ -239,6 +239,13 @@ def sage_attn_host(shape: Shape, causal: bool, sm_scale: float, mode: int, flags
                               dev_buf.numel(), _stream(stream)), "sage_attn_host")
 
 
+def sage_host_status(dev_buf: torch.Tensor):
+    """(code, site) of the last sage_attn_host call on dev_buf: the status word
+    at its start (read after the call's stream has completed)."""
+    st = dev_buf[:16].view(torch.int32).cpu().tolist()
+    return st[0], st[1]
+
+
 def sage_status_str(code: int) -> str:
     return lib.sage_status_str(code).decode()
 

@@ -159,15 +159,12 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
                                            (cudaStream_t)stream);
 }
 
-static size_t io_bytes(const sage_shape *s) {
-  const size_t qn = (size_t)s->B * s->Hq * s->N * s->d * 2, kn = (size_t)s->B * s->Hkv * s->M * s->d * 2;
-  return align_up(qn, 1024) * 2 + align_up(kn, 1024) * 2;  // q, o, k, v
-}
-
 size_t sage_host_buffer_bytes(const sage_shape *shape, int quant_mode, int bq, int bk) {
   sage_ws_layout L;
   if (request_layout(shape, quant_mode, bq, bk, &L) != SAGE_OK) return 0;
-  return L.total + io_bytes(shape);
+  size_t bytes = 0;
+  if (host_buffer_bytes(*shape, quant_mode, bq, bk, &bytes) != SAGE_OK) return 0;
+  return bytes;
 }
 
 sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, int quant_mode, int flags, int bq,
@@ -176,29 +173,16 @@ sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, 
   sage_ws_layout L;
   sage_status st = request_layout(shape, quant_mode, bq, bk, &L);
   if (st != SAGE_OK) return st;
-  // every argument condition of the two calls below, before the first copy
+  // every argument condition of the calls it makes, before the first copy
   st = check_attn_args(shape, causal, sm_scale, quant_mode, flags, bk);
   if (st != SAGE_OK) return st;
   if (!q_host || !k_host || !v_host || !o_host || !dev_buf) return SAGE_ERR_INVALID_ARG;
   if (((uintptr_t)dev_buf & 1023)) return SAGE_ERR_INVALID_ARG;
-  if (dev_bytes < L.total + io_bytes(shape)) return SAGE_ERR_WORKSPACE;
-  const size_t qn = (size_t)shape->B * shape->Hq * shape->N * shape->d * 2;
-  const size_t kn = (size_t)shape->B * shape->Hkv * shape->M * shape->d * 2;
-  char *ws = (char *)dev_buf;
-  char *dq = ws + L.total;
-  char *dk = dq + align_up(qn, 1024);
-  char *dv = dk + align_up(kn, 1024);
-  char *dO = dv + align_up(kn, 1024);
-  cudaStream_t cs = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(dq, q_host, qn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (cudaMemcpyAsync(dk, k_host, kn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
-  if (cudaMemcpyAsync(dv, v_host, kn, cudaMemcpyHostToDevice, cs) != cudaSuccess) return SAGE_ERR_CUDA;
-  st = sage_quantize_qkv(shape, quant_mode, flags, bq, bk, dq, dk, dv, ws, L.total, stream);
-  if (st != SAGE_OK) return st;
-  st = sage_attn_fwd(shape, causal, sm_scale, quant_mode, flags, bq, bk, ws, L.total, dO, stream);
-  if (st != SAGE_OK) return st;
-  if (cudaMemcpyAsync(o_host, dO, qn, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return SAGE_ERR_CUDA;
-  return SAGE_OK;
+  size_t need = 0;
+  if ((st = host_buffer_bytes(*shape, quant_mode, bq, bk, &need)) != SAGE_OK) return st;
+  if (dev_bytes < need) return SAGE_ERR_WORKSPACE;
+  return run_attn_host(*shape, causal, sm_scale, quant_mode, flags, bq, bk, q_host, k_host, v_host, o_host, dev_buf,
+                       (cudaStream_t)stream);
 }
 
 size_t sage_varlen_workspace_bytes(int nseq, const int *cu_seqlens_q, const int *cu_seqlens_k, int Hq, int Hkv,

@@ -17,6 +17,12 @@ sage_status launch_attn_q8(const sage_shape &s, int causal, float sm_scale, int 
   const char *pp = getenv("SAGE_PINGPONG");
   if (mode != SAGE_SAGEBWD_I8 && pp && pp[0] == '1')
     return launch_attn_q8_ping(s, causal, sm_scale, mode, flags, bk, ws, L, o, stream);
+  // head dim 64 with 64-key tiles: two query blocks per work item (modes 0
+  // and 1) unless SAGE_ATTN_SCHEDULE=split asks for the one-block schedule
+  const char *sch = getenv("SAGE_ATTN_SCHEDULE");
+  const bool split = sch && sch[0] == 's';
+  if (!split && s.d == 64 && bk == 64 && (mode == SAGE_Q8_PV8 || mode == SAGE_QF8_PV8))
+    return launch_attn_q8x2_64(s, causal, sm_scale, mode, flags, ws, L, o, stream);
   return dispatch_q8<false, false>(s, causal, sm_scale, mode, flags, bk, ws, L, o, stream, var);
 }
 

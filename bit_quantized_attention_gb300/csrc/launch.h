@@ -44,6 +44,11 @@ sage_status launch_attn_q8_var(const sage_shape &s, int causal, float sm_scale, 
 sage_status launch_bwd_prepare(const sage_shape &s, const void *o, const void *dout, void *ws,
                                const sage_ws_layout &L, cudaStream_t stream);
 
+// The two-query-block schedule of the INT8 / FP8 attention (attn_q8x2.cuh):
+// batched requests, head dim 64, 64-key tiles, modes 0 and 1.
+sage_status launch_attn_q8x2_64(const sage_shape &s, int causal, float sm_scale, int mode, int flags, const void *ws,
+                                const sage_ws_layout &L, void *o, cudaStream_t stream);
+
 // The SageBwd backward (attn_bwd.cu): dK and dV, then dQ, fp32 outputs.
 sage_status launch_attn_bwd(const sage_shape &s, int causal, float sm_scale, int flags, const void *ws,
                             const sage_ws_layout &L, const void *v, const void *dout, float *dq, float *dk, float *dv,
@@ -52,6 +57,13 @@ sage_status launch_attn_bwd(const sage_shape &s, int causal, float sm_scale, int
 // Attention for SAGE_NVFP4 (attn_fp4.cu); bk must be 128.
 sage_status launch_attn_fp4(const sage_shape &s, int causal, float sm_scale, int flags, int bk, const void *ws,
                             const sage_ws_layout &L, void *o, cudaStream_t stream, const VarDev &var = VarDev());
+
+// The end-to-end call on host buffers, chunked and pipelined (host.cu): the
+// device buffer it needs, and the call itself (arguments already checked).
+sage_status host_buffer_bytes(const sage_shape &s, int mode, int bq, int bk, size_t *bytes);
+sage_status run_attn_host(const sage_shape &s, int causal, float sm_scale, int mode, int flags, int bq, int bk,
+                          const void *q_host, const void *k_host, const void *v_host, void *o_host, void *dev_buf,
+                          cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (api.cu).
 // A 2-D byte tensor [rows][cols] with row pitch `pitch` bytes, box {box_cols, box_rows}.

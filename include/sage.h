@@ -174,10 +174,20 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
                           int flags, int bq, int bk, const void *workspace, size_t workspace_bytes,
                           void *o, sage_stream_t stream);
 
-/* End-to-end call on HOST buffers: copies q, k, v (host, ideally pinned) into
- * dev_buf, runs sage_quantize_qkv and sage_attn_fwd, copies o back to o_host,
- * all on `stream` (asynchronous with pinned host memory).  dev_buf is one
- * caller-allocated device buffer of at least sage_host_buffer_bytes(). */
+/* End-to-end call on HOST buffers (ideally pinned): q, k, v copied in, the
+ * pre-pass and the attention run, o copied back, asynchronously on `stream`.
+ * The request is cut into chunks of whole kv heads of one batch element
+ * (independent problems: their own means and scales, so the result is the
+ * same as one call on the whole request) and the copies of one chunk overlap
+ * the kernels of the others: host -> device on one internal stream, the
+ * kernels on `stream`, device -> host on another internal stream.  The two
+ * internal streams and their events are created once per device on the first
+ * call (no device memory); the call is ordered after earlier work on `stream`
+ * and later work on `stream` after its last copy.  dev_buf is one
+ * caller-allocated, 1024-byte aligned device buffer of at least
+ * sage_host_buffer_bytes(); its first 16 bytes hold the call's device status
+ * word int[4] (code, site: the first error of any chunk) once `stream` has
+ * completed. */
 size_t sage_host_buffer_bytes(const sage_shape *shape, int quant_mode, int bq, int bk);
 sage_status sage_attn_host(const sage_shape *shape, int causal, float sm_scale, int quant_mode,
                            int flags, int bq, int bk, const void *q_host, const void *k_host,
