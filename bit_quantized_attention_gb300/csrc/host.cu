@@ -1,13 +1,14 @@
 // The end-to-end call on host buffers (sage_attn_host): the request is cut
 // into chunks of whole kv-heads of one batch element -- independent problems
 // with their own statistics and scales -- and the copies of one chunk overlap
-// the kernels of the others: host -> device copies of chunk c + 1 on one
-// stream, chunk c's pre-pass and attention on the caller's stream (in a
-// workspace slot of their own), device -> host copy of chunk c - 1 on a third
-// stream.  The two copy streams and their events are created once per device
-// on the first call (no device memory); the call is ordered after earlier
-// work on the caller's stream, and later work on that stream after its last
-// copy.
+// the kernels of the others: host -> device copies on one stream, the
+// pre-pass and attention of even chunks on the caller's stream and of odd
+// chunks on a second compute stream (each chunk in the workspace slot of its
+// stream, so the next chunk's blocks fill the SMs the previous chunk's last
+// blocks leave idle), device -> host copies on a fourth stream.  The internal
+// streams and their events are created once per device on the first call (no
+// device memory); the call is ordered after earlier work on the caller's
+// stream, and later work on that stream after its last copy.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -64,7 +65,7 @@ sage_status slot_bytes(const sage_shape &s, int mode, int bq, int bk, size_t *by
 }
 
 struct HostPipe {
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, cmp = nullptr;
   cudaEvent_t start = nullptr, done = nullptr, in_done[2] = {nullptr, nullptr}, cmp_done[2] = {nullptr, nullptr};
   bool ok = false;
 };
@@ -82,6 +83,7 @@ HostPipe *host_pipe() {
     const unsigned ef = cudaEventDisableTiming;
     bool good = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
                 cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaStreamCreateWithFlags(&p.cmp, cudaStreamNonBlocking) == cudaSuccess &&
                 cudaEventCreateWithFlags(&p.start, ef) == cudaSuccess &&
                 cudaEventCreateWithFlags(&p.done, ef) == cudaSuccess;
     for (int i = 0; i < 2 && good; ++i)
@@ -96,10 +98,9 @@ HostPipe *host_pipe() {
 // keep the first error of any chunk: the call's status word takes a chunk's
 // when it holds none yet
 __global__ void merge_status_kernel(const int *chunk, int *total) {
-  if (threadIdx.x == 0 && total[0] == 0 && chunk[0] != 0) {
+  if (threadIdx.x == 0 && chunk[0] != 0 && atomicCAS(&total[0], 0, chunk[0]) == 0) {
     total[1] = chunk[1];
     total[2] = chunk[2];
-    total[0] = chunk[0];
   }
 }
 
@@ -141,6 +142,8 @@ sage_status run_attn_host(const sage_shape &s, int causal, float sm_scale, int m
   SAGE_CK(cudaEventRecord(hp->start, stream));
   SAGE_CK(cudaStreamWaitEvent(hp->in, hp->start, 0));
   SAGE_CK(cudaStreamWaitEvent(hp->out, hp->start, 0));
+  SAGE_CK(cudaStreamWaitEvent(hp->cmp, hp->start, 0));
+  cudaStream_t cmp[2] = {stream, hp->cmp};
   const std::vector<HostChunk> chunks = host_chunks(s);
   for (size_t i = 0; i < chunks.size(); ++i) {
     const HostChunk &c = chunks[i];
@@ -153,23 +156,26 @@ sage_status run_attn_host(const sage_shape &s, int causal, float sm_scale, int m
     SAGE_CK(cudaMemcpyAsync(dk + ko, kh + ko, kb, cudaMemcpyHostToDevice, hp->in));
     SAGE_CK(cudaMemcpyAsync(dv + ko, vh + ko, kb, cudaMemcpyHostToDevice, hp->in));
     SAGE_CK(cudaEventRecord(hp->in_done[r], hp->in));
-    // the kernels, in workspace slot r (its previous user, chunk i - 2, ran
-    // earlier on this same stream)
-    SAGE_CK(cudaStreamWaitEvent(stream, hp->in_done[r], 0));
+    // the kernels on compute stream r, in workspace slot r (its previous
+    // user, chunk i - 2, ran earlier on this same stream)
+    cudaStream_t cst = cmp[r];
+    SAGE_CK(cudaStreamWaitEvent(cst, hp->in_done[r], 0));
     char *ws = slots + r * slot;
-    st = sage_quantize_qkv(&cs, mode, flags, bq, bk, dq + qo, dk + ko, dv + ko, ws, slot, (sage_stream_t)stream);
+    st = sage_quantize_qkv(&cs, mode, flags, bq, bk, dq + qo, dk + ko, dv + ko, ws, slot, (sage_stream_t)cst);
     if (st != SAGE_OK) return st;
-    st = sage_attn_fwd(&cs, causal, sm_scale, mode, flags, bq, bk, ws, slot, dO + qo, (sage_stream_t)stream);
+    st = sage_attn_fwd(&cs, causal, sm_scale, mode, flags, bq, bk, ws, slot, dO + qo, (sage_stream_t)cst);
     if (st != SAGE_OK) return st;
     sage_ws_layout L;
     if ((st = compute_layout(&cs, mode, bq, bk, &L)) != SAGE_OK) return st;
-    merge_status_kernel<<<1, 32, 0, stream>>>((const int *)(ws + L.status), status);
+    merge_status_kernel<<<1, 32, 0, cst>>>((const int *)(ws + L.status), status);
     SAGE_CK(cudaGetLastError());
-    SAGE_CK(cudaEventRecord(hp->cmp_done[r], stream));
+    SAGE_CK(cudaEventRecord(hp->cmp_done[r], cst));
     // device -> host: this chunk's output rows
     SAGE_CK(cudaStreamWaitEvent(hp->out, hp->cmp_done[r], 0));
     SAGE_CK(cudaMemcpyAsync(oh + qo, dO + qo, qb, cudaMemcpyDeviceToHost, hp->out));
   }
+  // the caller's stream after the last copy back (which follows both compute
+  // streams' last chunks)
   SAGE_CK(cudaEventRecord(hp->done, hp->out));
   SAGE_CK(cudaStreamWaitEvent(stream, hp->done, 0));
 #undef SAGE_CK

@@ -180,10 +180,11 @@ sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, i
  * (independent problems: their own means and scales, so the result is the
  * same as one call on the whole request) and the copies of one chunk overlap
  * the kernels of the others: host -> device on one internal stream, the
- * kernels on `stream`, device -> host on another internal stream.  The two
- * internal streams and their events are created once per device on the first
- * call (no device memory); the call is ordered after earlier work on `stream`
- * and later work on `stream` after its last copy.  dev_buf is one
+ * kernels of even chunks on `stream` and of odd chunks on a second internal
+ * stream, device -> host on a third.  The internal streams and their events
+ * are created once per device on the first call (no device memory); the call
+ * is ordered after earlier work on `stream` and later work on `stream` after
+ * its last copy.  Calls on one dev_buf must not overlap.  dev_buf is one
  * caller-allocated, 1024-byte aligned device buffer of at least
  * sage_host_buffer_bytes(); its first 16 bytes hold the call's device status
  * word int[4] (code, site: the first error of any chunk) once `stream` has
