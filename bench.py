@@ -78,8 +78,10 @@ def peak_source(mode: int, src: str, bf16: float) -> str:
 ATTN_KERNEL = {0: "attn_q8_kernel", 1: "attn_q8_kernel", 2: "attn_fp4_kernel"}
 # the files each attention kernel is compiled from (its DRAM traffic depends on
 # nothing else in the library)
-ATTN_SOURCES = {0: ("attn_q8.cu", "attn_q8.cuh", "sm103.cuh", "layout.h", "launch.h"),
-                1: ("attn_q8.cu", "attn_q8.cuh", "sm103.cuh", "layout.h", "launch.h"),
+ATTN_SOURCES = {0: ("attn_q8.cu", "attn_q8.cuh", "attn_q8x2.cuh", "attn_q8x2_64.cu", "sm103.cuh", "layout.h",
+                    "launch.h"),
+                1: ("attn_q8.cu", "attn_q8.cuh", "attn_q8x2.cuh", "attn_q8x2_64.cu", "sm103.cuh", "layout.h",
+                    "launch.h"),
                 2: ("attn_fp4.cu", "sm103.cuh", "layout.h", "launch.h")}
 
 

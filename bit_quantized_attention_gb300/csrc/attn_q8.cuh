@@ -148,8 +148,9 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c) {
   return (uint32_t)((r >> 3) * (8 * SW) + (r & 7) * SW + ((c ^ x) << 4));
 }
 
-// Work item idx of the grid-wide list: longest causal rows first (batched:
-// by block index; kVar, packed sequences: the table's order).  N, M: the
+// Work item idx of the grid-wide list: longest causal rows first (batched
+// causal: by block index, heads interleaved; batched non-causal: head-major;
+// kVar, packed sequences: the table's order).  N, M: the
 // item's query and key counts (the request's, or its sequence's); q0: the
 // sequence's first row in the packed output (kVar).
 struct Item {
@@ -166,10 +167,19 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
     it.N = sq.N;
     it.M = sq.M;
     it.q0 = sq.q0;
-  } else {
+  } else if (p.causal) {
+    // longest rows first, heads interleaved: the causal items differ in length
     const int BH = p.items / p.Tm;
     it.qi = p.Tm - 1 - idx / BH;
     it.bh = idx % BH;
+    it.N = p.N;
+    it.M = p.M;
+    it.q0 = 0;
+  } else {
+    // head-major: items of equal length, and the CTAs in flight share one or
+    // two heads' K / V tiles, which stay in L2 while every block streams them
+    it.qi = idx % p.Tm;
+    it.bh = idx / p.Tm;
     it.N = p.N;
     it.M = p.M;
     it.q0 = 0;

@@ -113,15 +113,21 @@ __device__ __forceinline__ uint32_t x2_swz(int r, int c) {
 }
 
 // Work item idx: query blocks 2p and 2p + 1 of head bh (longest causal rows
-// first); T key tiles of 64, enough for the item's last valid row.
+// first, heads interleaved; non-causal: head-major); T key tiles of 64,
+// enough for the item's last valid row.
 struct X2Item {
   int bh, p, hkv, T;
 };
 __device__ __forceinline__ X2Item x2_item(const X2Params &q, int idx) {
   X2Item it;
   const int BH = q.items / q.Tp;
-  it.p = q.Tp - 1 - idx / BH;
-  it.bh = idx % BH;
+  if (q.causal) {  // longest rows first, heads interleaved
+    it.p = q.Tp - 1 - idx / BH;
+    it.bh = idx % BH;
+  } else {  // head-major: the CTAs in flight share a head's K / V tiles in L2
+    it.p = idx % q.Tp;
+    it.bh = idx / q.Tp;
+  }
   const int b = it.bh / q.Hq, h = it.bh % q.Hq;
   it.hkv = b * q.Hkv + h / (q.Hq / q.Hkv);
   const int last_row = min(q.N, it.p * 256 + 256) - 1;

@@ -54,7 +54,7 @@ def test_kernel_hash_ignores_comments_not_code(tmp_path, monkeypatch):
 def test_traffic_record_needs_the_kernels_current_sources(tmp_path, monkeypatch):
     d = tmp_path / "bit_quantized_attention_gb300" / "csrc"
     d.mkdir(parents=True)
-    for f in ("attn_q8.cu", "attn_q8.cuh", "sm103.cuh", "layout.h", "launch.h", "api.cu", "attn_fp4.cu"):
+    for f in set(bench.ATTN_SOURCES[0]) | set(bench.ATTN_SOURCES[2]) | {"api.cu"}:
         (d / f).write_text("int %s_x;\n" % f.replace(".", "_"))
     root = str(tmp_path)
     monkeypatch.setattr(bench, "ROOT", root)

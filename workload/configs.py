@@ -53,6 +53,8 @@ class Config:
     v_bias_std: float = 0.0              # per-(b, head, channel) bias
     v_student_t: float = 0.0             # >0: V ~ Student-t with this many degrees of freedom
     v_clip: float = 0.0                  # >0: clip V to +-v_clip
+    q_from_k_noise: float = 0.0          # >0: each query row is a random key row of its kv head
+                                         # (before K's offsets) plus N(0, noise^2): peaked rows
     note: str = ""
 
     @property

@@ -26,6 +26,12 @@ def make_qkv_float(cfg: Config):
 
     q = rq.standard_normal((B, Hq, N, d), dtype=np.float32)
     k = rk.standard_normal((B, Hkv, M, d), dtype=np.float32)
+    if cfg.q_from_k_noise > 0:
+        # peaked attention: query i of head h copies key pick[i] of its kv head
+        g = Hq // Hkv
+        pick = rq.integers(0, M, size=(B, Hq, N))
+        kk = np.repeat(k, g, axis=1)
+        q = np.take_along_axis(kk, pick[..., None], axis=2) + q * np.float32(cfg.q_from_k_noise)
 
     if cfg.v_student_t > 0:
         nu = cfg.v_student_t
