@@ -98,7 +98,10 @@ struct Cfg {
   static constexpr int NFLOAT = NB * 128 /*alpha*/ + NB * 256 /*l*/ + 4 * 128 /*max*/ + NB * BK /*dS*/ + 2 * D /*q_bar*/ +
                                 (kPV16 ? 2 * NB * 128 : 0) /*s_P s_V, final max*/;
   static constexpr int UB_BYTES = kDsT ? 16 * ROWB : 0;  // one q_bar tile (16 rows, K-major, swizzled)
-  static constexpr int FIXED = Q_BYTES + NB * P_BYTES + 2 * UB_BYTES;
+  // one augmentation operand of the QK product: 128 rows of 8 TF32 words
+  // (32-byte rows, 32-byte swizzle); per item the rows' 1/delta_Q, per tile the keys' dS
+  static constexpr int AUG_BYTES = kDsT ? 128 * 32 : 0;
+  static constexpr int FIXED = Q_BYTES + NB * P_BYTES + 2 * UB_BYTES + (2 + NB) * AUG_BYTES;
   static constexpr int MISC = NFLOAT * 4 + 512;  // floats, then barriers
   // K and V have rings of their own: a K tile is free once its QK has run
   // (and, with dS, once the accumulation warpgroup has read it); a V tile once its PV has
@@ -120,6 +123,8 @@ struct Cfg {
   static_assert(!kPV16 || (kQK16 && BK == 64), "SageBwd forward: INT8 codes, 64-key tiles");
   // dS^T = K^ (128 keys x d, A) x q_bar tile (16 x d, B): column 0 the hi row, 1 the lo row
   static constexpr uint32_t IDESC_DS = instr_desc(kFmtF32, kFmtF16, kFmtF16, 16, 128);
+  // S = [1/delta_Q row augmentation] x [dS key augmentation]^T, then += Q^ K^T
+  static constexpr uint32_t IDESC_AUG = instr_desc(kFmtF32, kFmtTF32, kFmtTF32, BK, 128);
 };
 
 struct AttnParams {
@@ -231,8 +236,9 @@ __device__ __forceinline__ float qbar_dot_key(const uint8_t *kt, const float *qb
   return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
 }
 
-// kSmoothQ: Q smoothing on (dS added to the scores); its instances carry the dS
-// stream, the others none of its state.  kPV16: the SageBwd forward.  kPing:
+// kSmoothQ: Q smoothing on (dS added to the scores, or folded into S by the
+// tensor core); its instances carry the dS stream, the others none of its
+// state.  kPV16: the SageBwd forward.  kPing:
 // the softmax warpgroups take whole key tiles in turn instead of halves of
 // every tile (INT8 / FP8 P~).  kVar: packed sequences (work item table and
 // per-sequence lengths).
@@ -240,9 +246,12 @@ template <int D, int BK, bool kQK16, bool kSmoothQ, bool kPV16, bool kPing = fal
 __global__ void __launch_bounds__(kThreads, 1)
     attn_q8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles);
-  // otherwise the accumulation warpgroup takes it on CUDA cores
+  // dS on the tensor core where the codes allow it (INT8 as fp16, 128-key tiles),
+  // folded into S; otherwise the accumulation warpgroup takes it on CUDA cores
+  // and the softmax adds it
   constexpr bool kDsMma = kSmoothQ && kQK16 && BK == 128;
+  // the softmax adds dS itself (the CUDA-core dS); with kDsMma it comes inside S
+  constexpr bool kDsAdd = kSmoothQ && !kDsMma;
   static_assert(!kPing || !kPV16, "tiles in turn: FP8 P~");
   using C = Cfg<D, BK, kQK16, kDsMma, kPV16>;
   constexpr int KST = C::KST, VST = C::VST;
@@ -254,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sK = sP + NB * C::P_BYTES;   // [KST]
   uint8_t *sV = sK + KST * C::K_BYTES;  // [VST]
   uint8_t *sU = sV + VST * C::V_BYTES;  // [2 item parities] q_bar tiles (dS on the tensor core)
-  float *s_alpha = (float *)(sU + 2 * C::UB_BYTES);  // [NB][128]
+  uint8_t *sAq = sU + 2 * C::UB_BYTES;   // [2 item parities] row augmentation: 1/delta_Q
+  uint8_t *sAk = sAq + 2 * C::AUG_BYTES; // [NB] key augmentation: dS of a tile
+  float *s_alpha = (float *)(sAk + NB * C::AUG_BYTES);  // [NB][128]
   float *s_l = s_alpha + NB * 128;                   // [NB][2 halves][128], at an item's last tile
   float *s_mx = s_l + NB * 256;                      // [2 parities][2 halves][128]
   float *s_ds = s_mx + 4 * 128;                      // [NB][BK] dS of a tile, in t units
@@ -278,8 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *dsr_full = qb_full + 2;  // [NB] dS^T of a tile in TMEM (tensor-core dS)
   uint64_t *dsr_free = dsr_full + NB;  // [NB] that TMEM region read
   uint64_t *ub_full = dsr_free + NB;   // [2] q_bar tile of an item written
-  uint64_t *ub_empty = ub_full + 2;    // [2] its last dS MMA done
-  uint64_t *qk_done = ub_empty + 2;
+  uint64_t *ub_empty = ub_full + 2;    // [2] its last dS MMA and QK done
+  uint64_t *aug_full = ub_empty + 2;   // [NB] key augmentation of a tile written
+  uint64_t *aug_empty = aug_full + NB; // [NB] its QK done
+  uint64_t *qk_done = aug_empty + NB;
   uint64_t *pv_done = qk_done + 1;
   uint32_t *s_tmem = (uint32_t *)(pv_done + 1);
   volatile int *s_abort = (volatile int *)(s_tmem + 1);
@@ -307,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ds_full[x], kWG);
       mbar_init(&dsr_full[x], 1);
       mbar_init(&dsr_free[x], kWG);
+      mbar_init(&aug_full[x], kWG);
+      mbar_init(&aug_empty[x], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&ub_full[x], kWG);
@@ -415,24 +430,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       // limit, before any other wait of the CTA could) and the CTA unwinds
       bool ok = !p.stall || __all_sync(0xffffffffu, mbar_wait(qk_done, 0, status, 29, s_abort, p.spin >> 1));
       int gt = 0;
+      // Q smoothing on the tensor core: dS^T(tile) = K^ q_bar^T into dS region
+      // dg % NB as soon as the K^ tile has landed, one tile ahead of its QK.
+      // The accumulation warpgroup turns it into the key augmentation of the
+      // tile, and QK(tile) starts from [1/delta_Q] x [dS]^T (one TF32 step)
+      // before adding Q^ K^T, so S arrives with dS / delta_Q folded in.  dS
+      // stream: tile dg is tile dj of the CTA's item dn (dT tiles).
+      int dg = 0, dn = 0, dj = 0, dT = 0;
+      bool d_more = kDsMma && blockIdx.x < p.items;
+      if (d_more) dT = item_of<kVar>(p, blockIdx.x, BK).T;
+      auto issue_ds = [&]() -> bool {  // false: a wait failed
+        const int b2 = dg % NB, s2 = dg % KST;
+        // the item's q_bar tile and row augmentation, a free dS region, the K^ tile
+        bool w = dj > 0 || mbar_wait(&ub_full[dn & 1], (dn >> 1) & 1, status, 26, s_abort, p.spin);
+        if (dg >= NB) w = w && mbar_wait(&dsr_free[b2], ((dg - NB) / NB) & 1, status, 28, s_abort, p.spin);
+        w = w && mbar_wait(&k_full[s2], (dg / KST) & 1, status, 21, s_abort, p.spin);
+        if (!__all_sync(0xffffffffu, w)) return false;
+        tc_fence_after();
+        if (elect_one()) {
+          // the K^ tile as A (128 keys), the item's q_bar tile as B (16 rows: hi, lo, zeros)
+          const uint32_t u_base = smem_u32(sU) + (dn & 1) * C::UB_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
+            const int byte = kk * 32;
+            const uint32_t ak = k_base + s2 * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
+            const uint32_t bu = u_base + (byte / C::QK_SW) * 16 * C::QK_SW + (byte % C::QK_SW);
+            mma_f16(tmem + C::DS_COL + b2 * 16, smem_desc(ak, 8 * C::QK_SW, kSwizzle128),
+                    smem_desc(bu, 8 * C::QK_SW, kSwizzle128), C::IDESC_DS, kk > 0);
+          }
+          mma_commit(&dsr_full[b2]);
+        }
+        __syncwarp();
+        ++dg;
+        if (++dj == dT) {
+          dj = 0;
+          const int nx = blockIdx.x + (++dn) * G;
+          d_more = nx < p.items;
+          if (d_more) dT = item_of<kVar>(p, nx, BK).T;
+        }
+        return true;
+      };
       for (int n = 0; ok && blockIdx.x + n * G < p.items; ++n) {
         const Item it = item_of<kVar>(p, blockIdx.x + n * G, BK);
         if (!__all_sync(0xffffffffu, mbar_wait(q_full, n & 1, status, 23, s_abort, p.spin))) break;
-        // the item's q_bar tile (tensor-core dS)
-        if (kDsMma && !__all_sync(0xffffffffu, mbar_wait(&ub_full[n & 1], (n >> 1) & 1, status, 26, s_abort, p.spin)))
-          break;
         for (int j = 0; j < it.T; ++j, ++gt) {
           const int b = gt % NB, s = gt % KST;
+          while (kDsMma && ok && d_more && dg <= gt + 1) ok = issue_ds();
+          if (!ok) break;
           bool w = true;
           if (gt >= NB) w = mbar_wait(&sr_free[b], ((gt - NB) / NB) & 1, status, 20, s_abort, p.spin);
-          if (kDsMma && gt >= NB) w = w && mbar_wait(&dsr_free[b], ((gt - NB) / NB) & 1, status, 28, s_abort, p.spin);
-          w = w && mbar_wait(&k_full[s], (gt / KST) & 1, status, 21, s_abort, p.spin);
+          if (kDsMma)  // the key augmentation (its K^ tile landed before its dS MMA)
+            w = w && mbar_wait(&aug_full[b], (gt / NB) & 1, status, 30, s_abort, p.spin);
+          else
+            w = w && mbar_wait(&k_full[s], (gt / KST) & 1, status, 21, s_abort, p.spin);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (elect_one()) {
+            if constexpr (kDsMma)
+              mma_tf32(tmem + b * C::SRW, smem_desc(smem_u32(sAq) + (n & 1) * C::AUG_BYTES, 256, kSwizzle32),
+                       smem_desc(smem_u32(sAk) + b * C::AUG_BYTES, 256, kSwizzle32), C::IDESC_AUG, 0);
 #pragma unroll
             for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
               const int byte = kk * 32;
@@ -441,29 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = smem_desc(aq, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
               const uint64_t bd = smem_desc(bk, 8 * C::QK_SW, C::QK_SW == 128 ? kSwizzle128 : kSwizzle64);
               if (kQK16)
-                mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
+                mma_f16(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kDsMma || kk > 0);
               else
                 mma_f8(tmem + b * C::SRW, ad, bd, C::IDESC_QK, kk > 0);
             }
             mma_commit(&s_full[b]);
-            if constexpr (kDsMma) {
-              // dS^T(tile) = K^ q_bar^T: the K^ tile as A (128 keys), the item's
-              // q_bar tile as B (16 rows: hi, lo, zeros) into dS region b
-              const uint32_t u_base = smem_u32(sU) + (n & 1) * C::UB_BYTES;
-#pragma unroll
-              for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
-                const int byte = kk * 32;
-                const uint32_t ak = k_base + s * C::K_BYTES + (byte / C::QK_SW) * BK * C::QK_SW + (byte % C::QK_SW);
-                const uint32_t bu = u_base + (byte / C::QK_SW) * 16 * C::QK_SW + (byte % C::QK_SW);
-                mma_f16(tmem + C::DS_COL + b * 16, smem_desc(ak, 8 * C::QK_SW, kSwizzle128),
-                        smem_desc(bu, 8 * C::QK_SW, kSwizzle128), C::IDESC_DS, kk > 0);
-              }
-              mma_commit(&dsr_full[b]);
-            }
+            if (kDsMma) mma_commit(&aug_empty[b]);
             mma_commit(&k_empty[s]);
             if (j == it.T - 1) {
               mma_commit(q_empty);  // Q^ may be replaced once these MMAs are done
-              if (kDsMma) mma_commit(&ub_empty[n & 1]);  // and the item's q_bar tile
+              if (kDsMma) mma_commit(&ub_empty[n & 1]);  // and the item's q_bar tile and row augmentation
             }
           }
           __syncwarp();
@@ -548,11 +594,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Tensor-core dS: the q_bar tile of item u (fp16 rows: hi = q_bar rounded
     // toward zero, lo = the rest rounded to nearest; |q_bar| < 2^16 by the
-    // pre-pass range check, so hi + lo carries 22 bits) goes into buffer u & 1
-    // once the item u - 2 that used it has had its last dS MMA (ub_empty), and
-    // is published to the QK issuer through ub_full (every thread arrives after
-    // its writes and a proxy fence).  Rows 2..15 stay zero.  un counts the
-    // items written so far.
+    // pre-pass range check, so hi + lo carries 22 bits) and the item's row
+    // augmentation go into buffer u & 1 once the item u - 2 that used them has
+    // had its last QK (ub_empty), and are published to the QK issuer through
+    // ub_full (every thread arrives after its writes and a proxy fence).  Rows
+    // 2..15 of the q_bar tile stay zero.  Row r of the augmentation holds
+    // a = 1/u_r as TF32 hi, hi, lo, lo in its first 16 bytes and zeros in the
+    // next 16 (u_r = delta_Q of the row, or 1 where that is 0: a block whose
+    // smoothed Q codes are all zero); the key augmentation repeats its pair in
+    // both 16-byte halves of a row, so the product a dS comes out whichever
+    // half the 32-byte swizzle puts first.  un counts the items written so far.
     int un = 0;
     auto prep_ub = [&](int u, bool block) -> int {  // 1 written, 0 not yet, -1 wait failed
       if (u >= 2) {
@@ -570,6 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int byte = 2 * r, cc = byte / C::QK_SW, bb = byte % C::QK_SW;
         *reinterpret_cast<__half *>(ub + cc * 16 * C::QK_SW + swz_off<C::QK_SW>(0, bb / 16) + (bb & 15)) = hi;
         *reinterpret_cast<__half *>(ub + cc * 16 * C::QK_SW + swz_off<C::QK_SW>(1, bb / 16) + (bb & 15)) = lo;
+      }
+      {
+        const float dq = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)t.bh * p.N_pad + t.row0 + r]
+                                                      : p.dq[(size_t)t.bh * p.Tm + t.qi];
+        const float a = 1.0f / (dq > 0.0f ? dq : 1.0f);
+        const uint32_t ah = __float_as_uint(a) & kTf32Mask;
+        const uint32_t al = __float_as_uint(a - __uint_as_float(ah)) & kTf32Mask;
+        uint4 *row = reinterpret_cast<uint4 *>(sAq + (u & 1) * C::AUG_BYTES + r * 32);
+        row[0] = make_uint4(ah, ah, al, al);
+        row[1] = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       mbar_arrive(&ub_full[u & 1]);
@@ -591,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < it.T; ++j, ++gt) {
         const int b = gt % NB;
         while (kDsMma && d_more && dg < gt + 3) {
-          // dS_j[c] = delta_K,j (K^_j q_bar^T)[c], in t units, from the tensor core: thread r takes key r
+          // the key augmentation of tile dg from its dS^T = K^ q_bar^T in TMEM:
+          // thread r takes key r, b = K^_r . q_bar split into TF32 hi + lo
           bool prep_ok = true;
           while (un <= dn && prep_ok) prep_ok = prep_ub(un++, true) > 0;
           if (!prep_ok) {
@@ -607,14 +669,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // the buffer's previous tile dg - NB has had its QK
+          if (dg >= NB &&
+              !__all_sync(0xffffffffu, mbar_wait(&aug_empty[b2], ((dg - NB) / NB) & 1, status, 45, s_abort, p.spin))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           uint32_t dh, dl;
           tmem_ld2(tmem + lane_off + C::DS_COL + b2 * 16, dh, dl);
           tmem_wait_ld();
-          s_ds[b2 * BK + r] = (__uint_as_float(dh) + __uint_as_float(dl)) * d_dk[dj] * c2;
           tc_fence_before();
           mbar_arrive(&dsr_free[b2]);
-          mbar_arrive(&ds_full[b2]);
+          const float bv = __uint_as_float(dh) + __uint_as_float(dl);
+          const uint32_t bh = __float_as_uint(bv) & kTf32Mask;
+          const uint32_t bl = __float_as_uint(bv - __uint_as_float(bh)) & kTf32Mask;
+          uint4 *row = reinterpret_cast<uint4 *>(sAk + b2 * C::AUG_BYTES + r * 32);
+          row[0] = make_uint4(bh, bl, bh, bl);
+          row[1] = make_uint4(bh, bl, bh, bl);
+          fence_proxy_async_smem();
+          mbar_arrive(&aug_full[b2]);
           ++dg;
           if (++dj == dT) {
             dj = 0;
@@ -751,15 +825,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; !stop && blockIdx.x + n * G < p.items; ++n) {
       const Item it = item_of<kVar>(p, blockIdx.x + n * G, BK);
       const int diag = it.row0 + r + it.M - it.N;  // last key visible to this row (causal)
-      const float dq = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
-                                                    : p.dq[(size_t)it.bh * p.Tm + it.qi];
+      const float dq0 = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
+                                                     : p.dq[(size_t)it.bh * p.Tm + it.qi];
+      const float dq = (kDsMma && !(dq0 > 0.0f)) ? 1.0f : dq0;  // the unit S comes in (dS folded)
       const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
       for (int j = 0; j < it.T; ++j, ++gt) {
         if ((gt & 1) != wg) continue;
         const int bb = gt % NB;
         const float dkj = dkr[j];  // in flight during the S wait
         const bool okw = mbar_wait(&s_full[bb], (gt / NB) & 1, status, 32, s_abort, p.spin) &&
-                         (!kSmoothQ || mbar_wait(&ds_full[bb], (gt / NB) & 1, status, 31, s_abort, p.spin));
+                         (!kDsAdd || mbar_wait(&ds_full[bb], (gt / NB) & 1, status, 31, s_abort, p.spin));
         if (!__all_sync(0xffffffffu, okw)) {
           stop = true;
           break;
@@ -769,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // x orders like t: the raw MMA output with the scale folded into the
         // exponent when k1 > 0 and there is no dS, else t itself (a masked -inf
         // never meets a 0)
-        const bool raw = !kSmoothQ && k1 > 0.0f;
+        const bool raw = !kDsAdd && k1 > 0.0f;
         const float *dsc = s_ds + bb * BK;  // dS of the tile in t units (Q smoothing)
         const float xs = raw ? k1 : 1.0f;
         const bool edge = (j * BK + BK > it.M) || (p.causal && j * BK + BK - 1 > it.row0 + it.M - it.N);
@@ -785,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float x = __uint_as_float(v[e]);
-            if constexpr (kSmoothQ)
+            if constexpr (kDsAdd)
               x = fmaf(x, k1, dsc[ch * 32 + e]);
             else if (!raw)
               x *= k1;
@@ -824,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
-            if constexpr (kSmoothQ) {
+            if constexpr (kDsAdd) {
               const float2 t2 = __ffma2_rn(make_float2(x0, x1), make_float2(k1, k1),
                                            *reinterpret_cast<const float2 *>(dsc + ch * 32 + e));
               x0 = t2.x;
@@ -875,8 +950,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_of<kVar>(p, blockIdx.x + n * G, BK);
       const int diag = it.row0 + r + it.M - it.N;  // last key visible to this row (causal)
       // this row's Q scale: its own (per-token Q) or its block's
-      const float dq = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
-                                                    : p.dq[(size_t)it.bh * p.Tm + it.qi];
+      const float dq0 = (p.flags & SAGE_Q_PER_TOKEN) ? p.dqt[(size_t)it.bh * p.N_pad + it.row0 + r]
+                                                     : p.dq[(size_t)it.bh * p.Tm + it.qi];
+      const float dq = (kDsMma && !(dq0 > 0.0f)) ? 1.0f : dq0;  // the unit S comes in (dS folded)
       float m = -INFINITY, l = 0.0f;
       const float *dkr = p.dk + (size_t)it.hkv * p.Tn;
       const float *dvbr = kPV16 ? p.dvb + (size_t)it.hkv * p.Tn : nullptr;  // SageBwd V block scales
@@ -887,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float k1 = dq * dkj * c2;  // S code -> t
         // the TMEM loads are warp-collective: the warp decides together
         const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[bb], pj, status, 32, s_abort, p.spin) &&
-                                                     (!smooth_q || mbar_wait(&ds_full[bb], pj, status, 31, s_abort, p.spin)));
+                                                     (!kDsAdd || mbar_wait(&ds_full[bb], pj, status, 31, s_abort, p.spin)));
         if (!okw) {
           stop = true;
           break;
@@ -898,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with k1 > 0 that is the raw MMA output (t = x k1, the scale folded
         // into the exponent below); otherwise t itself (xs = 1), so a masked
         // -inf never meets a zero scale.
-        const bool raw = !smooth_q && k1 > 0.0f;
+        const bool raw = !kDsAdd && k1 > 0.0f;
         const float xs = raw ? k1 : 1.0f;
         float x[HALF];
         {
@@ -911,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < HALF; ++e) x[e] = __uint_as_float(v[e]);
         }
         if (!raw) {
-          if (smooth_q) {
+          if (kDsAdd) {
             const float4 *dsc = reinterpret_cast<const float4 *>(s_ds + bb * BK + hf * HALF);
             const float2 k12 = make_float2(k1, k1);
 #pragma unroll

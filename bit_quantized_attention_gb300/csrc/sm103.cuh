@@ -226,20 +226,30 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes
   return d;
 }
 
-// Instruction descriptor (kind::f16 / kind::f8f6f4, dense, both operands
-// K-major): accumulator format at bits 4-5 (1 = f32), A format bits 7-9,
+// Instruction descriptor (kind::f16 / kind::tf32 / kind::f8f6f4, dense, both
+// operands K-major): accumulator format at bits 4-5 (1 = f32), A format bits 7-9,
 // B format bits 10-12, N/8 at bits 17-22, M/16 at bits 24-28.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t c_fmt, uint32_t a_fmt, uint32_t b_fmt, int n,
                                                   int m) {
   return (c_fmt << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-enum : uint32_t { kFmtF32 = 1, kFmtF16 = 0, kFmtE4M3 = 0 };
+enum : uint32_t { kFmtF32 = 1, kFmtF16 = 0, kFmtE4M3 = 0, kFmtTF32 = 2 };
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// TF32 x TF32 (K = 8 per instruction, operands as 32-bit words whose low 13
+// mantissa bits are not used)
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // the bits of an fp32 word a TF32 operand keeps
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,

@@ -35,6 +35,10 @@ ATTN_SMALL = SMALL + [
     _small("per_token_q_causal_many", B=2, Hq=24, Hkv=8, N=600, M=700, causal=True, flags=7 | 0x10, d=128,
            bk=128),
     _small("per_token_q_fp8_d64_bk64", mode=1, N=300, M=450, flags=1 | 0x10, d=64, bk=64),
+    # Q block 2 holds one row: its smoothed Q is zero, so is its scale, and
+    # its scores are the dS term alone
+    _small("smooth_q_one_row_tail", N=257, M=300, flags=3, d=64, bk=128, q_offset_std=2.0),
+    _small("smooth_q_per_token_d64", N=300, M=520, causal=True, flags=3 | 0x10, d=64, bk=128, q_offset_std=2.0),
 ]
 
 FP4_ATTN_SMALL = FP4_SMALL + [
@@ -115,8 +119,22 @@ def test_zero_scale_key_tile(sage, mode):
     check(cfg, o.reshape(-1, cfg.d), q, k, v, rows)
 
 
+@pytest.mark.parametrize("mode,bk", [(0, 128), (0, 64), (1, 128)])
+def test_constant_query_block_with_q_smoothing(sage, mode, bk):
+    """Q block 0 repeats one query row and block 2 holds a single row: with Q
+    smoothing both blocks quantize to zero codes with a zero scale, and their
+    scores are the dS term alone."""
+    cfg = _small("constant_q_block", mode=mode, N=257, M=300, flags=3, d=64, bk=bk, q_offset_std=2.0)
+    q, k, v = make_inputs(cfg)
+    q[:, :, :128, :] = q[:, :, :1, :]
+    o = gpu_attention(sage, cfg, q, k, v)
+    assert np.isfinite(o).all()
+    rows = oracle.all_rows((cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.M, cfg.d))
+    check(cfg, o.reshape(-1, cfg.d), q, k, v, rows)
+
+
 def test_attention_deterministic(sage):
-    cfg = ATTN_SMALL[-2]
+    cfg = next(c for c in ATTN_SMALL if c.name == "per_token_q_causal_many")
     q, k, v = make_inputs(cfg)
     a = gpu_attention(sage, cfg, q, k, v)
     b = gpu_attention(sage, cfg, q, k, v)

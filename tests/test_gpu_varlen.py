@@ -40,6 +40,8 @@ CASES = [
     # name, mode, flags, causal, Hq, Hkv, d, bk, query lengths, key lengths
     ("int8_ragged", 0, 1, False, 4, 2, 64, 64, [200, 0, 1, 333, 64], [130, 9, 1, 700, 64]),
     ("int8_causal_smooth", 0, 7, True, 4, 1, 128, 128, [128, 37, 300], [128, 500, 300]),
+    # a one-query sequence and a 129-query one: Q blocks of one row (zero smoothed codes)
+    ("int8_smooth_q_one_query", 0, 3, False, 2, 2, 64, 128, [1, 129, 200], [50, 300, 129]),
     ("fp8_gqa", 1, 3, False, 8, 2, 128, 128, [90, 256, 17], [1000, 40, 17]),
     ("sagebwd_causal", 3, 1, True, 4, 2, 64, 64, [150, 65, 1], [150, 300, 2]),
     ("int8_per_token_q", 0, 1 | 0x10, True, 2, 2, 128, 64, [129, 400], [129, 401]),
