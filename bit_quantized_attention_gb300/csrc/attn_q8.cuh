@@ -173,10 +173,40 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
     it.M = sq.M;
     it.q0 = sq.q0;
   } else if (p.causal) {
-    // longest rows first, heads interleaved: the causal items differ in length
+    // Causal items differ in length, but a head's query blocks qi and
+    // Tm - 1 - qi together always take the same number of key tiles.  Items
+    // are handed out in such pairs: in round k of the grid (items k G .. k G +
+    // G - 1) CTA c takes the long block of pair (k / 2) G + c when k is even,
+    // its short block when k is odd.  Every CTA then gets the same work per
+    // two rounds, runs both blocks of a pair back to back on one head's K / V,
+    // and the CTAs in flight share G / (Tm / 2) heads' K / V tiles in L2.  The
+    // pairs left after the full rounds, and the middle block of each head
+    // when Tm is odd, come last, longest first.
+    const int G = gridDim.x;
     const int BH = p.items / p.Tm;
-    it.qi = p.Tm - 1 - idx / BH;
-    it.bh = idx % BH;
+    const int PH = p.Tm / 2;  // pairs per head
+    const int NP = BH * PH;
+    const int R = NP / G;     // full rounds of pairs
+    const int mid = (p.Tm & 1) ? BH : 0;
+    if (idx < 2 * R * G) {
+      const int k = idx / G, P = (k >> 1) * G + idx % G;
+      it.bh = P / PH;
+      it.qi = (k & 1) ? P % PH : p.Tm - 1 - P % PH;
+    } else {
+      const int rem = idx - 2 * R * G, r = NP - R * G;
+      if (rem < r) {  // long blocks of the last pairs
+        const int P = R * G + rem;
+        it.bh = P / PH;
+        it.qi = p.Tm - 1 - P % PH;
+      } else if (rem < r + mid) {  // middle blocks
+        it.bh = rem - r;
+        it.qi = PH;
+      } else {  // short blocks of the last pairs
+        const int P = R * G + rem - r - mid;
+        it.bh = P / PH;
+        it.qi = P % PH;
+      }
+    }
     it.N = p.N;
     it.M = p.M;
     it.q0 = 0;
@@ -255,6 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(!kPing || !kPV16, "tiles in turn: FP8 P~");
   using C = Cfg<D, BK, kQK16, kDsMma, kPV16>;
   constexpr int KST = C::KST, VST = C::VST;
+  // tensor-core dS: how many tiles ahead of a QK the issuer runs the dS MMA
+  // (it waits for that K^ tile first, so the lead stays below the K^ ring)
+  constexpr int kDsAhead = KST >= 3 ? 2 : 1;
   constexpr int HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -431,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = !p.stall || __all_sync(0xffffffffu, mbar_wait(qk_done, 0, status, 29, s_abort, p.spin >> 1));
       int gt = 0;
       // Q smoothing on the tensor core: dS^T(tile) = K^ q_bar^T into dS region
-      // dg % NB as soon as the K^ tile has landed, one tile ahead of its QK.
+      // dg % NB as soon as the K^ tile has landed, kDsAhead tiles ahead of its QK.
       // The accumulation warpgroup turns it into the key augmentation of the
       // tile, and QK(tile) starts from [1/delta_Q] x [dS]^T (one TF32 step)
       // before adding Q^ K^T, so S arrives with dS / delta_Q folded in.  dS
@@ -475,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(q_full, n & 1, status, 23, s_abort, p.spin))) break;
         for (int j = 0; j < it.T; ++j, ++gt) {
           const int b = gt % NB, s = gt % KST;
-          while (kDsMma && ok && d_more && dg <= gt + 1) ok = issue_ds();
+          while (kDsMma && ok && d_more && dg <= gt + kDsAhead) ok = issue_ds();
           if (!ok) break;
           bool w = true;
           if (gt >= NB) w = mbar_wait(&sr_free[b], ((gt - NB) / NB) & 1, status, 20, s_abort, p.spin);
@@ -578,7 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after this read and the QK commit.  q_bar of item dn sits in
     // s_qb[dn & 1], published through qb_full[dn & 1]: every thread arrives
     // there after its last dS of item dn - 1, so no one still reads the
-    // buffer's previous item dn - 2.
+    // buffer's previous item dn - 2.  With the tensor-core dS the stream
+    // reaches up to tile gt + 1 + kDsAhead, the tiles past gt + 1 only when
+    // their dS and key-augmentation buffer are there already.
     static_assert(NB >= 3, "dS buffers: tiles gt + 1 and gt + 2 beside gt - 1");
     int dn = 0, dj = 0, dg = 0, dT = 0;
     const float *d_dk = nullptr;  // delta_K row of item dn
@@ -651,27 +686,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lsum = 0.0f, mrow = 0.0f;
       for (int j = 0; j < it.T; ++j, ++gt) {
         const int b = gt % NB;
-        while (kDsMma && d_more && dg < gt + 3) {
+        while (kDsMma && d_more && dg < gt + 2 + kDsAhead) {
           // the key augmentation of tile dg from its dS^T = K^ q_bar^T in TMEM:
-          // thread r takes key r, b = K^_r . q_bar split into TF32 hi + lo
-          bool prep_ok = true;
-          while (un <= dn && prep_ok) prep_ok = prep_ub(un++, true) > 0;
-          if (!prep_ok) {
+          // thread r takes key r, b = K^_r . q_bar split into TF32 hi + lo.
+          // Up to tile gt + 1 the warpgroup waits for what it needs; beyond
+          // that it takes a tile only if everything is there already
+          const bool lazy = dg >= gt + 2;
+          int pr = 1;
+          while (un <= dn && pr > 0) {
+            pr = prep_ub(un, !lazy);
+            if (pr > 0) ++un;
+          }
+          if (pr < 0) {
             ok = false;
             break;
           }
+          if (pr == 0) break;  // not yet: later
           if (un == dn + 1 && blockIdx.x + un * G < p.items && prep_ub(un, false) > 0) ++un;
           const int b2 = dg % NB;
           const uint32_t ph = (dg / NB) & 1;
-          if (dg == gt + 2) {
-            if (!__all_sync(0xffffffffu, mbar_test_wait(&dsr_full[b2], ph))) break;  // not yet: later
-          } else if (!__all_sync(0xffffffffu, mbar_wait(&dsr_full[b2], ph, status, 42, s_abort, p.spin))) {
-            ok = false;
-            break;
-          }
-          // the buffer's previous tile dg - NB has had its QK
-          if (dg >= NB &&
-              !__all_sync(0xffffffffu, mbar_wait(&aug_empty[b2], ((dg - NB) / NB) & 1, status, 45, s_abort, p.spin))) {
+          // dS of the tile in TMEM; its buffer's previous tile dg - NB has had its QK
+          const uint32_t pe = ((dg - NB) / NB) & 1;
+          if (lazy) {
+            if (!__all_sync(0xffffffffu, mbar_test_wait(&dsr_full[b2], ph) &&
+                                             (dg < NB || mbar_test_wait(&aug_empty[b2], pe))))
+              break;  // not yet: later
+          } else if (!__all_sync(0xffffffffu, mbar_wait(&dsr_full[b2], ph, status, 42, s_abort, p.spin) &&
+                                                  (dg < NB || mbar_wait(&aug_empty[b2], pe, status, 45, s_abort, p.spin)))) {
             ok = false;
             break;
           }
