@@ -127,6 +127,14 @@ struct Cfg {
   static constexpr uint32_t IDESC_AUG = instr_desc(kFmtF32, kFmtTF32, kFmtTF32, BK, 128);
 };
 
+// The causal work order's per-launch constants (see causal_item): the grid G,
+// pairs per head PH = Tm / 2, the items in full rounds of pairs, the pairs left
+// after them, the middle blocks (one per head when Tm is odd), and 1/G, 1/PH.
+struct CausalOrder {
+  int G, PH, full, rest, mid;
+  float invG, invPH;
+};
+
 struct AttnParams {
   int N, M, N_pad, M_pad, Tm, Tn, Hq, Hkv, causal, flags;
   int items;      // work items (one query block of one head each): B * Hq * Tm, or the table's
@@ -143,6 +151,7 @@ struct AttnParams {
   int *status;
   long long spin;
   int stall;  // test hook: the QK issuer first waits on a barrier nothing arrives on
+  CausalOrder cz;
 };
 
 // byte offset of 16-byte chunk `c` of row `r` in a K-major swizzled tile whose
@@ -161,6 +170,43 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c) {
 struct Item {
   int bh, qi, hkv, row0, T, N, M, q0;
 };
+// a / d for 0 <= a < 2^24 and d >= 1, given inv = fl(1/d): the float quotient
+// is within one of the truth, and one step each way corrects it
+__device__ __forceinline__ int div_small(int a, int d, float inv) {
+  int q = __float2int_rz(__int2float_rn(a) * inv);
+  q -= (q * d > a) ? 1 : 0;
+  q += ((q + 1) * d <= a) ? 1 : 0;
+  return q;
+}
+
+// Causal items differ in length, but a head's query blocks qi and Tm - 1 - qi
+// together always take the same number of key tiles.  Items are handed out in
+// such pairs: in round k of the grid (items k G .. k G + G - 1) CTA c takes the
+// long block of pair (k / 2) G + c when k is even, its short block when k is
+// odd.  Every CTA then gets the same work per two rounds, runs both blocks of
+// a pair back to back on one head's K / V, and the CTAs in flight share
+// G / (Tm / 2) heads' K / V tiles in L2.  The pairs left after the full rounds,
+// and the middle block of each head when Tm is odd, come last, longest first.
+// The launcher supplies G and the pair counts (AttnParams::cz); every division
+// here is by one of them.  Returns (head, query block).
+__device__ __forceinline__ int2 causal_item(const AttnParams &p, int idx) {
+  const CausalOrder &z = p.cz;
+  int P;
+  bool lng;
+  if (idx < z.full) {  // full rounds of pairs
+    const int k = div_small(idx, z.G, z.invG);
+    P = (k >> 1) * z.G + (idx - k * z.G);
+    lng = (k & 1) == 0;
+  } else {
+    const int rem = idx - z.full;
+    if (rem >= z.rest && rem < z.rest + z.mid) return make_int2(rem - z.rest, z.PH);  // middle blocks
+    lng = rem < z.rest;  // long blocks of the last pairs, then their short blocks
+    P = z.full / 2 + (lng ? rem : rem - z.rest - z.mid);
+  }
+  const int h = div_small(P, z.PH, z.invPH), j = P - h * z.PH;
+  return make_int2(h, lng ? p.Tm - 1 - j : j);
+}
+
 template <bool kVar>
 __device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
   Item it;
@@ -173,40 +219,9 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, int idx, int BK) {
     it.M = sq.M;
     it.q0 = sq.q0;
   } else if (p.causal) {
-    // Causal items differ in length, but a head's query blocks qi and
-    // Tm - 1 - qi together always take the same number of key tiles.  Items
-    // are handed out in such pairs: in round k of the grid (items k G .. k G +
-    // G - 1) CTA c takes the long block of pair (k / 2) G + c when k is even,
-    // its short block when k is odd.  Every CTA then gets the same work per
-    // two rounds, runs both blocks of a pair back to back on one head's K / V,
-    // and the CTAs in flight share G / (Tm / 2) heads' K / V tiles in L2.  The
-    // pairs left after the full rounds, and the middle block of each head
-    // when Tm is odd, come last, longest first.
-    const int G = gridDim.x;
-    const int BH = p.items / p.Tm;
-    const int PH = p.Tm / 2;  // pairs per head
-    const int NP = BH * PH;
-    const int R = NP / G;     // full rounds of pairs
-    const int mid = (p.Tm & 1) ? BH : 0;
-    if (idx < 2 * R * G) {
-      const int k = idx / G, P = (k >> 1) * G + idx % G;
-      it.bh = P / PH;
-      it.qi = (k & 1) ? P % PH : p.Tm - 1 - P % PH;
-    } else {
-      const int rem = idx - 2 * R * G, r = NP - R * G;
-      if (rem < r) {  // long blocks of the last pairs
-        const int P = R * G + rem;
-        it.bh = P / PH;
-        it.qi = p.Tm - 1 - P % PH;
-      } else if (rem < r + mid) {  // middle blocks
-        it.bh = rem - r;
-        it.qi = PH;
-      } else {  // short blocks of the last pairs
-        const int P = R * G + rem - r - mid;
-        it.bh = P / PH;
-        it.qi = P % PH;
-      }
-    }
+    const int2 bq = causal_item(p, idx);
+    it.bh = bq.x;
+    it.qi = bq.y;
     it.N = p.N;
     it.M = p.M;
     it.q0 = 0;
@@ -634,11 +649,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // had its last QK (ub_empty), and are published to the QK issuer through
     // ub_full (every thread arrives after its writes and a proxy fence).  Rows
     // 2..15 of the q_bar tile stay zero.  Row r of the augmentation holds
-    // a = 1/u_r as TF32 hi, hi, lo, lo in its first 16 bytes and zeros in the
-    // next 16 (u_r = delta_Q of the row, or 1 where that is 0: a block whose
-    // smoothed Q codes are all zero); the key augmentation repeats its pair in
-    // both 16-byte halves of a row, so the product a dS comes out whichever
-    // half the 32-byte swizzle puts first.  un counts the items written so far.
+    // a = 1/u_r as TF32 hi, hi, lo, lo in its logical first 16 bytes and zeros
+    // in the other 16 (u_r = delta_Q of the row, or 1 where that is 0: a block
+    // whose smoothed Q codes are all zero); key c of the key augmentation holds
+    // dS_c as hi, lo, hi, lo the same way.  The 32-byte swizzle exchanges the
+    // two halves of rows 4..7 of every 8-row group (address bit 7 into bit 4),
+    // so logical half 0 of row r is physical half (r >> 2) & 1; the other half
+    // is zeroed once and never written.  un counts the items written so far.
     int un = 0;
     auto prep_ub = [&](int u, bool block) -> int {  // 1 written, 0 not yet, -1 wait failed
       if (u >= 2) {
@@ -664,16 +681,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ah = __float_as_uint(a) & kTf32Mask;
         const uint32_t al = __float_as_uint(a - __uint_as_float(ah)) & kTf32Mask;
         uint4 *row = reinterpret_cast<uint4 *>(sAq + (u & 1) * C::AUG_BYTES + r * 32);
-        row[0] = make_uint4(ah, ah, al, al);
-        row[1] = make_uint4(0, 0, 0, 0);
+        row[(r >> 2) & 1] = make_uint4(ah, ah, al, al);  // logical chunk 0; chunk 1 stays zero
       }
       fence_proxy_async_smem();
       mbar_arrive(&ub_full[u & 1]);
       return 1;
     };
     if constexpr (kDsMma) {
-      // zero both q_bar tiles once (rows 0 and 1 are rewritten per item)
-      for (int i = r; i < 2 * C::UB_BYTES / 16; i += kWG) reinterpret_cast<uint4 *>(sU)[i] = make_uint4(0, 0, 0, 0);
+      // zero both q_bar tiles (rows 0 and 1 are rewritten per item) and the
+      // augmentation buffers (only each row's logical chunk 0 is rewritten) once
+      for (int i = r; i < (2 * C::UB_BYTES + (2 + NB) * C::AUG_BYTES) / 16; i += kWG)
+        reinterpret_cast<uint4 *>(sU)[i] = make_uint4(0, 0, 0, 0);
       named_bar_sync(3, kWG);
     }
     if (d_more) ds_item(blockIdx.x);
@@ -726,8 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bh = __float_as_uint(bv) & kTf32Mask;
           const uint32_t bl = __float_as_uint(bv - __uint_as_float(bh)) & kTf32Mask;
           uint4 *row = reinterpret_cast<uint4 *>(sAk + b2 * C::AUG_BYTES + r * 32);
-          row[0] = make_uint4(bh, bl, bh, bl);
-          row[1] = make_uint4(bh, bl, bh, bl);
+          row[(r >> 2) & 1] = make_uint4(bh, bl, bh, bl);  // logical chunk 0; chunk 1 stays zero
           fence_proxy_async_smem();
           mbar_arrive(&aug_full[b2]);
           ++dg;
@@ -1208,6 +1225,18 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   }
   const int grid = p.items < sms ? p.items : sms;
   if (grid <= 0) return SAGE_OK;  // no work item (packed sequences without queries are rejected earlier)
+  if (p.causal && !var.item_tab) {
+    if (p.items >= (1 << 24)) return SAGE_ERR_UNSUPPORTED;  // causal_item divides in fp32
+    CausalOrder &z = p.cz;
+    const int BH = p.items / p.Tm, NP = BH * (p.Tm / 2), R = NP / grid;
+    z.G = grid;
+    z.PH = p.Tm / 2;
+    z.full = 2 * R * grid;
+    z.rest = NP - R * grid;
+    z.mid = (p.Tm & 1) ? BH : 0;
+    z.invG = 1.0f / (float)grid;
+    z.invPH = z.PH > 0 ? 1.0f / (float)z.PH : 0.0f;
+  }
   kern<<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }
