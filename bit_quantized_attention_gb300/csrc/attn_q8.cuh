@@ -710,17 +710,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Up to tile gt + 1 the warpgroup waits for what it needs; beyond
           // that it takes a tile only if everything is there already
           const bool lazy = dg >= gt + 2;
+          // the q_bar tiles: every item up to dn (waiting for a buffer unless
+          // lazy) and item dn + 1 if its buffer is free; one call site keeps
+          // this loop's code small
           int pr = 1;
-          while (un <= dn && pr > 0) {
-            pr = prep_ub(un, !lazy);
-            if (pr > 0) ++un;
+          while (un <= dn + 1) {
+            const bool need = un <= dn;
+            if (!need && blockIdx.x + un * G >= p.items) break;  // no item dn + 1
+            const int rv = prep_ub(un, need && !lazy);
+            if (rv > 0) {
+              ++un;
+              continue;
+            }
+            if (need) pr = rv;  // 0: not yet (lazy), -1: the wait failed
+            break;              // item dn + 1's buffer not free yet: later
           }
           if (pr < 0) {
             ok = false;
             break;
           }
           if (pr == 0) break;  // not yet: later
-          if (un == dn + 1 && blockIdx.x + un * G < p.items && prep_ub(un, false) > 0) ++un;
           const int b2 = dg % NB;
           const uint32_t ph = (dg / NB) & 1;
           // dS of the tile in TMEM; its buffer's previous tile dg - NB has had its QK
@@ -1063,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < HALF; ++e) x[e] *= k1;
           }
         }
-        if ((j * BK + BK > it.M) || (p.causal && j * BK + BK - 1 > it.row0 + it.M - it.N)) {
+        if (__builtin_expect((j * BK + BK > it.M) || (p.causal && j * BK + BK - 1 > it.row0 + it.M - it.N), 0)) {
           // edge tile: keys at or past lim are invisible to this row
           const int lim = (p.causal ? min(it.M, diag + 1) : it.M) - j * BK - hf * HALF;
 #pragma unroll
