@@ -114,7 +114,9 @@ struct Fp4Params {
   const VarSeq *seq;
 };
 
-template <int D, bool kPing, bool kVar>
+// kSmoothQ: Q smoothing on (dS on CUDA cores, added to the scores); an
+// instance of its own, so the others carry none of its code in their loops
+template <int D, bool kPing, bool kVar, bool kSmoothQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fp4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Fp4Params p) {
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int last_row = min(Nq, row0 + 128) - 1;
   const int Tn = kVar ? (Mk + BK - 1) / BK : p.Tn;
   const int T = p.causal ? min(Tn, (last_row + Mk - Nq) / BK + 1) : Tn;
-  const bool smooth_q = (p.flags & SAGE_SMOOTH_Q) != 0;
+  constexpr bool smooth_q = kSmoothQ;
   const bool direct = (p.flags & SAGE_P_DIRECT) != 0;  // phi on P~ itself (ablation)
 
   if (threadIdx.x == 0) {
@@ -758,7 +760,7 @@ sage_status launch_t(const sage_shape &s, int causal, float sm_scale, int flags,
   p.stall = test_stall();
   p.item_tab = var.item_tab;
   p.seq = var.seq;
-  auto kern = attn_fp4_kernel<D, kPing, kVar>;
+  auto kern = (flags & SAGE_SMOOTH_Q) ? attn_fp4_kernel<D, kPing, kVar, true> : attn_fp4_kernel<D, kPing, kVar, false>;
   // the register split assumes the block launches with kLaunchRegs per thread
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SAGE_ERR_CUDA;
