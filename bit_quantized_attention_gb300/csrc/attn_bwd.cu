@@ -149,7 +149,9 @@ __device__ __forceinline__ void codes32(const uint32_t (&x)[32], float inv, uint
 }
 
 // ---------------------------------------------------------------------------- dK, dV
-template <int D>
+// kSmoothQ: Q smoothing on (its corrections are an instance of their own, so
+// the other instance carries none of their code in its loops)
+template <int D, bool kSmoothQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_doc,
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int qlo = key - (p.M - p.N);  // first query that sees this key (causal)
     bool any = false;
     // the K^ tile (read below for dS) has landed
-    bool ok = !p.smooth_q || niter == 0 || __all_sync(0xffffffffu, mbar_wait(kv_full, 0, status, 69, s_abort, p.spin));
+    bool ok = !kSmoothQ || niter == 0 || __all_sync(0xffffffffu, mbar_wait(kv_full, 0, status, 69, s_abort, p.spin));
     // The four row warps meet at named barriers; each barrier also ORs a
     // failure flag, so after a wait that gave up they all leave the loop
     // together (a warp leaving alone would strand the others at a barrier).
@@ -290,12 +292,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q = i * 128 + c;
         s_lse[c] = q < p.N ? p.lse[(size_t)bh * p.N_pad + q] * kLog2e : 0.0f;
         s_D[c] = q < p.N ? p.drow[(size_t)bh * p.N_pad + q] : 0.0f;
-        if (p.smooth_q && c < D) s_qb[c] = qbar_i[c];
+        if (kSmoothQ && c < D) s_qb[c] = qbar_i[c];
       }
       if (named_bar_any(kBarRows, 128, !ok || *s_abort)) break;
       const float dqs = p.dq[(size_t)bh * p.Tm + i], sdo = p.dos[(size_t)bh * p.Tm + i];
       const float k1 = dqs * dkc * p.sm_log2;
-      const float ds2 = p.smooth_q ? qbar_dot_row<D>(sK, s_qb, c) * dkc * p.sm_log2 : 0.0f;
+      const float ds2 = kSmoothQ ? qbar_dot_row<D>(sK, s_qb, c) * dkc * p.sm_log2 : 0.0f;
       ok = __all_sync(0xffffffffu, mbar_wait(s_full, n & 1, status, 70, s_abort, p.spin));
       tc_fence_after();
       float pm = 0.0f, sm = 0.0f, cs = 0.0f;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // q_bar from global memory here (the shared copy may already hold the next block's)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 qb4 = p.smooth_q ? __ldg(reinterpret_cast<const float4 *>(qbar_i + ch * 32 + e))
+          const float4 qb4 = kSmoothQ ? __ldg(reinterpret_cast<const float4 *>(qbar_i + ch * 32 + e))
                                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           const float qv[4] = {qb4.x, qb4.y, qb4.z, qb4.w};
 #pragma unroll
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------- dQ
-template <int D>
+template <int D, bool kSmoothQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
-  if (p.smooth_q && threadIdx.x < D) s_qb[threadIdx.x] = p.qbar[((size_t)bh * p.Tm + i) * D + threadIdx.x];
+  if (kSmoothQ && threadIdx.x < D) s_qb[threadIdx.x] = p.qbar[((size_t)bh * p.Tm + i) * D + threadIdx.x];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int s = j & 1;
       const float dk0 = p.dk[(size_t)hk * p.Tn + 2 * j];
       const float dk1 = 2 * j + 1 < p.Tn ? p.dk[(size_t)hk * p.Tn + 2 * j + 1] : 0.0f;
-      if (p.smooth_q) {
+      if (kSmoothQ) {
         // dS of key r of the tile, shared with every row through shared memory
         ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j >> 1) & 1, status, 90, s_abort, p.spin));
         if (ok) s_ds[s * 128 + r] = qbar_dot_row<D>(sK + s * C::T128, s_qb, r) * (r < 64 ? dk0 : dk1) * p.sm_log2;
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const int key = j * 128 + ch * 32 + e;
           const bool vis = q_ok && key < p.M && (!p.causal || key <= diag);
-          const float ds2 = p.smooth_q ? s_ds[s * 128 + ch * 32 + e] : 0.0f;
+          const float ds2 = kSmoothQ ? s_ds[s * 128 + ch * 32 + e] : 0.0f;
           const float pr = vis ? ex2_approx(fmaf(__uint_as_float(v[e]), k1, ds2) - lse2) : 0.0f;
           const float dsv = vis ? pr * (__uint_as_float(w[e]) - Dq) : 0.0f;
           rs += dsv;
@@ -716,8 +718,8 @@ sage_status launch_bwd_t(const sage_shape &s, int causal, float sm_scale, int fl
   p.spin = spin_limit_cycles();
   const int smem_a = 1024 + 5 * C::T128 + 2 * C::PT + (256 + D + 8) * 4 + 128;
   const int smem_b = 1024 + 6 * C::T128 + C::PT + (256 + D + 8) * 4 + 128;
-  auto ka = bwd_dkdv_kernel<D>;
-  auto kb = bwd_dq_kernel<D>;
+  auto ka = p.smooth_q ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
+  auto kb = p.smooth_q ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
   if (cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_a) != cudaSuccess ||
       cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_b) != cudaSuccess)
     return SAGE_ERR_CUDA;
