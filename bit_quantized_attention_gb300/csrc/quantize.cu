@@ -330,6 +330,14 @@ struct QuantArgs {
   int nq, nk;  // CTA counts of the Q and K roles (V takes the rest)
 };
 
+// The exact quotients the quantizers fall back to near a rounding tie, out of
+// line: they run rarely, and inlined at every (unrolled) call site their
+// divisions would fill the pre-pass kernels' instruction footprint.
+__device__ __noinline__ float rint_div_exact(float x, float d) { return rintf(__fdiv_rn(x, d)); }
+__device__ __noinline__ uint32_t e4m3_div_exact2(float x0, float x1, float d0, float d1) {
+  return cvt_e4m3x2(__fdiv_rn(x0, d0), __fdiv_rn(x1, d1));
+}
+
 // rint(RN(x / d)) clamped to +-127, exactly as rint(__fdiv_rn(x, d)) gives it.
 // q = x * RN(1/d) is within about 1.5e-5 of x/d for |x/d| <= 127, and RN(x/d)
 // within 7.6e-6 of x/d; unless q lies within 1e-4 of a half-integer, both round
@@ -338,7 +346,7 @@ struct QuantArgs {
 __device__ __forceinline__ float int8_code(float x, float d, float rcp) {
   const float q = __fmul_rn(x, rcp);
   float c = rintf(q);
-  if (!(fabsf(fabsf(__fsub_rn(q, c)) - 0.5f) > 1e-4f)) c = rintf(__fdiv_rn(x, d));
+  if (__builtin_expect(!(fabsf(fabsf(__fsub_rn(q, c)) - 0.5f) > 1e-4f), 0)) c = rint_div_exact(x, d);
   return fminf(fmaxf(c, -127.0f), 127.0f);
 }
 
@@ -352,8 +360,8 @@ __device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float d0, flo
   const float lo = 1.0f - 0x1p-19f, hi = 1.0f + 0x1p-19f;
   const uint16_t a = cvt_e4m3x2(__fmul_rn(q0, lo), __fmul_rn(q1, lo));
   const uint16_t b = cvt_e4m3x2(__fmul_rn(q0, hi), __fmul_rn(q1, hi));
-  if (a == b && isfinite(q0) && isfinite(q1)) return a;
-  return cvt_e4m3x2(__fdiv_rn(x0, d0), __fdiv_rn(x1, d1));
+  if (__builtin_expect(a == b && isfinite(q0) && isfinite(q1), 1)) return a;
+  return (uint16_t)e4m3_div_exact2(x0, x1, d0, d1);
 }
 
 // Codes of 8 smoothed values g = fl(f - mu) with scale delta: 8 fp16 integers
@@ -753,6 +761,9 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
 }
 
+__device__ __noinline__ uint32_t e2m1_div_exact2(float x0, float x1, float d) {
+  return cvt_e2m1x2(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+}
 // E2M1 codes of RN(x0 / d), RN(x1 / d) as one byte, exactly as
 // cvt(__fdiv_rn(x, d)) gives them (same bracket argument as e4m3_code2).
 __device__ __forceinline__ uint32_t e2m1_code2(float x0, float x1, float d, float rcp) {
@@ -760,8 +771,8 @@ __device__ __forceinline__ uint32_t e2m1_code2(float x0, float x1, float d, floa
   const float lo = 1.0f - 0x1p-19f, hi = 1.0f + 0x1p-19f;
   const uint32_t a = cvt_e2m1x2(__fmul_rn(q0, lo), __fmul_rn(q1, lo));
   const uint32_t b = cvt_e2m1x2(__fmul_rn(q0, hi), __fmul_rn(q1, hi));
-  if (a == b && isfinite(q0) && isfinite(q1)) return a;
-  return cvt_e2m1x2(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+  if (__builtin_expect(a == b && isfinite(q0) && isfinite(q1), 1)) return a;
+  return e2m1_div_exact2(x0, x1, d);
 }
 
 // scale byte of a block with absolute maximum amax: E4M3(fl(amax / 6))
