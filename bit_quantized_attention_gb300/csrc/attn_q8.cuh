@@ -21,13 +21,14 @@
 //
 // GB300 mapping (the pages' Ada/Hopper register-level design is prior art):
 // a persistent CTA per SM walks its share of the work items (one query block
-// of one head each, longest causal rows first, round robin over the CTAs) with
-// 16 warps; every ring and barrier phase runs on tile counters that continue
+// of one head each: head-major, or for causal masks pairs of complementary
+// blocks of one head; round robin over the CTAs) with 16 warps; every ring and barrier phase runs on tile counters that continue
 // across items, so the next item's loads and first MMAs overlap the previous
 // item's last tiles and epilogue.
 //   warps 0-7   two warpgroups on the same 128 query rows (one row per thread,
 //               its TMEM lane); warpgroup h takes keys [h BK/2, (h+1) BK/2) of
-//               every tile: dequantize, add dS, mask, exponentials, P^ into the
+//               every tile: dequantize (adding dS where it is not folded into
+//               S), mask, exponentials, P^ into the
 //               swizzled K-major A operand of the PV MMA in shared memory.
 //               Each half publishes its own maximum at once and takes its
 //               exponentials against it, e = exp2(t - m_half); the new running
@@ -36,15 +37,19 @@
 //               before its exponentials.
 //   warps 8-11  two-level accumulation O = alpha O + R with the thread's row
 //               of O in registers, then the epilogue; with Q smoothing also
-//               dS one or two tiles ahead, off the softmax's per-tile chain:
-//               read from TMEM (one key per thread) where the tensor core
-//               computed it, else from the K^ tile in shared memory
+//               dS ahead of the softmax: read from TMEM (one key per thread)
+//               where the tensor core computed it and written as the tile's
+//               key augmentation (the correction then comes folded into S),
+//               else computed from the K^ tile in shared memory for the
+//               softmax to add
 //   warp 12     TMA producer: Q^ once, K^_j and V^T_j into a ring of stages
 //   warp 13     QK issuer: S(j) = Q^ K^_j^T (kind::f16 on INT8 codes held as
 //               exact fp16 integers -- sm_103a has no INT8 tensor path -- or
 //               kind::f8f6f4 on E4M3 codes); with Q smoothing on INT8 codes
 //               and 128-key tiles also dS^T(j) = K^_j U^T, U the item's q_bar
-//               as fp16 hi / lo rows (kind::f16, M = 128 keys, N = 16)
+//               as fp16 hi / lo rows (kind::f16, M = 128 keys, N = 16), run
+//               ahead, and S(j) starts from one kind::tf32 step
+//               [1/delta_Q rows] x [dS keys]^T of the augmentation operands
 //   warp 14     PV issuer: R(j) = P^(j) V^_j (kind::f8f6f4)
 // TMEM: three S/R regions (R of tile j overwrites S of tile j once the softmax
 // has read it), so QK runs up to three tiles ahead of the accumulation; with
