@@ -152,6 +152,33 @@ def test_host_call_checks_everything_before_its_first_copy(sage):
     assert sage.lib.sage_host_buffer_bytes(C.byref(sage.Shape(1, 3, 2, 256, 256, 64)), 0, 128, 64) == 0
 
 
+def _host_chunks(B, Hq, Hkv, N):
+    """The host call's chunking: about 512 query blocks per chunk, 6 to 24
+    chunks, whole kv-heads of one batch element each."""
+    target = max(6, min(24, B * Hq * ((N + 127) // 128) // 512))
+    per_b = max(1, min(Hkv, (target + B - 1) // B))
+    return [(b, k * Hkv // per_b, (k + 1) * Hkv // per_b) for b in range(B) for k in range(per_b)
+            if (k + 1) * Hkv // per_b > k * Hkv // per_b]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,M,d,mode,bk", [
+    (2, 48, 48, 17776, 17776, 64, 0, 128),   # the video shape: 24 chunks of 4 kv-heads
+    (4, 32, 32, 4096, 4096, 128, 0, 128),    # 8 chunks
+    (1, 32, 8, 4096, 65536, 128, 0, 128),    # the minimum of 6 chunks, uneven head counts
+    (1, 2, 2, 256, 256, 64, 2, 128),         # fewer kv-heads than chunks
+])
+def test_host_buffer_follows_the_chunking_rule(sage, B, Hq, Hkv, N, M, d, mode, bk):
+    """sage_host_buffer_bytes = the status word + q, k, v, o + two workspace
+    slots, each the largest chunk's workspace, rounded up to 1024 bytes."""
+    G = Hq // Hkv
+    al = lambda n: (n + 1023) // 1024 * 1024
+    slot = max(sage.sage_workspace_bytes(sage.Shape(1, (g1 - g0) * G, g1 - g0, N, M, d), mode, 128, bk)
+               for _, g0, g1 in _host_chunks(B, Hq, Hkv, N))
+    io = al(B * Hq * N * d * 2) * 2 + al(B * Hkv * M * d * 2) * 2
+    got = sage.lib.sage_host_buffer_bytes(C.byref(sage.Shape(B, Hq, Hkv, N, M, d)), mode, 128, bk)
+    assert got == 1024 + io + 2 * al(slot)
+
+
 def test_status_strings(sage):
     for code in range(7):
         assert sage.sage_status_str(code)
