@@ -18,6 +18,8 @@ CASES = [
     _small("host_bk64_many_chunks", B=3, Hq=12, Hkv=4, N=130, M=257, flags=5, d=64, bk=64),
     _small("host_fp8", mode=1, B=2, Hq=4, Hkv=4, N=256, M=256, flags=1, d=128, bk=128),
     _small("host_nvfp4", mode=2, B=2, Hq=4, Hkv=4, N=256, M=384, flags=1, d=128, bk=128),
+    # 96 heads x 128 query blocks = 12288 blocks: the largest chunk count (24 chunks of 4 kv heads)
+    _small("host_24_chunks", B=1, Hq=96, Hkv=96, N=16384, M=16384, flags=7, d=64, bk=128),
 ]
 
 
