@@ -169,7 +169,9 @@ sage_status sage_quantize_qkv_static_scratch(const sage_shape *shape, int quant_
  * "The Complete Algorithm", SageAttention3 summary §3.4 "FP4 Attention Kernel
  * Algorithm").  causal != 0 masks key j for query i when j > i + (M - N)
  * (bottom-right aligned; requires M >= N).  quant_mode, flags, bq and bk must
- * be those given to sage_quantize_qkv for this workspace.  Writes o (bf16). */
+ * be those given to sage_quantize_qkv for this workspace.  Writes o (bf16).
+ * SAGE_ERR_UNSUPPORTED for a causal INT8 / FP8 request of 2^24 or more query
+ * blocks (B * Hq * ceil(N / 128)), whose work order the kernel cannot form. */
 sage_status sage_attn_fwd(const sage_shape *shape, int causal, float sm_scale, int quant_mode,
                           int flags, int bq, int bk, const void *workspace, size_t workspace_bytes,
                           void *o, sage_stream_t stream);
